@@ -1,0 +1,82 @@
+"""The 2-layer single-head decoder of [LCP5], float64.
+
+[LCP5] section "27 例得到的计算量与误差" fixes: two layers, one head, width
+16, vocabulary 32, float64, sinusoidal absolute positions, tanh residual, no
+training, no FFN, no LayerNorm.  The architecture itself belongs to an earlier
+article of that series and is not printed, so this module takes the plainest
+reading (listed in the design doc):
+
+* h = E[id] + PE(position), PE the sinusoid of "Attention Is All You Need":
+  PE[p, 2i] = sin(p / 10000**(2i/d)), PE[p, 2i+1] = cos(p / 10000**(2i/d));
+* per layer: q, k, v = h Wq, h Wk, h Wv (16 x 16), a = causal softmax(q k^T
+  / sqrt(16)) v, h <- h + tanh(a Wo);
+* the output is the final hidden state of every computed row;
+* weights ~ N(0, 1/16) drawn from numpy ``default_rng(seed)`` in the order
+  E, then (Wq, Wk, Wv, Wo) of layer 0, then of layer 1.  No RoPE.
+
+The cache is the dict of the truncation listing under "哪些东西必须一起裁剪":
+{'next_position': int, 'layers': [(k [T, d], v [T, d], positions [T])]}.
+"""
+
+import math
+
+import numpy as np
+
+from .attention import causal_attention
+
+
+def sinusoidal_positions(positions, d):
+    """Additive sinusoidal position rows [len(positions), d]."""
+    pos = np.asarray(positions, dtype=np.float64)[:, None]
+    i = np.arange(0, d, 2, dtype=np.float64)[None, :]
+    ang = pos / np.power(10000.0, i / d)
+    pe = np.zeros((pos.shape[0], d))
+    pe[:, 0::2] = np.sin(ang)
+    pe[:, 1::2] = np.cos(ang)
+    return pe
+
+
+class ToyDecoder:
+    def __init__(self, seed, d=16, vocab=32, layers=2):
+        rng = np.random.default_rng(seed)
+        std = math.sqrt(1.0 / 16.0)
+        self.d, self.vocab, self.n_layers = d, vocab, layers
+        self.E = rng.normal(0.0, std, (vocab, d))
+        self.W = [tuple(rng.normal(0.0, std, (d, d)) for _ in range(4)) for _ in range(layers)]
+
+    def embed(self, ids, positions):
+        return self.E[np.asarray(ids, dtype=np.int64)] + sinusoidal_positions(positions, self.d)
+
+    def project(self, layer, h):
+        Wq, Wk, Wv, _ = self.W[layer]
+        return h @ Wq, h @ Wk, h @ Wv
+
+    def mix(self, layer, h, attn):
+        return h + np.tanh(attn @ self.W[layer][3])
+
+    def forward_full(self, ids):
+        """Uncached forward of every row; returns (hidden [n, d], cache dict)."""
+        return self.chunk(ids, {"next_position": 0,
+                                "layers": [(np.zeros((0, self.d)), np.zeros((0, self.d)),
+                                            np.zeros(0, dtype=np.int64))] * self.n_layers})
+
+    def chunk(self, ids, cache):
+        """Continue from ``cache``: rows at positions next_position, ... .
+
+        Returns (hidden states of the new rows [n, d], the extended cache).
+        Slots of the new rows follow the retained rows; row i attends the
+        retained slots and new rows 0..i.
+        """
+        n = len(ids)
+        start = int(cache["next_position"])
+        positions = start + np.arange(n)
+        h = self.embed(ids, positions)
+        new_layers = []
+        for layer, (kc, vc, pc) in enumerate(cache["layers"]):
+            q, k, v = self.project(layer, h)
+            K = np.concatenate([kc, k], axis=0)
+            V = np.concatenate([vc, v], axis=0)
+            a = causal_attention(q, K, V, kc.shape[0] + np.arange(n))
+            h = self.mix(layer, h, a)
+            new_layers.append((K, V, np.concatenate([pc, positions])))
+        return h, {"next_position": start + n, "layers": new_layers}
