@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Throughput of cached incremental attention on GB300 through libkvc's C ABI.
+
+Workloads (seeded, synthetic; sizes as the pages' workloads are stated):
+
+* mha_decode (default, headline): B = 32, H = 32, d_h = 128, bf16, C = 8192,
+  old lengths uniform in [1, 8128], 64 decode steps.  One bench step =
+  kvc_truncate back to the old lengths + 64 kvc_append_attend calls.  Metric:
+  K/V bytes the attention must read (every retained row of every lane at every
+  decode step) per second.
+* gqa_decode / mqa_decode: B = 64, H_q = 32, H_kv = 8 / 1, C = 32768, old
+  lengths uniform in [16384, 32736], 32 decode steps.
+* suffix: B = 8, H = 32, d_h = 128, 16384 cached tokens with one edited id
+  each + 512 appended: one bench step = kvc_lcp per sequence + kvc_truncate +
+  kvc_prefill_suffix of the suffix chunk.  Metric: TFLOP/s of the unmasked
+  QK^T and PV work.
+
+Every step reads far more than the 129 MB L2 (2.2 GB of K/V per MHA decode
+step), so no L2 flush is inserted.  `value` is device-timed with inputs
+resident in HBM; `e2e` repeats the measurement through the same C-ABI calls
+with the per-step inputs copied from pinned host memory and the outputs
+copied back inside the timed region.  `roofline` times the dominant kernel
+with CUDA events recorded by the library around each launch on its stream.
+`cpu_baseline` times the float64 oracle on a bounded sample on the host.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="mha_decode",
+                   choices=["mha_decode", "gqa_decode", "mqa_decode", "suffix", "all"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids) and ids[local_rank].strip().isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------- decode workloads
+
+class DecodeBench:
+    def __init__(self, name, device):
+        from kv_cache_append_rope_gb300 import workloads as W
+        from kv_cache_append_rope_gb300.kvc import KVCache
+        cfg = dict(W.CONFIGS[name])
+        self.name, self.cfg, self.device = name, cfg, device
+        B, Hq, Hkv, D, C, steps = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["C"], cfg["steps"]
+        self.L0 = W.old_lengths(cfg["seed"], B, cfg["lo"], cfg["hi"], C, steps)
+        self.cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype="bf16", rope_base=10000.0,
+                             device=device.index or 0)
+        S = int(self.L0.max())
+        seed = cfg["seed"] * 1000
+        # unrotated prefix rows (kept for the oracle sample), appended without attending
+        self.k_prefix = W.normal((B, Hkv, S, D), seed + 1, device=device)
+        self.v_prefix = W.normal((B, Hkv, S, D), seed + 2, device=device)
+        self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, seqlen=self.L0.tolist(), out=False)
+        self.q = W.normal((steps, B, Hq, 1, D), seed + 3, device=device)
+        self.k = W.normal((steps, B, Hkv, 1, D), seed + 4, device=device)
+        self.v = W.normal((steps, B, Hkv, 1, D), seed + 5, device=device)
+        self.out = torch.empty((steps, B, Hq, 1, D), dtype=torch.float32, device=device)
+        torch.cuda.synchronize(device)
+        # algorithmic K/V bytes read by attention over the 64 steps: every lane reads t rows of K and V
+        t = self.L0[None, :] + 1 + np.arange(steps)[:, None]          # [steps, B]
+        self.kv_bytes_per_call = (t.sum(axis=1) * Hkv * D * 2 * 2).astype(np.float64)
+        self.kv_bytes = float(self.kv_bytes_per_call.sum())
+        # everything else the step must move: q/k/v rows in, new K/V rows written, outputs out
+        self.io_bytes = float(steps * B * (Hq * D * 2 + 2 * Hkv * D * 2 + 2 * Hkv * D * 2 + Hq * D * 4))
+        self.steps = steps
+
+    def step(self):
+        self.cache.truncate(self.L0.tolist())
+        for i in range(self.steps):
+            self.cache.append_attend(0, self.q[i], self.k[i], self.v[i], out=self.out[i])
+
+    def e2e_setup(self):
+        self.hq = self.q.cpu().pin_memory()
+        self.hk = self.k.cpu().pin_memory()
+        self.hv = self.v.cpu().pin_memory()
+        self.hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        self.dq = torch.empty_like(self.q[0])
+        self.dk = torch.empty_like(self.k[0])
+        self.dv = torch.empty_like(self.v[0])
+        self.h2d = (self.hq.nbytes + self.hk.nbytes + self.hv.nbytes)
+        self.d2h = self.hout.nbytes
+
+    def e2e_step(self):
+        self.cache.truncate(self.L0.tolist())
+        for i in range(self.steps):
+            self.dq.copy_(self.hq[i], non_blocking=True)
+            self.dk.copy_(self.hk[i], non_blocking=True)
+            self.dv.copy_(self.hv[i], non_blocking=True)
+            self.cache.append_attend(0, self.dq, self.dk, self.dv, out=self.out[i])
+            self.hout[i].copy_(self.out[i], non_blocking=True)
+
+    def dominant(self):
+        return "decode"
+
+    def dominant_algorithmic(self, launches):
+        """Algorithmic bytes of `launches` decode-kernel launches (cycling through the 64 steps)."""
+        reps, rem = divmod(launches, self.steps)
+        return reps * self.kv_bytes + float(self.kv_bytes_per_call[:rem].sum())
+
+    def units(self, n_steps):
+        return n_steps * self.kv_bytes / 1e9, "GB/s"
+
+    def config(self):
+        c = self.cfg
+        return {"workload": self.name, "B": c["B"], "H_q": c["Hq"], "H_kv": c["Hkv"], "d_h": c["D"], "C": c["C"],
+                "decode_steps_per_step": c["steps"], "old_length_range": [int(self.L0.min()), int(self.L0.max())],
+                "old_length_rule": f"uniform integers in [{c['lo']}, min({c['hi']}, C - steps)] from seed {c['seed']}",
+                "l2": "inputs larger than L2: each decode step streams "
+                      f"{self.kv_bytes / self.steps / 1e9:.2f} GB of K/V (L2 is 0.129 GB)"}
+
+    def oracle_sample(self, budget_s=15.0):
+        """Oracle decode of sampled lanes (all steps); returns (seconds, bytes, description)."""
+        from oracle import attention as A
+        c = self.cfg
+        B, G = c["B"], c["Hq"] // c["Hkv"]
+        order = np.argsort(self.L0)
+        lanes = [int(order[0]), int(order[-1])] + [int(b) for b in order[1:-1][::max(1, B // 6)]]
+        done_bytes, t_total, n = 0.0, 0.0, 0
+        for b in lanes:
+            L0 = int(self.L0[b])
+            hk = 0
+            k = np.concatenate([self.k_prefix[b, hk, :L0].double().cpu().numpy(),
+                                self.k[:, b, hk, 0].double().cpu().numpy()])[None]
+            v = np.concatenate([self.v_prefix[b, hk, :L0].double().cpu().numpy(),
+                                self.v[:, b, hk, 0].double().cpu().numpy()])[None]
+            q = self.q[:, b, hk * G:(hk + 1) * G, 0].double().cpu().numpy()
+            t0 = time.perf_counter()
+            A.decode_steps_reference(q, k, v, L0, 10000.0, "bf16")
+            t_total += time.perf_counter() - t0
+            done_bytes += float(((L0 + 1 + np.arange(self.steps)) * c["D"] * 2 * 2).sum())
+            n += 1
+            if t_total > budget_s:
+                break
+        return t_total, done_bytes, f"{n} (b, kv-head) lanes x {self.steps} decode steps (all {G} query heads each)"
+
+
+# ----------------------------------------------------------------- suffix workload
+
+class SuffixBench:
+    def __init__(self, device):
+        from kv_cache_append_rope_gb300 import workloads as W
+        from kv_cache_append_rope_gb300.kvc import KVCache
+        c = dict(W.CONFIGS["suffix"])
+        self.cfg, self.device = c, device
+        B, H, D = c["B"], c["Hq"], c["D"]
+        self.T = c["prefix"] + c["appended"]
+        self.cached, self.query, self.edit = W.edited_histories(c["seed"], B, c["prefix"], c["appended"], c["vocab"])
+        self.cache = KVCache(B, H, self.T, D, dtype="bf16", rope_base=10000.0, device=device.index or 0)
+        seed = c["seed"] * 1000
+        self.k_prefix = W.normal((B, H, c["prefix"], D), seed + 1, device=device)
+        self.v_prefix = W.normal((B, H, c["prefix"], D), seed + 2, device=device)
+        self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, out=False)
+        from kv_cache_append_rope_gb300 import kvc
+        self.cuts = [kvc.lcp(self.cached[b].tolist(), self.query[b].tolist()) for b in range(B)]
+        self.S = self.T - min(self.cuts)
+        self.q = W.normal((B, H, self.S, D), seed + 3, device=device)
+        self.k = W.normal((B, H, self.S, D), seed + 4, device=device)
+        self.v = W.normal((B, H, self.S, D), seed + 5, device=device)
+        self.out = torch.empty((B, H, self.S, D), dtype=torch.float32, device=device)
+        self.seqlen = [self.T - cu for cu in self.cuts]
+        self.flops = float(sum(H * 4 * D * (s * cu + s * (s + 1) / 2) for s, cu in zip(self.seqlen, self.cuts)))
+        torch.cuda.synchronize(device)
+
+    def step(self):
+        from kv_cache_append_rope_gb300 import kvc
+        cuts = [kvc.lcp(self.cached[b], self.query[b]) for b in range(self.cfg["B"])]
+        self.cache.truncate(cuts)
+        self.cache.prefill_suffix(0, self.q, self.k, self.v, seqlen=self.seqlen, out=self.out)
+
+    def e2e_setup(self):
+        self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
+        self.hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        self.dq, self.dk, self.dv = (torch.empty_like(x) for x in (self.q, self.k, self.v))
+        self.h2d = self.hq.nbytes + self.hk.nbytes + self.hv.nbytes
+        self.d2h = self.hout.nbytes
+
+    def e2e_step(self):
+        from kv_cache_append_rope_gb300 import kvc
+        cuts = [kvc.lcp(self.cached[b], self.query[b]) for b in range(self.cfg["B"])]
+        self.cache.truncate(cuts)
+        self.dq.copy_(self.hq, non_blocking=True)
+        self.dk.copy_(self.hk, non_blocking=True)
+        self.dv.copy_(self.hv, non_blocking=True)
+        self.cache.prefill_suffix(0, self.dq, self.dk, self.dv, seqlen=self.seqlen, out=self.out)
+        self.hout.copy_(self.out, non_blocking=True)
+
+    def dominant(self):
+        return "suffix" if self.cache.kernel_stats("suffix")[1] else "generic_attend"
+
+    def dominant_algorithmic(self, launches):
+        return launches * self.flops
+
+    def units(self, n_steps):
+        return n_steps * self.flops / 1e12, "TFLOP/s"
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "suffix", "B": c["B"], "H": c["Hq"], "d_h": c["D"], "prefix_tokens": c["prefix"],
+                "appended_tokens": c["appended"], "C": self.T, "cuts": self.cuts,
+                "flops_per_step": self.flops,
+                "l2": "inputs larger than L2: the K/V prefix alone is "
+                      f"{self.k_prefix.nbytes * 2 / 1e9:.1f} GB"}
+
+    def oracle_sample(self, budget_s=15.0):
+        from oracle import attention as A
+        b, h = int(np.argmax(self.cuts)), 0
+        cut = self.cuts[b]
+        S = self.seqlen[b]
+        rows = np.arange(0, S, max(1, S // 64))[:64]
+        k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(), self.k[b, h, :S].double().cpu().numpy()])
+        v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(), self.v[b, h, :S].double().cpu().numpy()])
+        q = self.q[b, h:h + 1, :S].double().cpu().numpy()
+        t0 = time.perf_counter()
+        A.suffix_reference(q, k[None], v[None], np.arange(self.T), cut, 10000.0, "bf16", rows=rows)
+        dt = time.perf_counter() - t0
+        flops = float(sum(4 * self.cfg["D"] * (cut + r + 1) for r in rows))
+        return dt, flops, f"{rows.size} suffix rows of one (b, h) lane against the full masked prefix"
+
+
+# ----------------------------------------------------------------- driver
+
+def make_bench(name, device):
+    return SuffixBench(device) if name == "suffix" else DecodeBench(name, device)
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_threads():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def run_ours(args, name, world, rank, local):
+    from kv_cache_append_rope_gb300 import _lib as L
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    hbm, tflops, peak_kind = peaks()
+    bench = make_bench(name, device)
+    cache = bench.cache
+    for _ in range(args.warmup):
+        bench.step()
+    torch.cuda.synchronize(device)
+    cache.reset_stats()
+    cache.set_option(L.OPT_TIMING, 1)
+    stream = torch.cuda.current_stream(device)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(gpu_index(local)) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            bench.step()
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world)
+    dom = bench.dominant()
+    dom_ms, dom_launches = cache.kernel_stats(dom)
+    _, launches = cache.kernel_stats(-1)
+    cache.set_option(L.OPT_TIMING, 0)
+    units, unit = bench.units(args.steps)
+    value = units * world / (ms / 1e3)
+    per_step_ms = ms / args.steps
+
+    # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / event-timed duration
+    alg = bench.dominant_algorithmic(dom_launches)
+    if unit == "GB/s":
+        achieved = alg / 1e9 / (dom_ms / 1e3)
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None, "kernel": "decode_bf16_kernel",
+                "peak_source": f"{peak_kind} hbm_gbs", "kernel_ms_per_launch": round(dom_ms / dom_launches, 5),
+                "algorithmic_bytes_per_launch": round(alg / dom_launches)}
+    else:
+        achieved = alg / 1e12 / (dom_ms / 1e3)
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(achieved / tflops, 4), "traffic": None, "kernel": dom,
+                "peak_source": f"{peak_kind} bf16_tflops (burst)", "kernel_ms_per_launch": round(dom_ms / dom_launches, 3),
+                "algorithmic_flops_per_launch": round(alg / dom_launches)}
+
+    e2e = None
+    if not args.no_e2e:
+        bench.e2e_setup()
+        for _ in range(max(1, args.warmup)):
+            bench.e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            bench.e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": round(units * world / e2e_s, 2), "unit": unit, "h2d_bytes_per_step": int(bench.h2d),
+               "d2h_bytes_per_step": int(bench.d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, work, sample = bench.oracle_sample()
+        cpu = {"value": round(work / (1e9 if unit == "GB/s" else 1e12) / secs, 6), "unit": unit,
+               "cores": cpu_threads(), "kind": "oracle", "sample": sample, "seconds": round(secs, 2)}
+
+    cache.check()
+    line = {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(per_step_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": bench.config(), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clocks.summary()}
+    if unit == "GB/s":
+        line["hbm_peak_frac"] = round(value / world / hbm, 4)
+        line["decode_steps_per_s"] = round(bench.steps * args.steps * world / (ms / 1e3), 1)
+    else:
+        line["tensor_peak_frac"] = round(value / world / tflops, 4)
+        line["steps_per_s"] = round(args.steps / (ms / 1e3), 3)
+    return line
+
+
+def run_reference(args, name):
+    """The oracle as the reference arm: each step a bounded sample of the same workload."""
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    if device is None:
+        return {"impl": "reference", "unavailable": "the workload inputs are generated on a CUDA device"}
+    bench = make_bench(name, device)
+    budget = 20.0 / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        bench.oracle_sample(budget)
+    secs, work, sample = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        s, w, sample = bench.oracle_sample(budget)
+        secs += s
+        work += w
+    units, unit = bench.units(1)
+    scale = 1e9 if unit == "GB/s" else 1e12
+    value = work / scale / secs
+    cpu = {"value": round(value, 6), "unit": unit, "cores": cpu_threads(), "kind": "oracle", "sample": sample}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": bench.config(), "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:
+        return                                   # the oracle arm runs on rank 0 only
+    world, rank, local = dist_setup(args) if args.impl == "ours" else (1, 0, 0)
+    names = ["mha_decode", "gqa_decode", "mqa_decode", "suffix"] if args.workload == "all" else [args.workload]
+    for name in names:
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps(run_reference(args, name)), flush=True)
+            continue
+        line = run_ours(args, name, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

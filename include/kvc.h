@@ -1,0 +1,267 @@
+/*
+ * kvc.h -- C ABI of libkvc: cached incremental causal attention with RoPE on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section (or listing title):
+ *   [Ch37] "Keep the prefix, project only the new row", learn_llm course,
+ *          chapter 37 (intale.github.io/learn_llm/en/course/37-incremental-attention/)
+ *   [LCP5] "LLM 机制实验（五）：改了历史，能否只重算变化的后缀？"
+ *          (huhohoo.com/docs/llm/longest-prefix-reuse)
+ *
+ * Model.  A handle owns, for every layer, fixed-capacity key and value
+ * buffers laid out [B, H_kv, C, d_h] in the storage dtype, a per-slot position
+ * array [B, C] (int32), and per-sequence logical length and next position
+ * (int32 [B]).  Rows are appended along the slot axis ([Ch37] "Append along
+ * the position axis"); the key is stored rotated (RoPE at its absolute
+ * position), the value unrotated, the query is never stored.
+ *
+ * Conventions shared by every entry point:
+ *   - Device memory.  Tensor data pointers passed in kvc_tensor are DEVICE
+ *     pointers (cudaMalloc / torch CUDA tensors), contiguous row-major, owned
+ *     by the caller and only read (inputs) or written (outputs) during the
+ *     call's stream work.  The handle owns its cache storage and scratch.
+ *   - Host memory.  Plain int32_t* arguments (cut, start_pos, seqlen, ids,
+ *     lengths) are HOST pointers, read before the call returns.
+ *   - Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream).  Work is enqueued asynchronously; calls on one handle
+ *     must be issued from one host thread and in stream order.
+ *   - Errors.  Every argument, shape, dtype, capacity and position check runs
+ *     on the host, against host mirrors of the lengths, BEFORE any work is
+ *     enqueued; a call that returns an error has changed neither storage nor
+ *     lengths ([Ch37] "Reset or reject without corrupting retained state").
+ *     kvc_last_error() gives the message of the handle's last failure.
+ *   - Dtypes.  Inputs q, k, v carry the storage dtype.  Outputs are f32 for
+ *     bf16 and f32 storage and f64 for f64 storage.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+
+typedef enum kvc_status {
+    KVC_OK = 0,
+    KVC_ERR_NULL = 1,                       /* a required pointer is NULL */
+    KVC_ERR_ZERO_BATCH = 2,                 /* batch size 0 */
+    KVC_ERR_ZERO_CAPACITY = 3,              /* capacity 0 */
+    KVC_ERR_CAPACITY_EXCEEDS_POSITIONS = 4, /* capacity > RoPE position capacity */
+    KVC_ERR_ELEMENT_OVERFLOW = 5,           /* B*H*C*d_h (or a byte count) overflows */
+    KVC_ERR_ALLOC = 6,                      /* device allocation failed */
+    KVC_ERR_FULL = 7,                       /* an append would pass capacity C */
+    KVC_ERR_KEY_SHAPE = 8,                  /* key tensor shape / rank mismatch */
+    KVC_ERR_VALUE_SHAPE = 9,                /* value tensor shape / rank mismatch */
+    KVC_ERR_QUERY_SHAPE = 10,               /* query shape mismatch, or not a single token */
+    KVC_ERR_OUTPUT_SHAPE = 11,              /* output shape mismatch */
+    KVC_ERR_DTYPE = 12,                     /* tensor dtype differs from the handle's */
+    KVC_ERR_LAYER = 13,                     /* layer index out of range */
+    KVC_ERR_NONFINITE_KEY = 14,             /* checked mode: NaN/Inf in the appended key */
+    KVC_ERR_NONFINITE_VALUE = 15,           /* checked mode: NaN/Inf in the appended value */
+    KVC_ERR_CUT = 16,                       /* cut < 0 or cut > current length */
+    KVC_ERR_EMPTY_QUERY = 17,               /* empty token-id query */
+    KVC_ERR_POSITION = 18,                  /* a RoPE position outside [0, max_positions) */
+    KVC_ERR_CONFIG = 19,                    /* invalid geometry or option */
+    KVC_ERR_CUDA = 20,                      /* a CUDA runtime call failed (no device, ...) */
+    KVC_ERR_DEVICE = 21                     /* a kernel reported a fault or a timed-out wait */
+} kvc_status;
+
+typedef enum kvc_dtype {
+    KVC_BF16 = 0,
+    KVC_F32 = 1,
+    KVC_F64 = 2
+} kvc_dtype;
+
+/* Geometry and numerics of a cache ([Ch37] "Keep layer, logical length, and
+ * capacity separate"; the RoPE configuration is captured at construction as in
+ * the listing "Own a fixed layer-bound cache, append one checked row, and
+ * reset logical length"). */
+typedef struct kvc_config {
+    int32_t batch;              /* B >= 1 sequences */
+    int32_t heads_q;            /* H_q >= 1 query heads */
+    int32_t heads_kv;           /* H_kv >= 1 key/value heads, divides H_q (query head h reads h / (H_q/H_kv)) */
+    int32_t capacity;           /* C >= 1 slots per sequence and layer */
+    int32_t head_dim;           /* d_h, even, 2 .. 256 */
+    int32_t layers;             /* >= 1 independent layer caches */
+    int32_t dtype;              /* kvc_dtype of storage and of q/k/v inputs */
+    int32_t rope_max_positions; /* RoPE table size; 0 means C; must be >= C */
+    double rope_base;           /* > 0: theta_j = base^(-2j/d_h); 0: no rotation */
+    int32_t checked;            /* nonzero: reject NaN/Inf keys and values (adds a device sync per call) */
+    int32_t device;             /* CUDA device ordinal */
+} kvc_config;
+
+/* A contiguous row-major tensor on the device.  ndim <= 4. */
+typedef struct kvc_tensor {
+    void* data;
+    int32_t dtype;              /* kvc_dtype */
+    int32_t ndim;
+    int64_t shape[4];
+} kvc_tensor;
+
+typedef struct kvc_handle kvc_handle;
+
+/* ABI version of the loaded library (KVC_ABI_VERSION). */
+int32_t kvc_abi_version(void);
+
+/* Static text for a status code. */
+const char* kvc_status_string(kvc_status status);
+
+/* Message of the last failed call on `h` (empty string if none).  With h ==
+ * NULL: the last failure of kvc_create / kvc_create_ex on this thread. */
+const char* kvc_last_error(const kvc_handle* h);
+
+/*
+ * kvc_create: a cache with H_q = H_kv = heads, bf16 storage, RoPE base 10000,
+ * rope_max_positions = capacity, unchecked, device 0.
+ * kvc_create_ex: any configuration.
+ * [Ch37] listing "Own a fixed layer-bound cache, append one checked row, and
+ * reset logical length" (construction): batch 0 -> KVC_ERR_ZERO_BATCH,
+ * capacity 0 -> KVC_ERR_ZERO_CAPACITY, capacity > rope_max_positions ->
+ * KVC_ERR_CAPACITY_EXCEEDS_POSITIONS, element-count overflow ->
+ * KVC_ERR_ELEMENT_OVERFLOW, device allocation failure -> KVC_ERR_ALLOC.
+ * Storage is zero-filled; every length and next position starts at 0.  On
+ * success *out owns all device memory until kvc_destroy.  On failure *out is
+ * set to NULL and nothing is allocated.
+ */
+kvc_status kvc_create(int32_t batch, int32_t heads, int32_t capacity, int32_t head_dim,
+                      int32_t layers, kvc_handle** out);
+kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out);
+
+/* Frees every device and host resource of `h` (NULL is a no-op).  The caller
+ * must ensure no enqueued work on the handle is still running. */
+void kvc_destroy(kvc_handle* h);
+
+/*
+ * One decode step of one layer for all B sequences ([Ch37] "Predict the third
+ * result before running the example", "Append along the position axis" and the
+ * listing "Evaluate one newest query across the retained rows plus the
+ * candidate key/value row before committing the append").
+ *   q   [B, H_q, 1, d_h]   the new query rows (unrotated), storage dtype
+ *   k   [B, H_kv, 1, d_h]  the new key rows (unrotated)
+ *   v   [B, H_kv, 1, d_h]  the new value rows
+ *   out [B, H_q, 1, d_h]   f32 (bf16/f32 storage) or f64 (f64 storage)
+ * For each sequence b with old length n_b and next position p_b (p_b == n_b
+ * except after a deliberately stale prefill): q and k are rotated at p_b; the
+ * rotated key (rounded once to the storage dtype) and the value are written to
+ * slot n_b, positions[b][n_b] = p_b; the new query of every head attends slots
+ * 0 .. n_b with scores q.k/sqrt(d_h) and a max-subtracted softmax; then
+ * n_b += 1 and p_b += 1.
+ * Errors (no state change): KVC_ERR_LAYER, KVC_ERR_NULL, KVC_ERR_DTYPE,
+ * KVC_ERR_QUERY_SHAPE (including more than one token), KVC_ERR_KEY_SHAPE,
+ * KVC_ERR_VALUE_SHAPE, KVC_ERR_OUTPUT_SHAPE, KVC_ERR_FULL (some n_b == C),
+ * KVC_ERR_POSITION (some p_b >= rope_max_positions), and in checked mode
+ * KVC_ERR_NONFINITE_KEY / KVC_ERR_NONFINITE_VALUE.
+ */
+kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q,
+                             const kvc_tensor* k, const kvc_tensor* v,
+                             const kvc_tensor* out, void* stream);
+
+/*
+ * Append a chunk of rows per sequence and attend it causally against the
+ * retained prefix plus the chunk ([LCP5] section "先看一次历史编辑": with the
+ * same configuration and positions the prefix rows do not depend on later
+ * tokens; listing under "哪些东西必须一起裁剪": continue from position cut).
+ *   q   [B, H_q, S, d_h], k and v [B, H_kv, S, d_h]: row i < seqlen[b] of
+ *       sequence b is new row i; rows >= seqlen[b] are ignored (padding).
+ *       q may be NULL when out is NULL (append only).
+ *   start_pos [B] host: position of row 0 (NULL -> each sequence's next
+ *       position, the normal path; a different value is accepted and recorded,
+ *       which is how a stale-position negative control is run).
+ *   seqlen [B] host: rows per sequence, 0 .. S (NULL -> S for all).
+ *   out [B, H_q, S, d_h] f32/f64, or NULL to append without attending
+ *       (prefill of a prefix).  Rows >= seqlen[b] of out are left untouched.
+ * Row i of sequence b goes to slot n_b + i with position start_pos[b] + i;
+ * its query attends slots 0 .. n_b + i (the mask is by slot).  Afterwards
+ * n_b += seqlen[b] and p_b = start_pos[b] + seqlen[b].
+ * Errors as kvc_append_attend, plus KVC_ERR_FULL when n_b + seqlen[b] > C and
+ * KVC_ERR_POSITION when a position leaves [0, rope_max_positions).
+ */
+kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
+                              const kvc_tensor* k, const kvc_tensor* v,
+                              const int32_t* start_pos, const int32_t* seqlen,
+                              const kvc_tensor* out, void* stream);
+
+/*
+ * [Ch37] "Keep layer, logical length, and capacity separate" / "Reset or reject
+ * without corrupting retained state": every layer's length and next position
+ * become 0.  Storage, positions, capacity and allocation are unchanged.
+ */
+kvc_status kvc_reset(kvc_handle* h, void* stream);
+
+/*
+ * [LCP5] listing under "哪些东西必须一起裁剪": for every layer and sequence b,
+ * keep rows < cut[b] and set length = next position = cut[b].
+ * cut [B] host.  KVC_ERR_CUT (no state change) if some cut[b] < 0 or
+ * cut[b] > the current length of sequence b in any layer.
+ */
+kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream);
+
+/*
+ * [LCP5] "先看一次历史编辑" and "查询流程与缓存所有权": cut = min(L, m - 1),
+ * L the length of the run of equal ids from index 0 of cached[0..n) and
+ * query[0..m).  Host only, no device.  n == 0 gives cut 0; m <= 0 ->
+ * KVC_ERR_EMPTY_QUERY; NULL arrays (with a non-zero length) -> KVC_ERR_NULL.
+ */
+kvc_status kvc_lcp(const int32_t* cached, int64_t n, const int32_t* query, int64_t m,
+                   int32_t* cut);
+
+/* Host mirrors of one layer's lengths and next positions, each [B] host
+ * (either may be NULL). */
+kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
+                           int32_t* next_positions);
+
+/* The handle's configuration (rope_max_positions resolved). */
+kvc_status kvc_get_config(const kvc_handle* h, kvc_config* out);
+
+/* Device pointers of one layer's storage, for audits: keys and values
+ * [B, H_kv, C, d_h] storage dtype, positions [B, C] int32.  Owned by the
+ * handle; valid until kvc_destroy.  Any output pointer may be NULL. */
+kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** values,
+                       int32_t** positions);
+
+/*
+ * Synchronises `stream`, then checks the device side: the kernels' error word
+ * (a bounded wait that gave up, an out-of-range slot) and that the device
+ * lengths and next positions equal the host mirrors.  KVC_ERR_DEVICE on any
+ * difference (message names it), KVC_ERR_CUDA if the synchronisation fails.
+ */
+kvc_status kvc_check(kvc_handle* h, void* stream);
+
+/* Tuning / test options (kvc_set_option). */
+typedef enum kvc_option {
+    KVC_OPT_DECODE_SPLIT_ROWS = 1, /* key rows per decode split (multiple of 64); 0 = automatic */
+    KVC_OPT_FORCE_GENERIC = 2,     /* 1 = use the dtype-generic CUDA-core kernels even for bf16, d_h = 128 */
+    KVC_OPT_SUFFIX_KERNEL = 3,     /* 0 = automatic, 1 = generic, 2 = tensor-core tile kernel */
+    KVC_OPT_TIMING = 4             /* 1 = record a CUDA event pair around every kernel launch */
+} kvc_option;
+
+kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
+
+/* Kernel families counted by kvc_kernel_stats. */
+typedef enum kvc_kernel {
+    KVC_KERNEL_ROPE_APPEND = 0,     /* fused RoPE + key/value append */
+    KVC_KERNEL_DECODE = 1,          /* split-K decode attention (bf16, d_h = 128) */
+    KVC_KERNEL_DECODE_COMBINE = 2,  /* log-sum-exp merge of decode splits */
+    KVC_KERNEL_SUFFIX = 3,          /* tensor-core suffix-chunk attention */
+    KVC_KERNEL_GENERIC_ATTEND = 4,  /* dtype-generic attention */
+    KVC_KERNEL_BOOKKEEPING = 5,     /* commit, truncate, finiteness check */
+    KVC_KERNEL_COUNT = 6
+} kvc_kernel;
+
+/*
+ * Launch count and (with KVC_OPT_TIMING on) summed device time in ms of one
+ * kernel family since the handle was created or kvc_reset_stats was called;
+ * kernel = -1 sums every family.  Reading the time synchronises on the
+ * recorded events.  Either output pointer may be NULL.
+ */
+kvc_status kvc_kernel_stats(kvc_handle* h, int32_t kernel, double* total_ms, int64_t* launches);
+kvc_status kvc_reset_stats(kvc_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,845 @@
+// Host side of the kvc C ABI: handle lifetime, argument checks against host
+// mirrors of the lengths (every rejection happens before any work is
+// enqueued), launch planning and the per-call kernel sequence.
+//
+// [Ch37] "Keep the prefix, project only the new row": the listing "Own a fixed
+// layer-bound cache, append one checked row, and reset logical length" defines
+// construction checks (zero batch, zero capacity, capacity beyond the RoPE
+// positions, element-count overflow, allocation), the append checks (key and
+// value shape, full cache, non-finite rows) and reset; section "Reset or
+// reject without corrupting retained state" requires that a rejected call
+// changes neither stored rows nor lengths.  [LCP5] adds truncation to a cut
+// with next_position = cut and the longest-common-prefix rule.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <string>
+#include <vector>
+
+#include "kvc_internal.h"
+
+using namespace kvc;
+
+struct kvc_handle : public kvc::Handle {};
+
+namespace {
+
+thread_local std::string g_create_error;
+
+std::string vformat(const char* fmt, va_list ap) {
+    char buf[1024];
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    return std::string(buf);
+}
+
+kvc_status fail(kvc_handle* h, kvc_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::string msg = vformat(fmt, ap);
+    va_end(ap);
+    if (h) h->last_error = msg;
+    else g_create_error = msg;
+    return st;
+}
+
+kvc_status cuda_fail(kvc_handle* h, cudaError_t e, const char* what) {
+    return fail(h, KVC_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+}
+
+#define KVC_CUDA(h, call)                                    \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+    } while (0)
+
+size_t dtype_size(int dtype) {
+    switch (dtype) {
+        case KVC_BF16: return 2;
+        case KVC_F32: return 4;
+        case KVC_F64: return 8;
+    }
+    return 0;
+}
+
+const char* dtype_name(int dtype) {
+    switch (dtype) {
+        case KVC_BF16: return "bf16";
+        case KVC_F32: return "f32";
+        case KVC_F64: return "f64";
+    }
+    return "?";
+}
+
+int out_dtype(int storage) { return storage == KVC_F64 ? KVC_F64 : KVC_F32; }
+
+bool mul_ok(size_t a, size_t b, size_t* out) {
+    if (a != 0 && b > std::numeric_limits<size_t>::max() / a) return false;
+    *out = a * b;
+    return true;
+}
+
+std::string shape_str(const int64_t* s, int n) {
+    std::string r = "[";
+    for (int i = 0; i < n; ++i) {
+        if (i) r += ", ";
+        r += std::to_string(s[i]);
+    }
+    return r + "]";
+}
+
+// Checks a [B, H, S?, d] tensor.  S < 0 accepts any positive third extent.
+kvc_status check_tensor(kvc_handle* h, const kvc_tensor* t, const char* name, kvc_status shape_err,
+                        int dtype, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+    if (!t || !t->data) return fail(h, KVC_ERR_NULL, "%s tensor or its data pointer is NULL", name);
+    if (t->dtype != dtype)
+        return fail(h, KVC_ERR_DTYPE, "%s has dtype %s, the cache expects %s", name, dtype_name(t->dtype),
+                    dtype_name(dtype));
+    const int64_t want[4] = {d0, d1, d2, d3};
+    bool ok = t->ndim == 4;
+    for (int i = 0; ok && i < 4; ++i) ok = want[i] < 0 ? t->shape[i] > 0 : t->shape[i] == want[i];
+    if (!ok) {
+        int64_t shown[4];
+        for (int i = 0; i < 4; ++i) shown[i] = want[i] < 0 ? -1 : want[i];
+        return fail(h, shape_err, "%s must have shape %s, got %s", name, shape_str(shown, 4).c_str(),
+                    shape_str(t->shape, t->ndim < 0 ? 0 : (t->ndim > 4 ? 4 : t->ndim)).c_str());
+    }
+    if (((uintptr_t)t->data & 15u) != 0)
+        return fail(h, KVC_ERR_CONFIG, "%s data pointer is not 16-byte aligned", name);
+    // A host pointer handed to a kernel would fault the device: insist on device memory
+    // of the handle's GPU.
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, t->data) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, KVC_ERR_CONFIG, "%s data pointer is not a CUDA allocation", name);
+    }
+    if ((attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) || attr.device != h->cfg.device)
+        return fail(h, KVC_ERR_CONFIG, "%s data must be device memory of GPU %d", name, h->cfg.device);
+    return KVC_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 2-D bf16 map over `rows` rows of 128 elements, box [box_rows x 64], 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, void* base, uint64_t rows, uint32_t box_rows) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches `fn` (returning cudaError_t) as one kernel of family `id`: counts it
+// and, when timing is on, brackets it with a CUDA event pair on its stream.
+template <typename F>
+cudaError_t timed(kvc_handle* h, int id, cudaStream_t s, F fn) {
+    auto& t = h->timers[id];
+    t.launches += 1;
+    if (!h->timing) return fn();
+    if (t.used == t.start.size()) {
+        cudaEvent_t a, b;
+        cudaError_t e = cudaEventCreate(&a);
+        if (e != cudaSuccess) return e;
+        e = cudaEventCreate(&b);
+        if (e != cudaSuccess) return e;
+        t.start.push_back(a);
+        t.stop.push_back(b);
+    }
+    cudaError_t e = cudaEventRecord(t.start[t.used], s);
+    if (e != cudaSuccess) return e;
+    e = fn();
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(t.stop[t.used], s);
+    t.used += 1;
+    return e;
+}
+
+cudaError_t collect_timer(kvc_handle* h, int id) {
+    auto& t = h->timers[id];
+    for (size_t i = 0; i < t.used; ++i) {
+        cudaError_t e = cudaEventSynchronize(t.stop[i]);
+        if (e != cudaSuccess) return e;
+        float ms = 0;
+        e = cudaEventElapsedTime(&ms, t.start[i], t.stop[i]);
+        if (e != cudaSuccess) return e;
+        t.ms += ms;
+    }
+    t.used = 0;
+    return cudaSuccess;
+}
+
+bool fast_decode_ok(const kvc_handle* h) {
+    return h->cfg.dtype == KVC_BF16 && h->cfg.head_dim == 128 && h->have_tmaps && !h->opt_force_generic &&
+           h->Hq() / h->Hkv() <= 32;
+}
+
+int sm_count(int device) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 152;
+    return n;
+}
+
+void free_all(kvc_handle* h) {
+    cudaFree(h->K);
+    cudaFree(h->V);
+    cudaFree(h->positions);
+    cudaFree(h->len_d);
+    cudaFree(h->next_d);
+    cudaFree(h->rope);
+    cudaFree(h->err_d);
+    cudaFree(h->nonfinite_d);
+    if (h->nonfinite_h) cudaFreeHost(h->nonfinite_h);
+    cudaFree(h->qrot);
+    cudaFree(h->part_o);
+    cudaFree(h->part_ml);
+    cudaFree(h->qrot_chunk);
+    cudaFree(h->work_counter);
+    h->ring.destroy();
+    for (auto& t : h->timers) {
+        for (auto e : t.start) cudaEventDestroy(e);
+        for (auto e : t.stop) cudaEventDestroy(e);
+        t.start.clear();
+        t.stop.clear();
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- ArgRing
+
+namespace kvc {
+
+cudaError_t ArgRing::init() {
+    for (int i = 0; i < kSlots; ++i) {
+        cudaError_t e = cudaEventCreateWithFlags(&done[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+void ArgRing::destroy() {
+    for (int i = 0; i < kSlots; ++i) {
+        if (pending[i]) cudaEventSynchronize(done[i]);
+        if (host[i]) cudaFreeHost(host[i]);
+        if (dev[i]) cudaFree(dev[i]);
+        if (done[i]) cudaEventDestroy(done[i]);
+        host[i] = dev[i] = nullptr;
+        done[i] = nullptr;
+    }
+}
+
+cudaError_t ArgRing::acquire(size_t bytes, void** host_ptr) {
+    const int s = next;
+    if (pending[s]) {
+        cudaError_t e = cudaEventSynchronize(done[s]);
+        if (e != cudaSuccess) return e;
+        pending[s] = false;
+    }
+    if (cap[s] < bytes) {
+        size_t c = std::max<size_t>(bytes, 4096);
+        if (host[s]) cudaFreeHost(host[s]);
+        if (dev[s]) cudaFree(dev[s]);
+        host[s] = dev[s] = nullptr;
+        cap[s] = 0;
+        cudaError_t e = cudaHostAlloc(&host[s], c, cudaHostAllocDefault);
+        if (e != cudaSuccess) return e;
+        e = cudaMalloc(&dev[s], c);
+        if (e != cudaSuccess) return e;
+        cap[s] = c;
+    }
+    cur = s;
+    *host_ptr = host[s];
+    return cudaSuccess;
+}
+
+cudaError_t ArgRing::upload(size_t bytes, cudaStream_t stream, void** dev_ptr) {
+    *dev_ptr = dev[cur];
+    return cudaMemcpyAsync(dev[cur], host[cur], bytes, cudaMemcpyHostToDevice, stream);
+}
+
+cudaError_t ArgRing::release(cudaStream_t stream) {
+    cudaError_t e = cudaEventRecord(done[cur], stream);
+    pending[cur] = true;
+    next = (cur + 1) % kSlots;
+    cur = -1;
+    return e;
+}
+
+}  // namespace kvc
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+const char* kvc_status_string(kvc_status s) {
+    switch (s) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_NULL: return "null pointer";
+        case KVC_ERR_ZERO_BATCH: return "zero batch size";
+        case KVC_ERR_ZERO_CAPACITY: return "zero capacity";
+        case KVC_ERR_CAPACITY_EXCEEDS_POSITIONS: return "capacity exceeds RoPE positions";
+        case KVC_ERR_ELEMENT_OVERFLOW: return "element count overflow";
+        case KVC_ERR_ALLOC: return "device allocation failed";
+        case KVC_ERR_FULL: return "cache full";
+        case KVC_ERR_KEY_SHAPE: return "key shape mismatch";
+        case KVC_ERR_VALUE_SHAPE: return "value shape mismatch";
+        case KVC_ERR_QUERY_SHAPE: return "query shape mismatch";
+        case KVC_ERR_OUTPUT_SHAPE: return "output shape mismatch";
+        case KVC_ERR_DTYPE: return "dtype mismatch";
+        case KVC_ERR_LAYER: return "layer out of range";
+        case KVC_ERR_NONFINITE_KEY: return "non-finite key";
+        case KVC_ERR_NONFINITE_VALUE: return "non-finite value";
+        case KVC_ERR_CUT: return "invalid cut";
+        case KVC_ERR_EMPTY_QUERY: return "empty query";
+        case KVC_ERR_POSITION: return "position out of range";
+        case KVC_ERR_CONFIG: return "invalid configuration";
+        case KVC_ERR_CUDA: return "CUDA error";
+        case KVC_ERR_DEVICE: return "device-side error";
+    }
+    return "unknown status";
+}
+
+const char* kvc_last_error(const kvc_handle* h) {
+    return h ? h->last_error.c_str() : g_create_error.c_str();
+}
+
+kvc_status kvc_create(int32_t batch, int32_t heads, int32_t capacity, int32_t head_dim, int32_t layers,
+                      kvc_handle** out) {
+    kvc_config c{};
+    c.batch = batch;
+    c.heads_q = heads;
+    c.heads_kv = heads;
+    c.capacity = capacity;
+    c.head_dim = head_dim;
+    c.layers = layers;
+    c.dtype = KVC_BF16;
+    c.rope_max_positions = 0;
+    c.rope_base = 10000.0;
+    c.checked = 0;
+    c.device = 0;
+    return kvc_create_ex(&c, out);
+}
+
+kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
+    if (!out) return fail(nullptr, KVC_ERR_NULL, "output handle pointer is NULL");
+    *out = nullptr;
+    if (!config) return fail(nullptr, KVC_ERR_NULL, "configuration pointer is NULL");
+    kvc_config c = *config;
+    if (c.batch <= 0) return fail(nullptr, KVC_ERR_ZERO_BATCH, "batch size must be at least 1, got %d", c.batch);
+    if (c.capacity <= 0)
+        return fail(nullptr, KVC_ERR_ZERO_CAPACITY, "capacity must be at least 1, got %d", c.capacity);
+    if (c.heads_q <= 0 || c.heads_kv <= 0 || c.heads_q % c.heads_kv)
+        return fail(nullptr, KVC_ERR_CONFIG, "heads_q (%d) must be a positive multiple of heads_kv (%d)", c.heads_q,
+                    c.heads_kv);
+    if (c.head_dim < 2 || c.head_dim > 256 || c.head_dim % 2)
+        return fail(nullptr, KVC_ERR_CONFIG, "head width must be even and in [2, 256], got %d", c.head_dim);
+    if (c.layers <= 0) return fail(nullptr, KVC_ERR_CONFIG, "layer count must be at least 1, got %d", c.layers);
+    if (!dtype_size(c.dtype)) return fail(nullptr, KVC_ERR_CONFIG, "unknown storage dtype %d", c.dtype);
+    if (!(c.rope_base >= 0.0) || !std::isfinite(c.rope_base))
+        return fail(nullptr, KVC_ERR_CONFIG, "RoPE base must be finite and >= 0");
+    if (c.rope_max_positions < 0) return fail(nullptr, KVC_ERR_CONFIG, "rope_max_positions must be >= 0");
+    const int maxpos = c.rope_max_positions ? c.rope_max_positions : c.capacity;
+    if (c.capacity > maxpos)
+        return fail(nullptr, KVC_ERR_CAPACITY_EXCEEDS_POSITIONS,
+                    "capacity %d is larger than the %d positions the RoPE table covers", c.capacity, maxpos);
+    c.rope_max_positions = maxpos;
+
+    size_t layer_elems, all_elems, bytes, t;
+    if (!mul_ok(c.batch, c.heads_kv, &t) || !mul_ok(t, c.capacity, &t) || !mul_ok(t, c.head_dim, &layer_elems) ||
+        !mul_ok(layer_elems, c.layers, &all_elems) || !mul_ok(all_elems, dtype_size(c.dtype), &bytes))
+        return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW,
+                    "element count overflows for batch %d, %d heads, capacity %d, head width %d, %d layers", c.batch,
+                    c.heads_kv, c.capacity, c.head_dim, c.layers);
+    if ((uint64_t)c.batch * c.heads_kv * c.capacity > (uint64_t)INT32_MAX)
+        return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW, "batch * heads_kv * capacity must fit in 31 bits");
+
+    cudaError_t e = cudaSetDevice(c.device);
+    if (e != cudaSuccess) return fail(nullptr, KVC_ERR_CUDA, "cudaSetDevice(%d) failed: %s", c.device, cudaGetErrorString(e));
+
+    kvc_handle* h = new kvc_handle();
+    h->cfg = c;
+    h->max_positions = maxpos;
+    h->elem_size = dtype_size(c.dtype);
+    h->layer_elems = layer_elems;
+    const size_t LB = (size_t)c.layers * c.batch;
+    auto alloc = [&](void** p, size_t n) -> bool {
+        cudaError_t ae = cudaMalloc(p, n);
+        if (ae != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        return true;
+    };
+    const size_t acc = c.dtype == KVC_F64 ? 8 : 4;
+    bool ok = alloc(&h->K, bytes) && alloc(&h->V, bytes) &&
+              alloc((void**)&h->positions, LB * c.capacity * sizeof(int32_t)) &&
+              alloc((void**)&h->len_d, LB * sizeof(int32_t)) && alloc((void**)&h->next_d, LB * sizeof(int32_t)) &&
+              alloc((void**)&h->err_d, sizeof(uint32_t)) &&
+              alloc((void**)&h->nonfinite_d, 2 * sizeof(unsigned long long)) &&
+              alloc(&h->qrot, (size_t)c.batch * c.heads_q * c.head_dim * acc) &&
+              alloc((void**)&h->work_counter, 64);
+    if (ok && c.rope_base > 0.0)
+        ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2));
+    if (!ok) {
+        free_all(h);
+        delete h;
+        return fail(nullptr, KVC_ERR_ALLOC, "cannot allocate %zu bytes of KV cache storage", 2 * bytes);
+    }
+    auto abort_cuda = [&](cudaError_t ce, const char* what) {
+        free_all(h);
+        delete h;
+        return fail(nullptr, KVC_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(ce));
+    };
+    if ((e = cudaMemset(h->K, 0, bytes)) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->V, 0, bytes)) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->positions, 0, LB * c.capacity * sizeof(int32_t))) != cudaSuccess)
+        return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->len_d, 0, LB * sizeof(int32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->next_d, 0, LB * sizeof(int32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->err_d, 0, sizeof(uint32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaHostAlloc((void**)&h->nonfinite_h, 2 * sizeof(unsigned long long), cudaHostAllocDefault)) !=
+        cudaSuccess)
+        return abort_cuda(e, "cudaHostAlloc");
+    if ((e = h->ring.init()) != cudaSuccess) return abort_cuda(e, "cudaEventCreate");
+
+    if (h->rope) {
+        // cos/sin of phi = p * theta_j, theta_j = base^(-2j/d_h): one IEEE product and one
+        // libm call per entry, computed once per handle.
+        const int half = c.head_dim / 2;
+        std::vector<double> inv(half);
+        for (int j = 0; j < half; ++j) inv[j] = std::pow(c.rope_base, -(2.0 * j) / c.head_dim);
+        std::vector<double2> tab((size_t)maxpos * half);
+        for (int p = 0; p < maxpos; ++p)
+            for (int j = 0; j < half; ++j) {
+                const double ang = (double)p * inv[j];
+                tab[(size_t)p * half + j] = make_double2(std::cos(ang), std::sin(ang));
+            }
+        if ((e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(double2), cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return abort_cuda(e, "cudaMemcpy");
+    }
+
+    if (c.dtype == KVC_BF16 && c.head_dim == 128) {
+        h->tmap_k.resize(c.layers);
+        h->tmap_v.resize(c.layers);
+        bool all = true;
+        const uint64_t rows = (uint64_t)c.batch * c.heads_kv * c.capacity;
+        for (int l = 0; l < c.layers && all; ++l)
+            all = encode_rows_map(&h->tmap_k[l], h->K_layer(l), rows, 64) &&
+                  encode_rows_map(&h->tmap_v[l], h->V_layer(l), rows, 64);
+        h->have_tmaps = all;
+    }
+    h->len_h.assign(LB, 0);
+    h->next_h.assign(LB, 0);
+    *out = h;
+    return KVC_OK;
+}
+
+void kvc_destroy(kvc_handle* h) {
+    if (!h) return;
+    cudaSetDevice(h->cfg.device);
+    cudaDeviceSynchronize();
+    free_all(h);
+    delete h;
+}
+
+static kvc_status check_layer(kvc_handle* h, int32_t layer) {
+    if (layer < 0 || layer >= h->cfg.layers)
+        return fail(h, KVC_ERR_LAYER, "layer %d is outside [0, %d)", layer, h->cfg.layers);
+    return KVC_OK;
+}
+
+static kvc_status ensure_partials(kvc_handle* h, size_t splits) {
+    if (h->part_splits >= splits) return KVC_OK;
+    cudaDeviceSynchronize();
+    cudaFree(h->part_o);
+    cudaFree(h->part_ml);
+    h->part_o = nullptr;
+    h->part_ml = nullptr;
+    h->part_splits = 0;
+    const size_t lanes = (size_t)h->B() * h->Hq();
+    if (cudaMalloc((void**)&h->part_o, lanes * splits * 128 * sizeof(float)) != cudaSuccess ||
+        cudaMalloc((void**)&h->part_ml, lanes * splits * sizeof(float2)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, KVC_ERR_ALLOC, "cannot allocate decode split scratch for %zu splits", splits);
+    }
+    h->part_splits = splits;
+    return KVC_OK;
+}
+
+static kvc_status check_nonfinite(kvc_handle* h, const kvc_tensor* k, const kvc_tensor* v, int64_t nk,
+                                  int64_t nv, cudaStream_t s) {
+    KVC_CUDA(h, cudaMemsetAsync(h->nonfinite_d, 0xff, 2 * sizeof(unsigned long long), s));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_nonfinite(h->cfg.dtype, k->data, nk, h->nonfinite_d, s); }));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_nonfinite(h->cfg.dtype, v->data, nv, h->nonfinite_d + 1, s); }));
+    KVC_CUDA(h, cudaMemcpyAsync(h->nonfinite_h, h->nonfinite_d, 2 * sizeof(unsigned long long),
+                                cudaMemcpyDeviceToHost, s));
+    KVC_CUDA(h, cudaStreamSynchronize(s));
+    for (int which = 0; which < 2; ++which) {
+        const unsigned long long idx = h->nonfinite_h[which];
+        if (idx == ~0ull) continue;
+        const kvc_tensor* t = which ? v : k;
+        double val = 0;
+        char raw[8] = {};
+        if (cudaMemcpy(raw, (const char*)t->data + idx * h->elem_size, h->elem_size, cudaMemcpyDeviceToHost) ==
+            cudaSuccess) {
+            if (h->cfg.dtype == KVC_F64) memcpy(&val, raw, 8);
+            else if (h->cfg.dtype == KVC_F32) { float f; memcpy(&f, raw, 4); val = f; }
+            else { uint32_t u = (uint32_t)(*(uint16_t*)raw) << 16; float f; memcpy(&f, &u, 4); val = f; }
+        }
+        return fail(h, which ? KVC_ERR_NONFINITE_VALUE : KVC_ERR_NONFINITE_KEY,
+                    "%s element at flat index %llu is not finite (%g); nothing was appended", which ? "value" : "key",
+                    idx, val);
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                             const kvc_tensor* v, const kvc_tensor* out, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    kvc_status st;
+    if ((st = check_layer(h, layer)) != KVC_OK) return st;
+    const int B = h->B(), Hq = h->Hq(), Hkv = h->Hkv(), D = h->D(), C = h->C();
+    const int dt = h->cfg.dtype;
+    if (q && q->ndim == 4 && q->shape[2] != 1)
+        return fail(h, KVC_ERR_QUERY_SHAPE, "one decode step takes a single token per sequence, got %lld",
+                    (long long)q->shape[2]);
+    if ((st = check_tensor(h, q, "query", KVC_ERR_QUERY_SHAPE, dt, B, Hq, 1, D)) != KVC_OK) return st;
+    if ((st = check_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, 1, D)) != KVC_OK) return st;
+    if ((st = check_tensor(h, v, "value", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, 1, D)) != KVC_OK) return st;
+    if ((st = check_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_dtype(dt), B, Hq, 1, D)) != KVC_OK)
+        return st;
+    int32_t* lenh = &h->len_h[(size_t)layer * B];
+    int32_t* nexth = &h->next_h[(size_t)layer * B];
+    int max_t = 0;
+    int64_t total_keys = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lenh[b] >= C)
+            return fail(h, KVC_ERR_FULL, "sequence %d of layer %d already holds %d rows, the capacity", b, layer, C);
+        if (h->rope && nexth[b] >= h->max_positions)
+            return fail(h, KVC_ERR_POSITION, "sequence %d would be rotated at position %d, beyond the %d-position table",
+                        b, nexth[b], h->max_positions);
+        max_t = std::max(max_t, lenh[b] + 1);
+        total_keys += lenh[b] + 1;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    if (h->cfg.checked) {
+        if ((st = check_nonfinite(h, k, v, (int64_t)B * Hkv * D, (int64_t)B * Hkv * D, s)) != KVC_OK) return st;
+    }
+    const bool fast = fast_decode_ok(h);
+    AppendLaunch ap{};
+    ap.q = q->data; ap.k = k->data; ap.v = v->data;
+    ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
+    ap.slot0 = h->len_layer(layer); ap.pos0 = h->next_layer(layer); ap.seqlen = nullptr;
+    ap.qrot = h->qrot; ap.qrot_kind = dt == KVC_F64 ? 1 : 0;
+    ap.rope = h->rope; ap.err = h->err_d;
+    ap.B = B; ap.Hq = Hq; ap.Hkv = Hkv; ap.S = 1; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
+
+    int split_rows = 0, max_splits = 1;
+    if (fast) {
+        if (h->opt_split_rows > 0) {
+            split_rows = (int)h->opt_split_rows;
+        } else {
+            const int G = Hq / Hkv;
+            const int64_t target = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(G) * 4;
+            int64_t r = (total_keys * Hkv + target - 1) / target;
+            r = (r + 63) / 64 * 64;
+            r = std::max<int64_t>(r, 256);
+            r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
+            split_rows = (int)r;
+        }
+        max_splits = (max_t + split_rows - 1) / split_rows;
+        if (max_splits > 1 && (st = ensure_partials(h, max_splits)) != KVC_OK) return st;
+    }
+
+    KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
+    if (fast) {
+        DecodeLaunch dl{};
+        dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
+        dl.qrot = (const float*)h->qrot; dl.len = h->len_layer(layer);
+        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
+        dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
+        if (max_splits > 1)
+            KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
+    } else {
+        GenericAttendLaunch g{};
+        g.qrot = h->qrot; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
+        g.slot0 = h->len_layer(layer); g.seqlen = nullptr; g.out = out->data;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
+    }
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
+        return launch_commit(h->len_layer(layer), h->next_layer(layer), h->next_layer(layer), nullptr, 1, B, s);
+    }));
+    for (int b = 0; b < B; ++b) {
+        lenh[b] += 1;
+        nexth[b] += 1;
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                              const kvc_tensor* v, const int32_t* start_pos, const int32_t* seqlen,
+                              const kvc_tensor* out, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    kvc_status st;
+    if ((st = check_layer(h, layer)) != KVC_OK) return st;
+    const int B = h->B(), Hq = h->Hq(), Hkv = h->Hkv(), D = h->D(), C = h->C();
+    const int dt = h->cfg.dtype;
+    // Appending without attending needs no query: q may then be NULL.
+    const bool need_q = out != nullptr || q != nullptr;
+    if (need_q && (st = check_tensor(h, q, "query", KVC_ERR_QUERY_SHAPE, dt, B, Hq, -1, D)) != KVC_OK) return st;
+    if (!need_q && (st = check_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, -1, D)) != KVC_OK) return st;
+    const int64_t S64 = need_q ? q->shape[2] : k->shape[2];
+    if (S64 > INT32_MAX) return fail(h, KVC_ERR_QUERY_SHAPE, "a chunk of %lld rows is too long", (long long)S64);
+    const int S = (int)S64;
+    if ((st = check_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, S, D)) != KVC_OK) return st;
+    if ((st = check_tensor(h, v, "value", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, S, D)) != KVC_OK) return st;
+    if (out && (st = check_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_dtype(dt), B, Hq, S, D)) != KVC_OK)
+        return st;
+    int32_t* lenh = &h->len_h[(size_t)layer * B];
+    int32_t* nexth = &h->next_h[(size_t)layer * B];
+    std::vector<int32_t> st_h(B), sl_h(B);
+    for (int b = 0; b < B; ++b) {
+        const int n = seqlen ? seqlen[b] : S;
+        if (n < 0 || n > S)
+            return fail(h, KVC_ERR_QUERY_SHAPE, "sequence %d declares %d rows, the chunk holds %d", b, n, S);
+        const int p = start_pos ? start_pos[b] : nexth[b];
+        if (lenh[b] + (int64_t)n > C)
+            return fail(h, KVC_ERR_FULL, "sequence %d of layer %d holds %d rows; %d more exceed the capacity %d", b,
+                        layer, lenh[b], n, C);
+        if (p < 0 || (int64_t)p + n > (h->rope ? (int64_t)h->max_positions : (int64_t)INT32_MAX))
+            return fail(h, KVC_ERR_POSITION, "sequence %d: positions %d .. %lld leave the %d-position table", b, p,
+                        (long long)p + n - 1, h->max_positions);
+        st_h[b] = p;
+        sl_h[b] = n;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    if (h->cfg.checked) {
+        const int64_t nk = (int64_t)B * Hkv * S * D;
+        if ((st = check_nonfinite(h, k, v, nk, nk, s)) != KVC_OK) return st;
+    }
+    // qrot scratch for the chunk (accumulator dtype for the generic kernel)
+    const size_t acc = dt == KVC_F64 ? 8 : 4;
+    const size_t qbytes = (size_t)B * Hq * S * D * acc;
+    if (out && qbytes > h->qrot_chunk_bytes) {
+        cudaStreamSynchronize(s);
+        cudaFree(h->qrot_chunk);
+        h->qrot_chunk = nullptr;
+        h->qrot_chunk_bytes = 0;
+        if (cudaMalloc(&h->qrot_chunk, qbytes) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, KVC_ERR_ALLOC, "cannot allocate %zu bytes of chunk scratch", qbytes);
+        }
+        h->qrot_chunk_bytes = qbytes;
+    }
+    void* hp;
+    KVC_CUDA(h, h->ring.acquire(2 * B * sizeof(int32_t), &hp));
+    memcpy(hp, st_h.data(), B * sizeof(int32_t));
+    memcpy((int32_t*)hp + B, sl_h.data(), B * sizeof(int32_t));
+    void* dp;
+    KVC_CUDA(h, h->ring.upload(2 * B * sizeof(int32_t), s, &dp));
+    const int32_t* start_d = (const int32_t*)dp;
+    const int32_t* seqlen_d = start_d + B;
+
+    AppendLaunch ap{};
+    ap.q = out ? q->data : nullptr; ap.k = k->data; ap.v = v->data;
+    ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
+    ap.slot0 = h->len_layer(layer); ap.pos0 = start_d; ap.seqlen = seqlen_d;
+    ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = dt == KVC_F64 ? 1 : 0;
+    ap.rope = h->rope; ap.err = h->err_d;
+    ap.B = B; ap.Hq = out ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
+    // Without an output the query heads are skipped (Hq = 0 in the launch).
+    KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
+    if (out) {
+        GenericAttendLaunch g{};
+        g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
+        g.slot0 = h->len_layer(layer); g.seqlen = seqlen_d; g.out = out->data;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
+    }
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
+        return launch_commit(h->len_layer(layer), h->next_layer(layer), start_d, seqlen_d, S, B, s);
+    }));
+    KVC_CUDA(h, h->ring.release(s));
+    for (int b = 0; b < B; ++b) {
+        lenh[b] += sl_h[b];
+        nexth[b] = st_h[b] + sl_h[b];
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_reset(kvc_handle* h, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    const size_t n = (size_t)h->cfg.layers * h->B();
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    KVC_CUDA(h, cudaMemsetAsync(h->len_d, 0, n * sizeof(int32_t), s));
+    KVC_CUDA(h, cudaMemsetAsync(h->next_d, 0, n * sizeof(int32_t), s));
+    std::fill(h->len_h.begin(), h->len_h.end(), 0);
+    std::fill(h->next_h.begin(), h->next_h.end(), 0);
+    return KVC_OK;
+}
+
+kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (!cut) return fail(h, KVC_ERR_NULL, "cut array is NULL");
+    const int B = h->B(), L = h->cfg.layers;
+    for (int b = 0; b < B; ++b) {
+        if (cut[b] < 0) return fail(h, KVC_ERR_CUT, "cut %d of sequence %d is negative", cut[b], b);
+        for (int l = 0; l < L; ++l)
+            if (cut[b] > h->len_h[(size_t)l * B + b])
+                return fail(h, KVC_ERR_CUT, "cut %d of sequence %d exceeds its length %d in layer %d", cut[b], b,
+                            h->len_h[(size_t)l * B + b], l);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    void* hp;
+    KVC_CUDA(h, h->ring.acquire(B * sizeof(int32_t), &hp));
+    memcpy(hp, cut, B * sizeof(int32_t));
+    void* dp;
+    KVC_CUDA(h, h->ring.upload(B * sizeof(int32_t), s, &dp));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_truncate(h->len_d, h->next_d, (const int32_t*)dp, L, B, s); }));
+    KVC_CUDA(h, h->ring.release(s));
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b) {
+            h->len_h[(size_t)l * B + b] = cut[b];
+            h->next_h[(size_t)l * B + b] = cut[b];
+        }
+    return KVC_OK;
+}
+
+kvc_status kvc_lcp(const int32_t* cached, int64_t n, const int32_t* query, int64_t m, int32_t* cut) {
+    if (!cut) return KVC_ERR_NULL;
+    if (m <= 0) return KVC_ERR_EMPTY_QUERY;
+    if (!query || (n > 0 && !cached) || n < 0) return KVC_ERR_NULL;
+    int64_t L = 0;
+    const int64_t lim = std::min(n, m);
+    while (L < lim && cached[L] == query[L]) ++L;
+    const int64_t c = std::min(L, m - 1);
+    if (c > INT32_MAX) return KVC_ERR_CUT;
+    *cut = (int32_t)c;
+    return KVC_OK;
+}
+
+kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths, int32_t* next_positions) {
+    if (!h) return KVC_ERR_NULL;
+    if (layer < 0 || layer >= h->cfg.layers) return KVC_ERR_LAYER;
+    const int B = h->B();
+    if (lengths) memcpy(lengths, &h->len_h[(size_t)layer * B], B * sizeof(int32_t));
+    if (next_positions) memcpy(next_positions, &h->next_h[(size_t)layer * B], B * sizeof(int32_t));
+    return KVC_OK;
+}
+
+kvc_status kvc_get_config(const kvc_handle* h, kvc_config* out) {
+    if (!h || !out) return KVC_ERR_NULL;
+    *out = h->cfg;
+    return KVC_OK;
+}
+
+kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** values, int32_t** positions) {
+    if (!h) return KVC_ERR_NULL;
+    if (layer < 0 || layer >= h->cfg.layers) return KVC_ERR_LAYER;
+    if (keys) *keys = h->K_layer(layer);
+    if (values) *values = h->V_layer(layer);
+    if (positions) *positions = h->pos_layer(layer);
+    return KVC_OK;
+}
+
+kvc_status kvc_check(kvc_handle* h, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    KVC_CUDA(h, cudaStreamSynchronize(s));
+    const size_t n = (size_t)h->cfg.layers * h->B();
+    std::vector<int32_t> len(n), next(n);
+    uint32_t err = 0;
+    KVC_CUDA(h, cudaMemcpy(len.data(), h->len_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    KVC_CUDA(h, cudaMemcpy(next.data(), h->next_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    KVC_CUDA(h, cudaMemcpy(&err, h->err_d, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    if (err)
+        return fail(h, KVC_ERR_DEVICE, "device error word 0x%x (1: slot out of range, 2: bounded wait timed out, 4: tensor memory)",
+                    err);
+    for (size_t i = 0; i < n; ++i)
+        if (len[i] != h->len_h[i] || next[i] != h->next_h[i])
+            return fail(h, KVC_ERR_DEVICE, "device length/next position (%d, %d) of entry %zu differ from the host (%d, %d)",
+                        len[i], next[i], i, h->len_h[i], h->next_h[i]);
+    return KVC_OK;
+}
+
+kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    switch (option) {
+        case KVC_OPT_DECODE_SPLIT_ROWS:
+            if (value < 0 || value % 64 || value > (int64_t)1 << 30)
+                return fail(h, KVC_ERR_CONFIG, "decode split rows must be 0 or a positive multiple of 64, got %lld",
+                            (long long)value);
+            h->opt_split_rows = value;
+            return KVC_OK;
+        case KVC_OPT_FORCE_GENERIC:
+            h->opt_force_generic = value != 0;
+            return KVC_OK;
+        case KVC_OPT_SUFFIX_KERNEL:
+            if (value < 0 || value > 2) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1 or 2");
+            h->opt_suffix_kernel = value;
+            return KVC_OK;
+        case KVC_OPT_TIMING:
+            h->timing = value != 0;
+            return KVC_OK;
+    }
+    return fail(h, KVC_ERR_CONFIG, "unknown option %d", option);
+}
+
+kvc_status kvc_kernel_stats(kvc_handle* h, int32_t kernel, double* total_ms, int64_t* launches) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (kernel < -1 || kernel >= KVC_KERNEL_COUNT) return fail(h, KVC_ERR_CONFIG, "unknown kernel family %d", kernel);
+    double ms = 0;
+    int64_t n = 0;
+    for (int id = 0; id < KVC_KERNEL_COUNT; ++id) {
+        if (kernel != -1 && id != kernel) continue;
+        KVC_CUDA(h, collect_timer(h, id));
+        ms += h->timers[id].ms;
+        n += h->timers[id].launches;
+    }
+    if (total_ms) *total_ms = ms;
+    if (launches) *launches = n;
+    return KVC_OK;
+}
+
+kvc_status kvc_reset_stats(kvc_handle* h) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    for (int id = 0; id < KVC_KERNEL_COUNT; ++id) {
+        KVC_CUDA(h, collect_timer(h, id));
+        h->timers[id].ms = 0;
+        h->timers[id].launches = 0;
+    }
+    return KVC_OK;
+}
+
+}  // extern "C"

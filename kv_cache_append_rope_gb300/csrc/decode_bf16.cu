@@ -1,0 +1,355 @@
+// Split-K flash-decoding for bf16 caches with d_h = 128 (MHA, GQA and MQA).
+//
+// [Ch37] "Keep the prefix, project only the new row", listing "Evaluate one
+// newest query across the retained rows plus the candidate key/value row
+// before committing the append": each new query scores all t retained rows
+// (s_j = q.k_j / sqrt(d_h)), takes a max-subtracted softmax and mixes the t
+// values.  [Ch37] "From causal attention to managed LLM inference state"
+// cites multi-query attention because reloading the K/V prefix is the
+// memory-bandwidth bottleneck; here one CTA serves all G = H_q / H_kv query
+// heads of one key/value head, so every K/V byte is read from HBM once.
+//
+// Work decomposition: grid (split, b * H_kv + kv_head).  A CTA owns key rows
+// [split * R, min((split + 1) * R, t)) of its lane (t = old length + 1: the
+// new row was already appended by the RoPE/append kernel).  One producer warp
+// streams 64-row K and V tiles with TMA (128-byte swizzle, no multicast) into
+// a ring of shared-memory stages guarded by mbarriers; four consumer warps
+// each take 16 rows of every stage and compute S = Q K^T and O += P V with
+// m16n8k16 bf16 tensor-core MMAs (fp32 accumulation), the G query heads
+// padded to 16 (or 32) MMA rows.  The softmax is online per warp (running
+// max and sum in log2 units, quad shuffles for row maxima); the four warps
+// are merged through shared memory and the split's (O, max, sum) is written
+// to scratch, or the normalised output when the lane has a single split.  A
+// second kernel merges the splits of every query head by log-sum-exp.
+#include <cuda.h>
+
+#include "device_common.cuh"
+#include "kvc_internal.h"
+#include "ptx.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int KT = 64;                 // key rows per stage
+constexpr int NCW = 4;                 // consumer warps
+constexpr int THREADS = (NCW + 1) * 32;
+constexpr int HALF_BYTES = KT * 128;   // 64 rows x 64 dims x 2 B
+constexpr int TILE_BYTES = 2 * HALF_BYTES;
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K and V
+
+template <int STAGES>
+constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/; }
+
+template <int MT> struct Cfg;
+template <> struct Cfg<1> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
+template <> struct Cfg<2> { static constexpr int STAGES = 4; static constexpr int MINB = 1; };
+
+template <int MT>
+__global__ void __launch_bounds__(THREADS, Cfg<MT>::MINB)
+decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   DecodeLaunch a) {
+    constexpr int STAGES = Cfg<MT>::STAGES;
+    const int split = blockIdx.x;
+    const int lane_kv = blockIdx.y;
+    const int b = lane_kv / a.Hkv;
+    const int hkv = lane_kv - b * a.Hkv;
+    const int t = a.len[b] + 1;
+    const int r0 = split * a.split_rows;
+    if (r0 >= t) return;
+    const int r1 = min(t, r0 + a.split_rows);
+    const int ntiles = (r1 - r0 + KT - 1) / KT;
+    const int G = a.Hq / a.Hkv;
+    const int nsplit_lane = (t + a.split_rows - 1) / a.split_rows;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    volatile int* s_err = (volatile int*)(empty + STAGES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), NCW);
+        }
+        *s_err = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    int issued = 0;
+    float o[MT][16][4];
+    float m[MT][2], l[MT][2];
+
+    if (warp == NCW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !mbar_wait_bounded(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1)) {
+                    *s_err = 1;
+                    atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                const int y = lane_kv * a.C + r0 + i * KT;
+                uint8_t* st = smem + s * STAGE_BYTES;
+                tma_load_2d(smem_u32(st), &tmK, 0, y, fb);
+                tma_load_2d(smem_u32(st + HALF_BYTES), &tmK, 64, y, fb);
+                tma_load_2d(smem_u32(st + TILE_BYTES), &tmV, 0, y, fb);
+                tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES), &tmV, 64, y, fb);
+                issued = i + 1;
+            }
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int qa = lane >> 2;          // fragment row (and row + 8)
+        const int qc = (lane & 3) * 2;     // fragment column pair
+        // Q fragments, pre-scaled so that scores come out in log2 units.
+        const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+        uint32_t qf[MT][8][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int ra = mt * 16 + qa, rb = ra + 8;
+            const float* qra = a.qrot + ((int64_t)b * a.Hq + hkv * G + ra) * D;
+            const float* qrb = a.qrot + ((int64_t)b * a.Hq + hkv * G + rb) * D;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int c = ks * 16 + qc;
+                float2 x0 = ra < G ? *(const float2*)(qra + c) : make_float2(0.f, 0.f);
+                float2 x1 = rb < G ? *(const float2*)(qrb + c) : make_float2(0.f, 0.f);
+                float2 x2 = ra < G ? *(const float2*)(qra + c + 8) : make_float2(0.f, 0.f);
+                float2 x3 = rb < G ? *(const float2*)(qrb + c + 8) : make_float2(0.f, 0.f);
+                qf[mt][ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
+                qf[mt][ks][1] = pack_bf16(x1.x * qscale, x1.y * qscale);
+                qf[mt][ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
+                qf[mt][ks][3] = pack_bf16(x3.x * qscale, x3.y * qscale);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            m[mt][0] = m[mt][1] = -INFINITY;
+            l[mt][0] = l[mt][1] = 0.f;
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][n][e] = 0.f;
+        }
+
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % STAGES;
+            if (!mbar_wait_bounded(smem_u32(&full[s]), (i / STAGES) & 1)) {
+                *s_err = 1;
+                atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+                break;
+            }
+            const uint32_t kt = smem_u32(smem + s * STAGE_BYTES);
+            const uint32_t vt = kt + TILE_BYTES;
+            const int key_base = r0 + i * KT + warp * 16;
+
+            // ---- S = Q K^T for this warp's 16 keys (two n8 tiles)
+            float sc[MT][2][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int row = warp * 16 + nt * 8 + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int dim0 = kk * 32 + (lane >> 3) * 8;
+                    const uint32_t addr = kt + (dim0 >> 6) * HALF_BYTES + swz128(row, (dim0 & 63) >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        mma_bf16_16816(sc[mt][nt], qf[mt][2 * kk], b0, b1);
+                        mma_bf16_16816(sc[mt][nt], qf[mt][2 * kk + 1], b2, b3);
+                    }
+                }
+            }
+            // ---- mask keys beyond this split
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = key_base + nt * 8 + qc + e;
+                    if (key >= r1) {
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            sc[mt][nt][e] = -INFINITY;
+                            sc[mt][nt][2 + e] = -INFINITY;
+                        }
+                    }
+                }
+            // ---- online softmax (rows qa and qa + 8 of each m tile)
+            uint32_t pf[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    float mx = fmaxf(fmaxf(sc[mt][0][2 * rr], sc[mt][0][2 * rr + 1]),
+                                     fmaxf(sc[mt][1][2 * rr], sc[mt][1][2 * rr + 1]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m[mt][rr], mx);
+                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                    const float corr = fast_exp2(m[mt][rr] - m_use);
+                    m[mt][rr] = m_new;
+                    float ps = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float p = fast_exp2(sc[mt][nt][2 * rr + e] - m_use);
+                            sc[mt][nt][2 * rr + e] = p;
+                            ps += p;
+                        }
+                    l[mt][rr] = l[mt][rr] * corr + ps;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        o[mt][n][2 * rr] *= corr;
+                        o[mt][n][2 * rr + 1] *= corr;
+                    }
+                }
+                pf[mt][0] = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+                pf[mt][1] = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+                pf[mt][2] = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+                pf[mt][3] = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+            }
+            // ---- O += P V (V^T fragments through transposing ldmatrix)
+            const int vrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                const int dim = np * 16 + (lane >> 4) * 8;
+                const uint32_t addr = vt + (dim >> 6) * HALF_BYTES + swz128(vrow, (dim & 63) >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(addr, b0, b1, b2, b3);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    mma_bf16_16816(o[mt][2 * np], pf[mt], b0, b1);
+                    mma_bf16_16816(o[mt][2 * np + 1], pf[mt], b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+    }
+
+    __syncthreads();
+    if (*s_err) {
+        // Let copies already issued land before the CTA's shared memory is released.
+        if (warp == NCW && lane == 0) {
+            for (int i = issued - STAGES < 0 ? 0 : issued - STAGES; i < issued; ++i)
+                mbar_wait_bounded(smem_u32(&full[i % STAGES]), (i / STAGES) & 1);
+        }
+        __syncthreads();
+        return;
+    }
+
+    // ---------------- merge the four consumer warps ----------------
+    float* Om = (float*)smem;                                    // [NCW][MT*16][D]
+    float2* ML = (float2*)(smem + NCW * MT * 16 * D * 4);        // [NCW][MT*16]
+    if (warp < NCW) {
+        const int qa = lane >> 2, qc = (lane & 3) * 2;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                float lr = l[mt][rr];
+                lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+                lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+                const int row = mt * 16 + qa + rr * 8;
+                float* dst = Om + ((size_t)warp * MT * 16 + row) * D;
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                    *(float2*)(dst + n * 8 + qc) = make_float2(o[mt][n][2 * rr], o[mt][n][2 * rr + 1]);
+                if ((lane & 3) == 0) ML[warp * MT * 16 + row] = make_float2(m[mt][rr], lr);
+            }
+        }
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < G * D; u += THREADS) {
+        const int g = u / D, dim = u - g * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ML[w * MT * 16 + g].x);
+        float O = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float2 ml = ML[w * MT * 16 + g];
+            const float f = fast_exp2(ml.x - M);
+            O += Om[((size_t)w * MT * 16 + g) * D + dim] * f;
+            L += ml.y * f;
+        }
+        const int64_t qh = (int64_t)b * a.Hq + hkv * G + g;
+        if (nsplit_lane == 1) {
+            a.out[qh * D + dim] = O / L;
+        } else {
+            const int64_t idx = qh * a.max_splits + split;
+            a.part_o[idx * D + dim] = O;
+            if (dim == 0) a.part_ml[idx] = make_float2(M, L);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
+    const int qh = blockIdx.x;
+    const int b = qh / a.Hq;
+    const int t = a.len[b] + 1;
+    const int ns = (t + a.split_rows - 1) / a.split_rows;
+    if (ns <= 1) return;
+    const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
+    float L = 0.f, O = 0.f;
+    const float* po = a.part_o + (int64_t)qh * a.max_splits * D + threadIdx.x;
+    for (int s = 0; s < ns; ++s) {
+        const float f = fast_exp2(ml[s].x - M);
+        L += ml[s].y * f;
+        O += po[(int64_t)s * D] * f;
+    }
+    a.out[(int64_t)qh * D + threadIdx.x] = O / L;
+}
+
+template <int MT>
+cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
+    constexpr int SMEM = smem_bytes<Cfg<MT>::STAGES>();
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid(a.max_splits, a.B * a.Hkv);
+    decode_bf16_kernel<MT><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s) {
+    decode_combine_kernel<<<a.B * a.Hq, 128, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg<2>::MINB; }
+
+cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s) {
+    const int G = a.Hq / a.Hkv;
+    if (G <= 16) return launch_mt<1>(a, s);
+    if (G <= 32) return launch_mt<2>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

@@ -1,0 +1,75 @@
+// Device helpers shared by the kvc kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvc {
+
+// Error bits written to the handle's device error word.
+enum DeviceError : uint32_t {
+    DEV_ERR_SLOT = 1u,        // an append slot or position fell outside its buffer
+    DEV_ERR_WAIT_TIMEOUT = 2u,// a bounded mbarrier wait gave up
+    DEV_ERR_TMEM = 4u         // tensor-memory allocation returned an unusable address
+};
+
+// ---- storage dtype traits ------------------------------------------------
+
+template <typename T> struct Storage;
+template <> struct Storage<__nv_bfloat16> {
+    __device__ static double to_f64(__nv_bfloat16 x) { return (double)__bfloat162float(x); }
+    __device__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+template <> struct Storage<float> {
+    __device__ static double to_f64(float x) { return (double)x; }
+    __device__ static float to_f32(float x) { return x; }
+};
+template <> struct Storage<double> {
+    __device__ static double to_f64(double x) { return x; }
+    __device__ static float to_f32(double x) { return (float)x; }
+};
+
+// Round a double to the nearest bfloat16, ties to even, in one rounding.
+// Truncate to binary32 (toward zero), then make the result "sticky" by setting
+// the lowest significand bit when the truncation was inexact (round-to-odd at
+// 24 bits), then round to nearest-even at 8 bits.  Rounding to odd at a
+// precision at least two bits wider than the target and then rounding to
+// nearest gives the correctly rounded result (Boldo & Melquiond, "Emulation of
+// FMA and correctly rounded sums: proved algorithms using rounding to odd").
+__device__ __forceinline__ __nv_bfloat16 f64_to_bf16_rn(double x) {
+    float t = __double2float_rz(x);
+    uint32_t bits = __float_as_uint(t);
+    if ((double)t != x && (bits & 0x7f800000u) != 0x7f800000u) bits |= 1u;
+    return __float2bfloat16_rn(__uint_as_float(bits));
+}
+
+template <typename T> __device__ __forceinline__ T from_f64_rn(double x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f64_rn<__nv_bfloat16>(double x) { return f64_to_bf16_rn(x); }
+template <> __device__ __forceinline__ float from_f64_rn<float>(double x) { return __double2float_rn(x); }
+template <> __device__ __forceinline__ double from_f64_rn<double>(double x) { return x; }
+
+// RoPE rotation of one interleaved pair in float64 with every product and sum
+// rounded separately (no fused multiply-add), so that the result equals the
+// plain IEEE evaluation of (x c - y s, x s + y c).
+__device__ __forceinline__ void rope_pair_f64(double x, double y, double c, double s,
+                                              double& xr, double& yr) {
+    xr = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
+    yr = __dadd_rn(__dmul_rn(x, s), __dmul_rn(y, c));
+}
+
+// ---- warp reductions -------------------------------------------------------
+
+template <typename A> __device__ __forceinline__ A warp_sum(A v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace kvc

@@ -1,0 +1,160 @@
+// Internal state of a kvc handle and the launchers of its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+// Host-pinned -> device staging of small per-call argument arrays (start
+// positions, chunk lengths, cuts, work lists).  Each slot is reused only after
+// the event recorded behind its consumers has completed.
+struct ArgRing {
+    static constexpr int kSlots = 8;
+    void* host[kSlots] = {};
+    void* dev[kSlots] = {};
+    size_t cap[kSlots] = {};
+    cudaEvent_t done[kSlots] = {};
+    bool pending[kSlots] = {};
+    int next = 0;
+    int cur = -1;
+
+    cudaError_t init();
+    void destroy();
+    // Returns a host staging buffer of at least `bytes` for the next slot.
+    cudaError_t acquire(size_t bytes, void** host_ptr);
+    // Enqueues the copy of the acquired slot; *dev_ptr is its device copy.
+    cudaError_t upload(size_t bytes, cudaStream_t stream, void** dev_ptr);
+    // Records the slot's release behind the work enqueued so far on `stream`.
+    cudaError_t release(cudaStream_t stream);
+};
+
+struct Handle {
+    kvc_config cfg{};
+    int max_positions = 0;
+    size_t elem_size = 0;       // bytes per storage element
+    size_t layer_elems = 0;     // B * H_kv * C * d_h
+    void* K = nullptr;          // [L][B][H_kv][C][d_h]
+    void* V = nullptr;
+    int32_t* positions = nullptr;  // [L][B][C]
+    int32_t* len_d = nullptr;      // [L][B]
+    int32_t* next_d = nullptr;     // [L][B]
+    double2* rope = nullptr;       // [max_positions][d_h/2] (cos, sin), or null when rope_base == 0
+    uint32_t* err_d = nullptr;     // device error word
+    unsigned long long* nonfinite_d = nullptr;  // first non-finite flat index of key [0] and value [1]
+    unsigned long long* nonfinite_h = nullptr;  // pinned mirror
+
+    std::vector<int32_t> len_h, next_h;  // host mirrors [L][B]
+
+    // decode scratch
+    void* qrot = nullptr;          // [B][H_q][d_h] float (bf16/f32 storage) or double (f64)
+    float* part_o = nullptr;       // [B*H_q][splits][d_h]
+    float2* part_ml = nullptr;     // [B*H_q][splits] (max in log2 units, sum)
+    size_t part_splits = 0;        // splits the partial buffers hold per query head
+    // prefill scratch
+    void* qrot_chunk = nullptr;    // [B][H_q][S][d_h] rotated queries of a chunk
+    size_t qrot_chunk_bytes = 0;
+    int* work_counter = nullptr;   // dynamic tile scheduler counter
+
+    // TMA descriptors over each layer's keys and values (bf16, d_h = 128)
+    std::vector<CUtensorMap> tmap_k, tmap_v;
+    bool have_tmaps = false;
+
+    ArgRing ring;
+    std::string last_error;
+
+    // per-family launch counters and optional CUDA-event timing
+    struct Timer {
+        std::vector<cudaEvent_t> start, stop;
+        size_t used = 0;
+        double ms = 0;
+        int64_t launches = 0;
+    } timers[KVC_KERNEL_COUNT];
+    bool timing = false;
+
+    // options
+    int64_t opt_split_rows = 0;
+    int64_t opt_force_generic = 0;
+    int64_t opt_suffix_kernel = 0;
+
+    int B() const { return cfg.batch; }
+    int Hq() const { return cfg.heads_q; }
+    int Hkv() const { return cfg.heads_kv; }
+    int C() const { return cfg.capacity; }
+    int D() const { return cfg.head_dim; }
+    char* K_layer(int l) const { return (char*)K + (size_t)l * layer_elems * elem_size; }
+    char* V_layer(int l) const { return (char*)V + (size_t)l * layer_elems * elem_size; }
+    int32_t* pos_layer(int l) const { return positions + (size_t)l * cfg.batch * cfg.capacity; }
+    int32_t* len_layer(int l) const { return len_d + (size_t)l * cfg.batch; }
+    int32_t* next_layer(int l) const { return next_d + (size_t)l * cfg.batch; }
+};
+
+// ---- kernel launchers (each returns the launch status) ----------------------
+
+struct AppendLaunch {
+    const void* q; const void* k; const void* v;   // [B,H_q,S,d], [B,H_kv,S,d]
+    void* K; void* V; int32_t* positions;          // one layer's storage
+    const int32_t* slot0;    // [B] device: slot of row 0 (the old length)
+    const int32_t* pos0;     // [B] device: position of row 0
+    const int32_t* seqlen;   // [B] device, or null: S rows each
+    void* qrot;              // [B,H_q,S,d] rotated queries
+    int qrot_kind;           // 0 = float, 1 = double, 2 = bf16
+    const double2* rope;     // null: no rotation
+    uint32_t* err;
+    int B, Hq, Hkv, S, C, d, max_positions;
+};
+cudaError_t launch_rope_append(int dtype, const AppendLaunch& a, cudaStream_t s);
+
+struct GenericAttendLaunch {
+    const void* qrot;        // [B,H_q,S,d] float or double
+    const void* K; const void* V;
+    const int32_t* slot0;    // [B] device: slot of row 0
+    const int32_t* seqlen;   // [B] device or null
+    void* out;               // [B,H_q,S,d] float or double
+    int B, Hq, Hkv, S, C, d;
+};
+cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaStream_t s);
+
+struct DecodeLaunch {
+    const CUtensorMap* tmK; const CUtensorMap* tmV;
+    const float* qrot;       // [B,H_q,128]
+    const int32_t* len;      // [B] old length: t = len + 1
+    float* part_o; float2* part_ml;
+    float* out;              // [B,H_q,128]
+    uint32_t* err;
+    int B, Hq, Hkv, C, split_rows, max_splits;
+};
+cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s);
+cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);
+int decode_bf16_ctas_per_sm(int group);
+
+cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,
+                          int uniform_rows, int B, cudaStream_t s);
+cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
+                            cudaStream_t s);
+cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,
+                             cudaStream_t s);
+
+// Tensor-core suffix-chunk kernel (bf16, d_h = 128).
+struct SuffixLaunch {
+    CUtensorMap tmQ, tmK, tmV;   // Q: [B*H_q*S, 128] bf16 rotated queries; K/V: one layer
+    const int32_t* slot0;        // [B] device, slot of suffix row 0 (= cut)
+    const int32_t* seqlen;       // [B] device
+    const int4* work;            // tiles: (b, h, q_tile, n_kv_tiles), longest first
+    int n_work;
+    int* counter;                // zeroed before launch
+    float* out;                  // [B,H_q,S,128]
+    uint32_t* err;
+    int B, Hq, Hkv, S, C;
+    float scale_log2;            // log2(e) / sqrt(d_h)
+};
+cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);
+int suffix_tc_grid(int sms);
+
+}  // namespace kvc

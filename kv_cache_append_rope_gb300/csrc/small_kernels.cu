@@ -1,0 +1,72 @@
+// Length bookkeeping and input checks.
+//
+// commit:   [Ch37] "Bind the state, calculate completely, then commit" -- the
+//           logical length grows only after the attention of the call has been
+//           enqueued; every length and next position of one layer is updated
+//           by one thread, so no kernel of the same call reads a half-updated
+//           length.
+// truncate: [LCP5] listing under "哪些东西必须一起裁剪" -- length and next
+//           position of every layer become cut; stored rows are not touched.
+// nonfinite: [Ch37] listing "Own a fixed layer-bound cache, append one checked
+//           row, and reset logical length" rejects non-finite keys and values
+//           before they are stored; this finds the first such flat index.
+#include "device_common.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+__global__ void commit_kernel(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,
+                              int uniform_rows, int B) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int n = seqlen ? seqlen[b] : uniform_rows;
+    const int p = pos0[b];
+    len[b] += n;
+    next[b] = p + n;
+}
+
+cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,
+                          int uniform_rows, int B, cudaStream_t s) {
+    commit_kernel<<<(B + 127) / 128, 128, 0, s>>>(len, next, pos0, seqlen, uniform_rows, B);
+    return cudaGetLastError();
+}
+
+__global__ void truncate_kernel(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B) {
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= layers * B) return;
+    const int c = cut[u % B];
+    len[u] = c;
+    next[u] = c;
+}
+
+cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
+                            cudaStream_t s) {
+    const int n = layers * B;
+    truncate_kernel<<<(n + 127) / 128, 128, 0, s>>>(len, next, cut, layers, B);
+    return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void nonfinite_kernel(const T* x, int64_t n, unsigned long long* first) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const double v = Storage<T>::to_f64(x[i]);
+        if (!isfinite(v)) atomicMin(first, (unsigned long long)i);
+    }
+}
+
+cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,
+                             cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    switch (dtype) {
+        case KVC_BF16: nonfinite_kernel<<<(unsigned)blocks, 256, 0, s>>>((const __nv_bfloat16*)x, n, first); break;
+        case KVC_F32: nonfinite_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float*)x, n, first); break;
+        case KVC_F64: nonfinite_kernel<<<(unsigned)blocks, 256, 0, s>>>((const double*)x, n, first); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -13,9 +13,9 @@ Definitions followed (cited by page title and section / listing title):
 * [Ch37] "From causal attention to managed LLM inference state": the
   reference is the full-prefix masked scaled dot-product attention of
   "Attention Is All You Need".
-* [LCP5] "在本例的因果注意力中..." (section "先看一次历史编辑") and the
-  listing under "哪些东西必须一起裁剪": after truncation to ``cut`` the suffix
-  is computed against the retained prefix, continuing at position ``cut``.
+* [LCP5] section "先看一次历史编辑" and the listing under
+  "哪些东西必须一起裁剪": after truncation to ``cut`` the suffix is computed
+  against the retained prefix, continuing at position ``cut``.
 
 Readings where the pages are silent (each also listed in the design doc):
 

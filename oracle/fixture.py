@@ -16,26 +16,14 @@ then commit").  These rows are a reading (the unpublished weights and inputs
 could differ while giving the same projections); the printed numbers are the
 pins.
 
-``random_variant`` is the other reading: Wq, Wk, Wv, Wo ~ N(0, 1/D) and inputs
-~ N(0, 1) drawn from ``default_rng(seed)`` in that order, pinned only by
-incremental == full-prefix.
+The other reading draws Wq, Wk, Wv, Wo ~ N(0, 1/D) and inputs ~ N(0, 1); it is
+pinned only by incremental == full-prefix.
 """
-
-import math
 
 import numpy as np
 
 D, H, DH, C = 4, 2, 2, 4
 ROPE_BASE = 10000.0
-
-
-def page_head_rows():
-    """Projected per-head rows [3 steps, H, d_h] (q = k = v), unrotated."""
-    rows = np.zeros((3, H, DH))
-    for p in range(3):
-        rows[p, 0] = (math.cos(p), -math.sin(p))
-    rows[:, 1] = [(1.0, 0.0), (0.0, 1.0), (1.0, 1.0)]
-    return rows
 
 
 def head_swap_projection():
@@ -53,12 +41,3 @@ def split_heads(x):
 def merge_heads(o):
     """[B, H, d_h] -> [B, D]."""
     return o.reshape(o.shape[0], H * DH)
-
-
-def random_variant(seed=0, steps=3):
-    """Weights and inputs of the random reading: (Wq, Wk, Wv, Wo, x [steps, D])."""
-    rng = np.random.default_rng(seed)
-    std = math.sqrt(1.0 / D)
-    Wq, Wk, Wv, Wo = (rng.normal(0.0, std, (D, D)) for _ in range(4))
-    x = rng.normal(0.0, 1.0, (steps, D))
-    return Wq, Wk, Wv, Wo, x

@@ -11,14 +11,12 @@ reading (listed in DESIGN.md):
 * per layer: q, k, v = h Wq, h Wk, h Wv (16 x 16), a = causal softmax(q k^T
   / sqrt(16)) v, h <- h + tanh(a Wo);
 * the output is the final hidden state of every computed row;
-* weights ~ N(0, 1/16) drawn from numpy ``default_rng(seed)`` in the order
-  E, then (Wq, Wk, Wv, Wo) of layer 0, then of layer 1.  No RoPE.
+* no RoPE.  The weights (E [vocab, d] and per layer Wq, Wk, Wv, Wo) are
+  inputs: the tests draw them ~ N(0, 1/16) from the seeded generator module.
 
 The cache is the dict of the truncation listing under "哪些东西必须一起裁剪":
 {'next_position': int, 'layers': [(k [T, d], v [T, d], positions [T])]}.
 """
-
-import math
 
 import numpy as np
 
@@ -37,12 +35,11 @@ def sinusoidal_positions(positions, d):
 
 
 class ToyDecoder:
-    def __init__(self, seed, d=16, vocab=32, layers=2):
-        rng = np.random.default_rng(seed)
-        std = math.sqrt(1.0 / 16.0)
-        self.d, self.vocab, self.n_layers = d, vocab, layers
-        self.E = rng.normal(0.0, std, (vocab, d))
-        self.W = [tuple(rng.normal(0.0, std, (d, d)) for _ in range(4)) for _ in range(layers)]
+    def __init__(self, E, W):
+        self.E = np.asarray(E, dtype=np.float64)
+        self.W = [tuple(np.asarray(w, dtype=np.float64) for w in layer) for layer in W]
+        self.vocab, self.d = self.E.shape
+        self.n_layers = len(self.W)
 
     def embed(self, ids, positions):
         return self.E[np.asarray(ids, dtype=np.int64)] + sinusoidal_positions(positions, self.d)

@@ -1,0 +1,114 @@
+"""Decode-step parity of libkvc against the float64 oracle.
+
+Every call goes through the C ABI (kv_cache_append_rope_gb300.kvc).  Inputs are
+seeded; the oracle sees exactly the storage-dtype values the GPU sees.
+Tolerances: f64 1e-12, f32 1e-5, bf16 2e-2 (max abs); stored rows, positions and
+lengths bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import TOL, device_tensor, need_gpu, storage_np, to_np
+from kv_cache_append_rope_gb300 import _lib as L
+from kv_cache_append_rope_gb300 import workloads as W
+from kv_cache_append_rope_gb300.kvc import KVCache
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+BASE = 10000.0
+
+
+def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0):
+    """Prefill ragged prefixes, run `steps` decode steps; return (cache, outs, inputs)."""
+    need_gpu()
+    B = len(L0)
+    T = max(L0) + steps
+    q = W.normal_np((B, Hq, T, D), seed)
+    k = W.normal_np((B, Hkv, T, D), seed + 1)
+    v = W.normal_np((B, Hkv, T, D), seed + 2)
+    qd, kd, vd = (device_tensor(x, dtype) for x in (q, k, v))
+    q, k, v = to_np(qd), to_np(kd), to_np(vd)        # the exact values the GPU sees
+    cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE)
+    if generic:
+        cache.set_option(L.OPT_FORCE_GENERIC, 1)
+    if split_rows:
+        cache.set_option(L.OPT_DECODE_SPLIT_ROWS, split_rows)
+    S = max(max(L0), 1)
+    cache.prefill_suffix(0, qd[:, :, :S].contiguous(), kd[:, :, :S].contiguous(), vd[:, :, :S].contiguous(),
+                         seqlen=L0, out=False)
+    outs = []
+    for i in range(steps):
+        idx = torch.tensor([l + i for l in L0], device="cuda")
+        sel = lambda x: x[torch.arange(B, device="cuda"), :, idx][:, :, None, :].contiguous()
+        outs.append(to_np(cache.append_attend(0, sel(qd), sel(kd), sel(vd))))
+    torch.cuda.synchronize()
+    return cache, outs, (q, k, v)
+
+
+def check_against_oracle(dtype, cache, outs, qkv, L0, steps):
+    q, k, v = qkv
+    B = len(L0)
+    worst = 0.0
+    Ks, Vs, Ps = storage_np(cache)
+    for b in range(B):
+        n = L0[b] + steps
+        ref = A.decode_steps_reference(np.transpose(q[b, :, L0[b]:n], (1, 0, 2)), k[b, :, :n], v[b, :, :n],
+                                       L0[b], BASE, dtype)
+        got = np.stack([o[b, :, 0] for o in outs])
+        worst = max(worst, np.abs(got - ref).max())
+        K, V = A.stored_rows(k[b, :, :n], v[b, :, :n], np.arange(n)[None], BASE, dtype)
+        np.testing.assert_array_equal(Ks[b, :, :n], K)          # rotated, rounded keys: bit-exact
+        np.testing.assert_array_equal(Vs[b, :, :n], V)
+        assert Ps[b, :n].tolist() == list(range(n))
+    assert worst <= TOL[dtype], worst
+    lens, nexts = cache.get_lengths(0)
+    assert lens == [l + steps for l in L0] and nexts == lens
+    cache.check()
+    return worst
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,generic", [
+    ("f64", 16, 4, 2, True),
+    ("f32", 64, 4, 4, True),
+    ("bf16", 64, 4, 1, True),
+    ("bf16", 128, 4, 4, True),
+    ("bf16", 128, 4, 4, False),
+    ("bf16", 128, 8, 2, False),
+])
+def test_decode_matches_oracle(dtype, D, Hq, Hkv, generic):
+    L0, steps = [0, 70, 200], 5
+    cache, outs, qkv = run_decode(dtype, D, Hq, Hkv, L0, steps, C=300, generic=generic)
+    check_against_oracle(dtype, cache, outs, qkv, L0, steps)
+
+
+@pytest.mark.parametrize("Hkv", [8, 1])
+def test_gqa_mqa_fast_path(Hkv):
+    L0, steps = [1, 100, 257, 63], 3
+    cache, outs, qkv = run_decode("bf16", 128, 32, Hkv, L0, steps, C=400)
+    check_against_oracle("bf16", cache, outs, qkv, L0, steps)
+
+
+def test_split_sizes_agree():
+    """One split, two, several and one per 64 rows: same outputs (log-sum-exp merge)."""
+    L0, steps = [5, 333, 700], 2
+    results = []
+    for rows in [1024, 448, 128, 64, 0]:
+        cache, outs, qkv = run_decode("bf16", 128, 8, 2, L0, steps, C=800, split_rows=rows)
+        check_against_oracle("bf16", cache, outs, qkv, L0, steps)
+        results.append(np.stack(outs))
+    for r in results[1:]:
+        assert np.abs(r - results[0]).max() < 5e-3
+
+
+def test_generic_and_fast_paths_agree():
+    L0, steps = [3, 150], 3
+    _, a, _ = run_decode("bf16", 128, 4, 4, L0, steps, C=200, generic=True)
+    _, b, _ = run_decode("bf16", 128, 4, 4, L0, steps, C=200, generic=False)
+    assert np.abs(np.stack(a) - np.stack(b)).max() < 1e-2
+
+
+def test_first_step_returns_the_value():
+    """t = 1: the single weight is 1 and the output is the (rounded) new value row."""
+    cache, outs, (q, k, v) = run_decode("bf16", 128, 4, 4, [0], 1, C=8)
+    np.testing.assert_allclose(outs[0][0, :, 0], v[0, :, 0], atol=1e-6)

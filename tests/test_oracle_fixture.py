@@ -5,10 +5,11 @@ from golden_data import ch37_trace
 from oracle import attention as A
 from oracle import fixture as F
 from oracle.rope import rotate
+from kv_cache_append_rope_gb300 import workloads as W
 
 
 def _replay():
-    rows = F.page_head_rows()
+    rows = W.fixture_head_rows()
     cache = A.LayerCache(1, F.H, F.H, F.C, F.DH, "f64", F.ROPE_BASE)
     outs, weights, shapes = [], [], []
     for p in range(3):
@@ -36,7 +37,7 @@ def test_fixture_trace_matches_printed_values():
 
 
 def test_fixture_incremental_equals_full_prefix():
-    rows = F.page_head_rows()
+    rows = W.fixture_head_rows()
     _, outs, _, _ = _replay()
     for p in range(3):
         hist = np.transpose(rows[:p + 1], (1, 0, 2))          # [H, t, d_h]
@@ -60,7 +61,7 @@ def test_fixture_work_counts_and_reset():
     cache.reset()
     assert (before, int(cache.length[0])) == (int(reset["before"]), int(reset["after"]))
     assert id(cache.K) == Kid and np.array_equal(cache.K, K) and np.array_equal(cache.V, V)
-    rows = F.page_head_rows()
+    rows = W.fixture_head_rows()
     replay = [F.merge_heads(cache.append_attend(rows[p][None], rows[p][None], rows[p][None]))
               @ F.head_swap_projection() for p in range(3)]
     for a, b in zip(replay, outs):
@@ -68,7 +69,7 @@ def test_fixture_work_counts_and_reset():
 
 
 def test_random_variant_incremental_equals_full_prefix():
-    Wq, Wk, Wv, Wo, x = F.random_variant(0)
+    Wq, Wk, Wv, Wo, x = W.fixture_random_variant(0)
     cache = A.LayerCache(1, F.H, F.H, F.C, F.DH, "f64", F.ROPE_BASE)
     q = F.split_heads(x @ Wq)            # [steps, H, d_h]
     k = F.split_heads(x @ Wk)

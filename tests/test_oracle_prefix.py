@@ -8,6 +8,7 @@ import pytest
 from golden_data import lcp5_table
 from oracle import prefix as P
 from oracle.toy_decoder import ToyDecoder
+from kv_cache_append_rope_gb300.workloads import toy_decoder_weights
 
 CACHED = list(range(1, 9))
 TAIL = [9, 10, 11, 12]
@@ -91,7 +92,7 @@ CONDITIONS = ["append", "edit_first", "edit_fifth", "edit_eighth", "shortened", 
 @pytest.mark.parametrize("seed", [7, 11, 23])
 @pytest.mark.parametrize("condition", CONDITIONS)
 def test_toy_decoder_reuse_equals_recompute_and_stale_control(seed, condition):
-    model = ToyDecoder(seed)
+    model = ToyDecoder(*toy_decoder_weights(seed))
     cached, query = query_for(condition)
     _, cache = model.forward_full(cached)
     cut = P.lcp_cut(cached, query)
@@ -115,7 +116,7 @@ def test_toy_decoder_reuse_equals_recompute_and_stale_control(seed, condition):
 
 
 def test_toy_decoder_is_causal():
-    model = ToyDecoder(7)
+    model = ToyDecoder(*toy_decoder_weights(7))
     a, _ = model.forward_full([1, 2, 3, 4, 5, 6])
     b, _ = model.forward_full([1, 2, 3, 30, 31, 0])
     np.testing.assert_array_equal(a[:3], b[:3])
