@@ -51,6 +51,8 @@ def parse():
                    choices=["mha_decode", "gqa_decode", "mqa_decode", "suffix", "all"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--batch", type=int, default=0,
+                   help="override B of a decode workload (a smaller case for ncu captures; not a bench line)")
     return p.parse_args()
 
 
@@ -135,10 +137,12 @@ def gpu_index(local_rank):
 # ----------------------------------------------------------------- decode workloads
 
 class DecodeBench:
-    def __init__(self, name, device):
+    def __init__(self, name, device, batch=0):
         from kv_cache_append_rope_gb300 import workloads as W
         from kv_cache_append_rope_gb300.kvc import KVCache
         cfg = dict(W.CONFIGS[name])
+        if batch:
+            cfg["B"] = batch
         self.name, self.cfg, self.device = name, cfg, device
         B, Hq, Hkv, D, C, steps = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["C"], cfg["steps"]
         self.L0 = W.old_lengths(cfg["seed"], B, cfg["lo"], cfg["hi"], C, steps)
@@ -318,8 +322,8 @@ class SuffixBench:
 
 # ----------------------------------------------------------------- driver
 
-def make_bench(name, device):
-    return SuffixBench(device) if name == "suffix" else DecodeBench(name, device)
+def make_bench(name, device, batch=0):
+    return SuffixBench(device) if name == "suffix" else DecodeBench(name, device, batch)
 
 
 def dist_setup(args):
@@ -360,7 +364,7 @@ def run_ours(args, name, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     hbm, tflops, peak_kind = peaks()
-    bench = make_bench(name, device)
+    bench = make_bench(name, device, args.batch)
     cache = bench.cache
     for _ in range(args.warmup):
         bench.step()
