@@ -230,6 +230,34 @@ kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** v
  */
 kvc_status kvc_check(kvc_handle* h, void* stream);
 
+/*
+ * Decode attention that allocates nothing.  The pages have no counterpart to
+ * this entry point; it exists for callers that cannot let a library call
+ * cudaMalloc -- a serving engine that owns all device memory through its own
+ * arena (so a request never fails halfway on an out-of-memory error and no
+ * allocation synchronises the device under running streams), or a host
+ * framework that hands out only buffers it created.  It runs the split-K
+ * decode kernel of kvc_append_attend over a cache the caller owns, with the
+ * kernel's scratch in one static 8 MiB device array of the library (held on
+ * every GPU that loads the library until the process exits).
+ *   keys, values [B, H_kv, C, 128] bf16 device: rotated keys and values
+ *   q_rot        [B, H_q, 128] f32 device: the new queries, already rotated
+ *   lengths      [B] HOST int32: rows 0 .. lengths[b]-1 of sequence b are
+ *                attended (1 <= lengths[b] <= C)
+ *   out          [B, H_q, 128] f32 device
+ * bf16 storage and d_h = 128 only; H_q / H_kv <= 32; B <= 4096 and
+ * B * H_q <= 16099 (what the array holds) -- larger sizes return
+ * KVC_ERR_CONFIG, lengths outside [1, C] KVC_ERR_FULL, NULL pointers
+ * KVC_ERR_NULL, a failed CUDA call KVC_ERR_CUDA.  Runs on the current device.
+ * The first call on a device resolves the array's device address there (make
+ * it before any stream capture).  Every call shares the array and it keeps the
+ * last call's contents; calls that overlap on the GPU race on it, so order
+ * them on one stream.
+ */
+kvc_status kvc_decode_attend_noalloc(const void* keys, const void* values, const float* q_rot,
+                                     const int32_t* lengths, float* out, int32_t batch, int32_t heads_q,
+                                     int32_t heads_kv, int32_t capacity, void* stream);
+
 /* Tuning / test options (kvc_set_option). */
 typedef enum kvc_option {
     KVC_OPT_DECODE_SPLIT_ROWS = 1, /* key rows per decode split (multiple of 64); 0 = automatic */

@@ -30,7 +30,7 @@ KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "gen
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
            "kvc_destroy", "kvc_append_attend", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
            "kvc_lcp", "kvc_get_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
-           "kvc_kernel_stats", "kvc_reset_stats")
+           "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
 
 
 class KVCError(RuntimeError):
@@ -83,6 +83,8 @@ def _load():
         "kvc_kernel_stats": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
                                             ctypes.POINTER(ctypes.c_int64)]),
         "kvc_reset_stats": (ctypes.c_int, [_P]),
+        "kvc_decode_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _I32P, _P, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_int32, ctypes.c_int32, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
