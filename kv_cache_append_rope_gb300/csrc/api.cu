@@ -445,11 +445,15 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
     if (c.dtype == KVC_BF16 && c.head_dim == 128) {
         h->tmap_k.resize(c.layers);
         h->tmap_v.resize(c.layers);
+        h->tmap_k128.resize(c.layers);
+        h->tmap_v128.resize(c.layers);
         bool all = true;
         const uint64_t rows = (uint64_t)c.batch * c.heads_kv * c.capacity;
         for (int l = 0; l < c.layers && all; ++l)
             all = encode_rows_map(&h->tmap_k[l], h->K_layer(l), rows, 64) &&
-                  encode_rows_map(&h->tmap_v[l], h->V_layer(l), rows, 64);
+                  encode_rows_map(&h->tmap_v[l], h->V_layer(l), rows, 64) &&
+                  encode_rows_map(&h->tmap_k128[l], h->K_layer(l), rows, 128) &&
+                  encode_rows_map(&h->tmap_v128[l], h->V_layer(l), rows, 128);
         h->have_tmaps = all;
     }
     h->len_h.assign(LB, 0);
@@ -645,8 +649,25 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         const int64_t nk = (int64_t)B * Hkv * S * D;
         if ((st = check_nonfinite(h, k, v, nk, nk, s)) != KVC_OK) return st;
     }
-    // qrot scratch for the chunk (accumulator dtype for the generic kernel)
-    const size_t acc = dt == KVC_F64 ? 8 : 4;
+    // Attention kernel: the tensor-core tile kernel for bf16 with d_h = 128, else the generic one.
+    const bool tc_ok = dt == KVC_BF16 && D == 128 && h->have_tmaps;
+    if (out && h->opt_suffix_kernel == 2 && !tc_ok)
+        return fail(h, KVC_ERR_CONFIG, "the tensor-core suffix kernel needs bf16 storage and d_h = 128");
+    const bool use_tc = out && tc_ok && !h->opt_force_generic && h->opt_suffix_kernel != 1;
+    std::vector<int4> work;
+    if (use_tc) {
+        for (int b = 0; b < B; ++b)
+            for (int hq = 0; hq < Hq; ++hq)
+                for (int qt = 0; qt * 128 < sl_h[b]; ++qt) {
+                    const int q_end = std::min(qt * 128 + 128, sl_h[b]);
+                    work.push_back(make_int4(b, hq, qt, (lenh[b] + q_end + 127) / 128));
+                }
+        std::stable_sort(work.begin(), work.end(), [](const int4& x, const int4& y) { return x.w > y.w; });
+        if ((uint64_t)B * Hq * S > (uint64_t)INT32_MAX)
+            return fail(h, KVC_ERR_ELEMENT_OVERFLOW, "B * H_q * S must fit in 31 bits for the tile kernel");
+    }
+    // qrot scratch for the chunk: bf16 for the tile kernel, the accumulator dtype for the generic one
+    const size_t acc = use_tc ? 2 : (dt == KVC_F64 ? 8 : 4);
     const size_t qbytes = (size_t)B * Hq * S * D * acc;
     if (out && qbytes > h->qrot_chunk_bytes) {
         cudaStreamSynchronize(s);
@@ -659,25 +680,41 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         }
         h->qrot_chunk_bytes = qbytes;
     }
+    const size_t arg_bytes = (2 * B * sizeof(int32_t) + 15) / 16 * 16;
+    const size_t ring_bytes = arg_bytes + work.size() * sizeof(int4);
     void* hp;
-    KVC_CUDA(h, h->ring.acquire(2 * B * sizeof(int32_t), &hp));
+    KVC_CUDA(h, h->ring.acquire(ring_bytes, &hp));
     memcpy(hp, st_h.data(), B * sizeof(int32_t));
     memcpy((int32_t*)hp + B, sl_h.data(), B * sizeof(int32_t));
+    if (!work.empty()) memcpy((char*)hp + arg_bytes, work.data(), work.size() * sizeof(int4));
     void* dp;
-    KVC_CUDA(h, h->ring.upload(2 * B * sizeof(int32_t), s, &dp));
+    KVC_CUDA(h, h->ring.upload(ring_bytes, s, &dp));
     const int32_t* start_d = (const int32_t*)dp;
     const int32_t* seqlen_d = start_d + B;
+    const int4* work_d = (const int4*)((const char*)dp + arg_bytes);
 
     AppendLaunch ap{};
     ap.q = out ? q->data : nullptr; ap.k = k->data; ap.v = v->data;
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
     ap.slot0 = h->len_layer(layer); ap.pos0 = start_d; ap.seqlen = seqlen_d;
-    ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = dt == KVC_F64 ? 1 : 0;
+    ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = use_tc ? 2 : (dt == KVC_F64 ? 1 : 0);
     ap.rope = h->rope; ap.err = h->err_d;
     ap.B = B; ap.Hq = out ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
     // Without an output the query heads are skipped (Hq = 0 in the launch).
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
-    if (out) {
+    if (out && use_tc && !work.empty()) {
+        SuffixLaunch sl{};
+        if (!encode_rows_map(&sl.tmQ, h->qrot_chunk, (uint64_t)B * Hq * S, 128))
+            return fail(h, KVC_ERR_CUDA, "cannot encode the query tensor map");
+        sl.tmK = h->tmap_k128[layer];
+        sl.tmV = h->tmap_v128[layer];
+        sl.slot0 = h->len_layer(layer); sl.seqlen = seqlen_d;
+        sl.work = work_d; sl.n_work = (int)work.size(); sl.counter = h->work_counter;
+        sl.out = (float*)out->data; sl.err = h->err_d;
+        sl.B = B; sl.Hq = Hq; sl.Hkv = Hkv; sl.S = S; sl.C = C;
+        sl.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+        KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc(sl, (int)work.size(), s); }));
+    } else if (out && !use_tc) {
         GenericAttendLaunch g{};
         g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = seqlen_d; g.out = out->data;

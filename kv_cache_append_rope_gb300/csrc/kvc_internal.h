@@ -62,8 +62,9 @@ struct Handle {
     size_t qrot_chunk_bytes = 0;
     int* work_counter = nullptr;   // dynamic tile scheduler counter
 
-    // TMA descriptors over each layer's keys and values (bf16, d_h = 128)
-    std::vector<CUtensorMap> tmap_k, tmap_v;
+    // TMA descriptors over each layer's keys and values (bf16, d_h = 128):
+    // 64-row boxes for decode, 128-row boxes for the suffix-chunk kernel
+    std::vector<CUtensorMap> tmap_k, tmap_v, tmap_k128, tmap_v128;
     bool have_tmaps = false;
 
     ArgRing ring;

@@ -25,16 +25,17 @@ def make_inputs(B, Hq, Hkv, T, D, dtype, seed):
     return qd, kd, vd
 
 
-@pytest.mark.parametrize("dtype,D,Hq,Hkv,kernel", [
-    ("f64", 16, 2, 2, 1),
-    ("f32", 32, 4, 2, 1),
-    ("bf16", 128, 4, 2, 1),
-    ("bf16", 128, 4, 4, 0),
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,kernel,T,cuts", [
+    ("f64", 16, 2, 2, 1, 300, [150, 0, 257]),
+    ("f32", 32, 4, 2, 1, 300, [150, 0, 257]),
+    ("bf16", 128, 4, 2, 1, 300, [150, 0, 257]),
+    ("bf16", 128, 4, 4, 0, 300, [150, 0, 257]),      # tensor-core tile kernel (automatic)
+    ("bf16", 128, 8, 2, 2, 300, [150, 0, 257]),      # tile kernel, grouped heads
+    ("bf16", 128, 2, 1, 2, 1500, [1200, 37, 640]),   # tile kernel, many key tiles per query tile
 ])
-def test_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel):
+def test_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, T, cuts):
     need_gpu()
-    B, T, C = 3, 300, 320
-    cuts = [150, 0, 257]
+    B, C = 3, T + 20
     qd, kd, vd = make_inputs(B, Hq, Hkv, T, D, dtype, seed=40)
     q, k, v = to_np(qd), to_np(kd), to_np(vd)
     cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE)
