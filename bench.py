@@ -52,7 +52,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=0,
-                   help="override B of a decode workload (a smaller case for ncu captures; not a bench line)")
+                   help="override B of a workload (a smaller case for ncu captures; not a bench line)")
     return p.parse_args()
 
 
@@ -240,10 +240,12 @@ class DecodeBench:
 # ----------------------------------------------------------------- suffix workload
 
 class SuffixBench:
-    def __init__(self, device):
+    def __init__(self, device, batch=0):
         from kv_cache_append_rope_gb300 import workloads as W
         from kv_cache_append_rope_gb300.kvc import KVCache
         c = dict(W.CONFIGS["suffix"])
+        if batch:
+            c["B"] = batch
         self.cfg, self.device = c, device
         B, H, D = c["B"], c["Hq"], c["D"]
         self.T = c["prefix"] + c["appended"]
@@ -309,7 +311,7 @@ class SuffixBench:
         b, h = int(np.argmax(self.cuts)), 0
         cut = self.cuts[b]
         S = self.seqlen[b]
-        rows = np.arange(0, S, max(1, S // 64))[:64]
+        rows = np.arange(0, S, max(1, S // 1536))[:1536]
         k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(), self.k[b, h, :S].double().cpu().numpy()])
         v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(), self.v[b, h, :S].double().cpu().numpy()])
         q = self.q[b, h:h + 1, :S].double().cpu().numpy()
@@ -323,7 +325,7 @@ class SuffixBench:
 # ----------------------------------------------------------------- driver
 
 def make_bench(name, device, batch=0):
-    return SuffixBench(device) if name == "suffix" else DecodeBench(name, device, batch)
+    return SuffixBench(device, batch) if name == "suffix" else DecodeBench(name, device, batch)
 
 
 def dist_setup(args):

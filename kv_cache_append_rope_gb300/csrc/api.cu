@@ -207,6 +207,7 @@ void free_all(kvc_handle* h) {
     cudaFree(h->len_d);
     cudaFree(h->next_d);
     cudaFree(h->rope);
+    cudaFree(h->rope_f);
     cudaFree(h->err_d);
     cudaFree(h->nonfinite_d);
     if (h->nonfinite_h) cudaFreeHost(h->nonfinite_h);
@@ -402,7 +403,8 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
               alloc(&h->qrot, (size_t)c.batch * c.heads_q * c.head_dim * acc) &&
               alloc((void**)&h->work_counter, 64);
     if (ok && c.rope_base > 0.0)
-        ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2));
+        ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2)) &&
+             alloc((void**)&h->rope_f, (size_t)maxpos * (c.head_dim / 2) * sizeof(float2));
     if (!ok) {
         free_all(h);
         delete h;
@@ -438,6 +440,11 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
                 tab[(size_t)p * half + j] = make_double2(std::cos(ang), std::sin(ang));
             }
         if ((e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(double2), cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return abort_cuda(e, "cudaMemcpy");
+        std::vector<float2> tabf(tab.size());
+        for (size_t i = 0; i < tab.size(); ++i) tabf[i] = make_float2((float)tab[i].x, (float)tab[i].y);
+        if ((e = cudaMemcpy(h->rope_f, tabf.data(), tabf.size() * sizeof(float2), cudaMemcpyHostToDevice)) !=
             cudaSuccess)
             return abort_cuda(e, "cudaMemcpy");
     }
@@ -560,7 +567,7 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
     ap.slot0 = h->len_layer(layer); ap.pos0 = h->next_layer(layer); ap.seqlen = nullptr;
     ap.qrot = h->qrot; ap.qrot_kind = dt == KVC_F64 ? 1 : 0;
-    ap.rope = h->rope; ap.err = h->err_d;
+    ap.rope = h->rope; ap.rope_f = h->rope_f; ap.err = h->err_d;
     ap.B = B; ap.Hq = Hq; ap.Hkv = Hkv; ap.S = 1; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
 
     int split_rows = 0, max_splits = 1;
@@ -662,7 +669,17 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
                     const int q_end = std::min(qt * 128 + 128, sl_h[b]);
                     work.push_back(make_int4(b, hq, qt, (lenh[b] + q_end + 127) / 128));
                 }
-        std::stable_sort(work.begin(), work.end(), [](const int4& x, const int4& y) { return x.w > y.w; });
+        // Group the query tiles of each (sequence, head) so they stream its K/V together
+        // (L2 reuse); groups by total work, longest first; inside a group longest first.
+        std::vector<int64_t> gw((size_t)B * Hq, 0);
+        for (const int4& t : work) gw[(size_t)t.x * Hq + t.y] += t.w;
+        std::stable_sort(work.begin(), work.end(), [&](const int4& x, const int4& y) {
+            const int64_t wx = gw[(size_t)x.x * Hq + x.y], wy = gw[(size_t)y.x * Hq + y.y];
+            if (wx != wy) return wx > wy;
+            if (x.x != y.x) return x.x < y.x;
+            if (x.y != y.y) return x.y < y.y;
+            return x.w > y.w;
+        });
         if ((uint64_t)B * Hq * S > (uint64_t)INT32_MAX)
             return fail(h, KVC_ERR_ELEMENT_OVERFLOW, "B * H_q * S must fit in 31 bits for the tile kernel");
     }
@@ -698,7 +715,7 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
     ap.slot0 = h->len_layer(layer); ap.pos0 = start_d; ap.seqlen = seqlen_d;
     ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = use_tc ? 2 : (dt == KVC_F64 ? 1 : 0);
-    ap.rope = h->rope; ap.err = h->err_d;
+    ap.rope = h->rope; ap.rope_f = h->rope_f; ap.err = h->err_d;
     ap.B = B; ap.Hq = out ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
     // Without an output the query heads are skipped (Hq = 0 in the launch).
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));

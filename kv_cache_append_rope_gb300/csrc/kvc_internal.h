@@ -46,6 +46,7 @@ struct Handle {
     int32_t* len_d = nullptr;      // [L][B]
     int32_t* next_d = nullptr;     // [L][B]
     double2* rope = nullptr;       // [max_positions][d_h/2] (cos, sin), or null when rope_base == 0
+    float2* rope_f = nullptr;      // the same table rounded to float32
     uint32_t* err_d = nullptr;     // device error word
     unsigned long long* nonfinite_d = nullptr;  // first non-finite flat index of key [0] and value [1]
     unsigned long long* nonfinite_h = nullptr;  // pinned mirror
@@ -107,6 +108,7 @@ struct AppendLaunch {
     void* qrot;              // [B,H_q,S,d] rotated queries
     int qrot_kind;           // 0 = float, 1 = double, 2 = bf16
     const double2* rope;     // null: no rotation
+    const float2* rope_f;    // the same table rounded to float32 (bf16 caches)
     uint32_t* err;
     int B, Hq, Hkv, S, C, d, max_positions;
 };

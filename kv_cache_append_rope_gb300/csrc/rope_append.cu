@@ -8,81 +8,173 @@
 //
 // One thread handles P interleaved pairs (16 bytes of bf16, 8 of f64) of one
 // row of one head of q, k or v.  Consecutive threads walk consecutive pairs of
-// a row, then rows, then heads, so loads and stores are coalesced.  The
-// rotation runs in float64 with separately rounded products and sums from a
-// float64 cos/sin table, and the result is rounded once to its destination
-// type, which makes the stored key bit-identical to the plain float64
-// definition rounded to the storage dtype.
+// a row, then rows, then heads, so loads and stores are coalesced.
+//
+// The stored key is defined as the float64 evaluation of (x c - y s, x s + y c)
+// -- every product and sum rounded separately, cos/sin from a float64 table --
+// rounded once to the storage dtype.  f32 and f64 caches evaluate exactly that.
+// bf16 caches (where float64 throughput would dominate a long chunk) evaluate
+// it in float32 and prove, element by element, that rounding to bf16 gives the
+// same bits: with r the float32 result and E a bound on |r - X| (X the float64
+// value), rounding to nearest is monotone, so RN(r - E) == RN(r + E) implies
+// RN(X) == RN(r).  Elements that fail the test (a bf16 rounding boundary
+// within E, about one in a thousand) are evaluated in float64.  Queries are
+// never stored and use the float32 rotation directly.
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "kvc_internal.h"
 
 namespace kvc {
 
+// r = a * b1 - c * d1 (sub) or a * b1 + c * d1 in float32 with one fused
+// multiply-add; the bound below covers the float32 rounding of cos/sin, of
+// the product c * d1 and of the fused operation with a factor of 4 to spare
+// (each is at most 2^-24 relative to the terms' magnitudes).
+// The rare exact evaluation, kept out of line so that the common path carries no
+// (predicated) float64 instructions.
+__device__ __noinline__ __nv_bfloat16 rope_bf16_fallback(float xf, float yf, const double2* table, int64_t ti,
+                                                         bool second) {
+    double2 cs = make_double2(1.0, 0.0);
+    if (table) cs = table[ti];
+    double xr, yr;
+    rope_pair_f64((double)xf, (double)yf, cs.x, cs.y, xr, yr);
+    return f64_to_bf16_rn(second ? yr : xr);
+}
+
+__device__ __forceinline__ __nv_bfloat16 rope_bf16_exact(float xf, float yf, float cf, float sf,
+                                                        const double2* table, int pos, int pairs, int j,
+                                                        bool second) {
+    const float t2 = second ? xf * sf : yf * sf;
+    const float t1a = second ? yf : xf;
+    const float r = second ? fmaf(t1a, cf, t2) : fmaf(t1a, cf, -t2);
+    const float bound = 0x1p-20f * (fabsf(t1a * cf) + fabsf(t2) + fabsf(r)) + 0x1p-140f;
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r - bound);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(r + bound);
+    if (__builtin_expect(__bfloat16_as_ushort(lo) == __bfloat16_as_ushort(hi), 1)) return lo;
+    return rope_bf16_fallback(xf, yf, table, (int64_t)pos * pairs + j, second);
+}
+
 template <typename T, int P>
 struct alignas((2 * P * sizeof(T)) >= 16 ? 16 : (2 * P * sizeof(T))) Pack { T v[2 * P]; };
 
-template <typename T, typename QO, int P>
-__global__ void __launch_bounds__(256) rope_append_kernel(AppendLaunch a) {
+constexpr int kRows = 4;   // rows of one (head, chunk) handled by a thread: 4 loads in flight
+
+template <typename T, typename QO, int P, bool FAST>
+__device__ __forceinline__ void rope_one(const AppendLaunch& a, int kind, int b, int h, int i, int slot, int pos,
+                                         int c, const Pack<T, P>& in) {
     using S = Storage<T>;
     const int pairs_per_row = a.d / 2;
-    const int chunks = pairs_per_row / P;
+    if (kind == 2) {
+        T* dst = (T*)a.V + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+        *reinterpret_cast<Pack<T, P>*>(dst) = in;
+        return;
+    }
+    const int64_t t0 = (int64_t)pos * pairs_per_row + P * c;
+    if constexpr (FAST) {
+        // bf16 storage: float32 rotation, bit-exact key rounding (see above)
+        Pack<T, P> ok;
+        Pack<QO, P> oq;
+        if (!a.rope) {          // no rotation: keys are copied, queries converted
+            ok = in;
+#pragma unroll
+            for (int e = 0; e < 2 * P; ++e) oq.v[e] = (QO)S::to_f32(in.v[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < P; ++e) {
+                const float2 cs = a.rope_f[t0 + e];
+                const float xf = S::to_f32(in.v[2 * e]);
+                const float yf = S::to_f32(in.v[2 * e + 1]);
+                if (kind == 1) {
+                    ok.v[2 * e] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, pairs_per_row, P * c + e, false);
+                    ok.v[2 * e + 1] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, pairs_per_row, P * c + e, true);
+                } else {
+                    oq.v[2 * e] = (QO)fmaf(xf, cs.x, -(yf * cs.y));
+                    oq.v[2 * e + 1] = (QO)fmaf(yf, cs.x, xf * cs.y);
+                }
+            }
+        }
+        if (kind == 1) {
+            T* dst = (T*)a.K + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+            *reinterpret_cast<Pack<T, P>*>(dst) = ok;
+            if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
+        } else {
+            QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
+            *reinterpret_cast<Pack<QO, P>*>(dst) = oq;
+        }
+        return;
+    }
+    double xr[2 * P];
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+        const double x = S::to_f64(in.v[2 * e]);
+        const double y = S::to_f64(in.v[2 * e + 1]);
+        if (a.rope) {
+            const double2 cs = a.rope[t0 + e];
+            rope_pair_f64(x, y, cs.x, cs.y, xr[2 * e], xr[2 * e + 1]);
+        } else {
+            xr[2 * e] = x;
+            xr[2 * e + 1] = y;
+        }
+    }
+    if (kind == 1) {
+        Pack<T, P> o;
+#pragma unroll
+        for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<T>(xr[e]);
+        T* dst = (T*)a.K + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+        *reinterpret_cast<Pack<T, P>*>(dst) = o;
+        if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
+    } else {
+        Pack<QO, P> o;
+#pragma unroll
+        for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<QO>(xr[e]);
+        QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
+        *reinterpret_cast<Pack<QO, P>*>(dst) = o;
+    }
+}
+
+template <typename T, typename QO, int P, bool FAST>
+__global__ void __launch_bounds__(256) rope_append_kernel(AppendLaunch a) {
+    const int chunks = a.d / 2 / P;
     const int heads_all = a.Hq + 2 * a.Hkv;
-    const int64_t total = (int64_t)a.B * heads_all * a.S * chunks;
+    const int groups = (a.S + kRows - 1) / kRows;
+    const int64_t total = (int64_t)a.B * heads_all * groups * chunks;
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
+        // consecutive threads: the chunks of one row, then row groups of the same head
+        // (contiguous in memory), then heads, then sequences
         const int c = (int)(u % chunks);
         int64_t r = u / chunks;
-        const int i = (int)(r % a.S);
-        r /= a.S;
+        const int ig = (int)(r % groups);
+        r /= groups;
         const int hh = (int)(r % heads_all);
         const int b = (int)(r / heads_all);
         const int rows = a.seqlen ? a.seqlen[b] : a.S;
-        if (i >= rows) continue;
-        const int slot = a.slot0[b] + i;
-        const int pos = a.pos0[b] + i;
-        if (slot < 0 || slot >= a.C || pos < 0 || (a.rope && pos >= a.max_positions)) {
-            atomicOr(a.err, (uint32_t)DEV_ERR_SLOT);
-            continue;
-        }
+        const int i0 = ig * kRows;
+        if (i0 >= rows) continue;
         int kind, h;   // 0 = query, 1 = key, 2 = value
         if (hh < a.Hq) { kind = 0; h = hh; }
         else if (hh < a.Hq + a.Hkv) { kind = 1; h = hh - a.Hq; }
         else { kind = 2; h = hh - a.Hq - a.Hkv; }
         const int H = kind == 0 ? a.Hq : a.Hkv;
         const T* src = (const T*)(kind == 0 ? a.q : kind == 1 ? a.k : a.v) +
-                       (((int64_t)b * H + h) * a.S + i) * a.d + 2 * P * c;
-        Pack<T, P> in = *reinterpret_cast<const Pack<T, P>*>(src);
-        if (kind == 2) {
-            T* dst = (T*)a.V + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
-            *reinterpret_cast<Pack<T, P>*>(dst) = in;
-            continue;
-        }
-        double xr[2 * P];
+                       (((int64_t)b * H + h) * a.S + i0) * a.d + 2 * P * c;
+        const int n = min(kRows, rows - i0);
+        Pack<T, P> in[kRows];
 #pragma unroll
-        for (int e = 0; e < P; ++e) {
-            const double x = S::to_f64(in.v[2 * e]);
-            const double y = S::to_f64(in.v[2 * e + 1]);
-            if (a.rope) {
-                const double2 cs = a.rope[(int64_t)pos * pairs_per_row + P * c + e];
-                rope_pair_f64(x, y, cs.x, cs.y, xr[2 * e], xr[2 * e + 1]);
-            } else {
-                xr[2 * e] = x;
-                xr[2 * e + 1] = y;
+        for (int rr = 0; rr < kRows; ++rr)
+            if (rr < n) in[rr] = *reinterpret_cast<const Pack<T, P>*>(src + (int64_t)rr * a.d);
+        const int slot0 = a.slot0[b] + i0;
+        const int pos0 = a.pos0[b] + i0;
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+            if (rr >= n) break;
+            const int slot = slot0 + rr, pos = pos0 + rr;
+            if (slot < 0 || slot >= a.C || pos < 0 || (a.rope && pos >= a.max_positions)) {
+                atomicOr(a.err, (uint32_t)DEV_ERR_SLOT);
+                continue;
             }
-        }
-        if (kind == 1) {
-            Pack<T, P> o;
-#pragma unroll
-            for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<T>(xr[e]);
-            T* dst = (T*)a.K + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
-            *reinterpret_cast<Pack<T, P>*>(dst) = o;
-            if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
-        } else {
-            Pack<QO, P> o;
-#pragma unroll
-            for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<QO>(xr[e]);
-            QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
-            *reinterpret_cast<Pack<QO, P>*>(dst) = o;
+            rope_one<T, QO, P, FAST>(a, kind, b, h, i0 + rr, slot, pos, c, in[rr]);
         }
     }
 }
@@ -94,7 +186,7 @@ static cudaError_t launch_typed(const AppendLaunch& a, cudaStream_t s) {
     int P = 1;
     if (P_max >= 4 && pairs % 4 == 0) P = 4;
     else if (P_max >= 2 && pairs % 2 == 0) P = 2;
-    const int64_t total = (int64_t)a.B * (a.Hq + 2 * a.Hkv) * a.S * (pairs / P);
+    const int64_t total = (int64_t)a.B * (a.Hq + 2 * a.Hkv) * ((a.S + kRows - 1) / kRows) * (pairs / P);
     if (total == 0) return cudaSuccess;
     int sms = 152;
     int dev;
@@ -102,10 +194,11 @@ static cudaError_t launch_typed(const AppendLaunch& a, cudaStream_t s) {
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)sms * 16;
     if (blocks > cap) blocks = cap;
+    constexpr bool FAST = std::is_same<T, __nv_bfloat16>::value;
     switch (P) {
-        case 4: rope_append_kernel<T, QO, 4><<<(unsigned)blocks, 256, 0, s>>>(a); break;
-        case 2: rope_append_kernel<T, QO, 2><<<(unsigned)blocks, 256, 0, s>>>(a); break;
-        default: rope_append_kernel<T, QO, 1><<<(unsigned)blocks, 256, 0, s>>>(a); break;
+        case 4: rope_append_kernel<T, QO, 4, FAST><<<(unsigned)blocks, 256, 0, s>>>(a); break;
+        case 2: rope_append_kernel<T, QO, 2, FAST><<<(unsigned)blocks, 256, 0, s>>>(a); break;
+        default: rope_append_kernel<T, QO, 1, FAST><<<(unsigned)blocks, 256, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }

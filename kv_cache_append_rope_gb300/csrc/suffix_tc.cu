@@ -9,24 +9,33 @@
 // max-subtracted softmax.  A long suffix is a dense Q K^T / P V contraction,
 // which is why this kernel uses tcgen05 tiles.
 //
-// One CTA per work item (sequence b, query head h, 128-row query tile qt),
-// items ordered longest first.  Query row i (slot cut + i) attends key slots
+// One CTA per work item (sequence b, query head h, 128-row query tile qt).
+// Items are grouped by (b, h) -- the query tiles of one head launch together
+// and walk its K/V tiles in step, so each tile comes from DRAM once and from
+// L2 for the rest -- and the groups are ordered by total work, longest first.  Query row i (slot cut + i) attends key slots
 // 0 .. cut + i; key tiles are 128 slots, the last ones masked element-wise.
 //
-// Warp roles (192 threads):
-//   warp 0    TMA producer: the rotated Q tile once, then K and V tiles into a
-//             two-stage ring (128-byte swizzle, no multicast).
+// Warp roles (320 threads):
+//   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 the
+//             rotated Q tile once and K tiles into a 3-stage ring, lane 1 V
+//             tiles into a 2-stage ring.
 //   warp 1    TMEM allocator (512 columns) and, on one elected thread, the MMA
 //             issuer: S = Q K^T into one of two TMEM S buffers (so the next
 //             tile's QK^T overlaps the current softmax), then O += P V into
-//             the TMEM O accumulator, each completion signalled with
-//             tcgen05.commit on an mbarrier.
-//   warps 2-5 softmax (thread = query row = TMEM lane): tcgen05.ld of the S
-//             row, causal mask, running max in log2 units, O rescaled through
+//             the TMEM O accumulator with P read from tensor memory, each
+//             completion signalled with tcgen05.commit on an mbarrier.
+// Tensor memory: S0, S1, O (128 columns each), P0, P1 (64 columns each).
+//   warps 2-9 softmax, two warps per TMEM sub-partition, each thread one
+//             query row (= TMEM lane) and one half of its 128 columns, the
+//             pair exchanging row maxima through shared memory (an mbarrier
+//             of 64 arrivals): tcgen05.ld of the S half-row, causal mask,
+//             running max in log2 units, O rescaled through
 //             TMEM only when the max grows by more than 2^8 (the final
 //             division by the running sum makes the stale max exact), P
-//             written as bf16 into a swizzled shared-memory tile for the PV
-//             MMA, and the normalised O row written to global memory.
+//             computed in registers while the previous tile's PV runs, then
+//             written as packed bf16 into one of two 64-column tensor-memory
+//             P buffers (tcgen05.st), from which the PV MMA reads its A
+//             operand, and the normalised O row written to global memory.
 // Every mbarrier wait is bounded (DEV_ERR_WAIT_TIMEOUT), the MMA thread waits
 // for its own last commit and the TMA thread for its own copies before the
 // allocator warp frees the tensor memory.
@@ -42,22 +51,27 @@ namespace {
 constexpr int BM = 128, BN = 128, D = 128;
 constexpr int HALF = BM * 128;             // 128 rows x 64 bf16 (one TMA box)
 constexpr int TILE = 2 * HALF;             // 128 rows x 128 bf16
+constexpr int KST = 3, VST = 2;            // K and V ring stages (K is needed first)
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;        // two stages
-constexpr int OFF_V = OFF_K + 2 * TILE;    // two stages
-constexpr int OFF_P = OFF_V + 2 * TILE;
-constexpr int OFF_BAR = OFF_P + TILE;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-constexpr int THREADS = 192;
+constexpr int OFF_K = OFF_Q + TILE;
+constexpr int OFF_V = OFF_K + KST * TILE;
+constexpr int OFF_BAR = OFF_V + VST * TILE;
+constexpr int SMEM_BYTES = OFF_BAR + 4096 + 1024;
+constexpr int NSW = 8;                     // softmax warps: two per TMEM sub-partition
+constexpr int THREADS = (2 + NSW) * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_P0 = 384, COL_P1 = 448;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct Bars {
+    float red_max[2][2][BM];   // [tile parity][column half][row]: partial row maxima
+    float red_sum[2][BM];      // [column half][row]: partial row sums
     uint64_t q_full;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
     uint64_t s_full[2], s_free[2];
-    uint64_t p_full, o_ready, mma_done;
+    uint64_t p_full[2], pv_done[2], mma_done;
+    uint64_t xchg[4][2];       // [sub-partition][tile parity]: the two softmax warps of a row block
+    uint64_t fin[4];           // [sub-partition]: final partial sums
     uint32_t tmem_base;
     int err;
 };
@@ -87,17 +101,26 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
             mbar_init(smem_u32(&bars->k_empty[s]), 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
             mbar_init(smem_u32(&bars->v_empty[s]), 1);
-            mbar_init(smem_u32(&bars->s_full[s]), 1);
-            mbar_init(smem_u32(&bars->s_free[s]), 4);
         }
-        mbar_init(smem_u32(&bars->p_full), 4);
-        mbar_init(smem_u32(&bars->o_ready), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars->s_full[s]), 1);
+            mbar_init(smem_u32(&bars->s_free[s]), NSW);
+            mbar_init(smem_u32(&bars->p_full[s]), NSW);
+            mbar_init(smem_u32(&bars->pv_done[s]), 1);
+        }
         mbar_init(smem_u32(&bars->mma_done), 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(smem_u32(&bars->xchg[q][0]), 64);
+            mbar_init(smem_u32(&bars->xchg[q][1]), 64);
+            mbar_init(smem_u32(&bars->fin[q]), 64);
+        }
         bars->err = 0;
         fence_mbar_init();
     }
@@ -112,44 +135,43 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            prefetch_tmap(&a.tmQ);
-            prefetch_tmap(&a.tmK);
-            prefetch_tmap(&a.tmV);
-            const int qrow = (b * a.Hq + h) * a.S + qt * BM;
+        // lane 0 streams Q and the K ring, lane 1 the V ring, so that the K
+        // look-ahead never waits behind a V stage that is still being read.
+        if (lane < 2) {
             const int kvrow = (b * a.Hkv + g) * a.C;
-            const uint32_t qb = smem_u32(&bars->q_full);
-            mbar_arrive_expect_tx(qb, TILE);
-            tma_load_2d(smem_u32(smem + OFF_Q), &a.tmQ, 0, qrow, qb);
-            tma_load_2d(smem_u32(smem + OFF_Q + HALF), &a.tmQ, 64, qrow, qb);
-            int issued_k = 0, issued_v = 0;
+            const bool is_k = lane == 0;
+            const int NS = is_k ? KST : VST;
+            uint64_t* full = is_k ? bars->k_full : bars->v_full;
+            uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+            const CUtensorMap* map = is_k ? &a.tmK : &a.tmV;
+            uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
+            prefetch_tmap(map);
+            uint32_t qb = 0;
+            if (is_k) {
+                prefetch_tmap(&a.tmQ);
+                const int qrow = (b * a.Hq + h) * a.S + qt * BM;
+                qb = smem_u32(&bars->q_full);
+                mbar_arrive_expect_tx(qb, TILE);
+                tma_load_2d(smem_u32(smem + OFF_Q), &a.tmQ, 0, qrow, qb);
+                tma_load_2d(smem_u32(smem + OFF_Q + HALF), &a.tmQ, 64, qrow, qb);
+            }
+            int issued = 0;
             for (int j = 0; j < n && !*(volatile int*)&bars->err; ++j) {
-                const int s = j & 1, use = j >> 1;
-                if (j >= 2 && !mbar_wait_bounded(smem_u32(&bars->k_empty[s]), (use - 1) & 1, a.err)) {
+                const int s = j % NS, use = j / NS;
+                if (j >= NS && !mbar_wait_bounded(smem_u32(&empty[s]), (use - 1) & 1, a.err)) {
                     fail_wait(bars, a.err);
                     break;
                 }
-                const uint32_t kb = smem_u32(&bars->k_full[s]);
-                mbar_arrive_expect_tx(kb, TILE);
-                tma_load_2d(smem_u32(smem + OFF_K + s * TILE), &a.tmK, 0, kvrow + j * BN, kb);
-                tma_load_2d(smem_u32(smem + OFF_K + s * TILE + HALF), &a.tmK, 64, kvrow + j * BN, kb);
-                issued_k = j + 1;
-                if (j >= 2 && !mbar_wait_bounded(smem_u32(&bars->v_empty[s]), (use - 1) & 1, a.err)) {
-                    fail_wait(bars, a.err);
-                    break;
-                }
-                const uint32_t vb = smem_u32(&bars->v_full[s]);
-                mbar_arrive_expect_tx(vb, TILE);
-                tma_load_2d(smem_u32(smem + OFF_V + s * TILE), &a.tmV, 0, kvrow + j * BN, vb);
-                tma_load_2d(smem_u32(smem + OFF_V + s * TILE + HALF), &a.tmV, 64, kvrow + j * BN, vb);
-                issued_v = j + 1;
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, TILE);
+                tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + j * BN, fb);
+                tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + j * BN, fb);
+                issued = j + 1;
             }
             // Our own copies must have landed before the CTA's shared memory is released.
-            mbar_wait_bounded(qb, 0, a.err);
-            for (int t = issued_k - 2 < 0 ? 0 : issued_k - 2; t < issued_k; ++t)
-                mbar_wait_bounded(smem_u32(&bars->k_full[t & 1]), (t >> 1) & 1, a.err);
-            for (int t = issued_v - 2 < 0 ? 0 : issued_v - 2; t < issued_v; ++t)
-                mbar_wait_bounded(smem_u32(&bars->v_full[t & 1]), (t >> 1) & 1, a.err);
+            if (is_k) mbar_wait_bounded(qb, 0, a.err);
+            for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
+                mbar_wait_bounded(smem_u32(&full[t % NS]), (t / NS) & 1, a.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -157,16 +179,15 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
             const uint32_t q_s = smem_u32(smem + OFF_Q);
-            const uint32_t p_s = smem_u32(smem + OFF_P);
             bool ok = mbar_wait_bounded(smem_u32(&bars->q_full), 0, a.err);
             if (!ok) fail_wait(bars, a.err);
             tc_fence_after();
             auto issue_qk = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait_bounded(smem_u32(&bars->k_full[s]), (j >> 1) & 1, a.err)) return false;
+                const int s = j & 1, ks = j % KST;
+                if (!mbar_wait_bounded(smem_u32(&bars->k_full[ks]), (j / KST) & 1, a.err)) return false;
                 if (j >= 2 && !mbar_wait_bounded(smem_u32(&bars->s_free[s]), ((j >> 1) - 1) & 1, a.err)) return false;
                 tc_fence_after();
-                const uint32_t k_s = smem_u32(smem + OFF_K + s * TILE);
+                const uint32_t k_s = smem_u32(smem + OFF_K + ks * TILE);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
@@ -174,29 +195,30 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                               smem_desc_sw128(k_s + off, 16, 1024), idesc_qk, kk > 0);
                 }
                 tc_commit(smem_u32(&bars->s_full[s]));
-                tc_commit(smem_u32(&bars->k_empty[s]));
+                tc_commit(smem_u32(&bars->k_empty[ks]));
                 return true;
             };
             if (ok) ok = issue_qk(0);
             for (int j = 0; ok && j < n; ++j) {
                 if (j + 1 < n && !(ok = issue_qk(j + 1))) break;
-                const int s = j & 1;
-                if (!mbar_wait_bounded(smem_u32(&bars->p_full), j & 1, a.err) ||
-                    !mbar_wait_bounded(smem_u32(&bars->v_full[s]), (j >> 1) & 1, a.err)) {
+                const int s = j & 1, vs = j % VST;
+                if (!mbar_wait_bounded(smem_u32(&bars->p_full[s]), (j >> 1) & 1, a.err) ||
+                    !mbar_wait_bounded(smem_u32(&bars->v_full[vs]), (j / VST) & 1, a.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t v_s = smem_u32(smem + OFF_V + s * TILE);
+                const uint32_t v_s = smem_u32(smem + OFF_V + vs * TILE);
+                const uint32_t p_t = tmem + (s ? COL_P1 : COL_P0);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    // A = P (K-major over keys), B = V (rows = keys, contiguous head dims: MN-major)
-                    const uint32_t poff = (kk >> 2) * HALF + (kk & 3) * 32;
-                    tc_mma_ss(tmem + COL_O, smem_desc_sw128(p_s + poff, 16, 1024),
-                              smem_desc_sw128(v_s + kk * 16 * 128, HALF, 1024), idesc_pv, (j > 0 || kk > 0));
+                    // A = P from tensor memory (16 keys = 8 columns per step),
+                    // B = V (rows = keys, contiguous head dims: MN-major)
+                    tc_mma_ts(tmem + COL_O, p_t + kk * 8, smem_desc_sw128(v_s + kk * 16 * 128, HALF, 1024),
+                              idesc_pv, (j > 0 || kk > 0));
                 }
-                tc_commit(smem_u32(&bars->o_ready));
-                tc_commit(smem_u32(&bars->v_empty[s]));
+                tc_commit(smem_u32(&bars->pv_done[s]));
+                tc_commit(smem_u32(&bars->v_empty[vs]));
             }
             if (!ok) fail_wait(bars, a.err);
             // every MMA issued by this thread completes before the tensor memory is freed
@@ -204,13 +226,16 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             mbar_wait_bounded(smem_u32(&bars->mma_done), 0);  // no abort: the MMAs always finish
         }
     } else {
-        // ------------------------------------------------------------ softmax warpgroup
-        const int sub = warp & 3;                    // TMEM sub-partition of this warp
+        // ------------------------------------------------------------ softmax warps
+        // Warp w (2..9) reads TMEM lanes 32 * (w % 4) .. + 31 (its sub-partition);
+        // warps 2-5 take columns 0-63 of those rows, warps 6-9 columns 64-127.
+        constexpr int HC = BN / 2;                   // columns per warp
+        const int sub = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = sub * 32 + lane;             // query row inside the tile = TMEM lane
         const int i = qt * BM + row;
         const int qslot = cut + i;
         const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-        uint8_t* prow = smem + OFF_P + row * 128;
         const float sl2 = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -221,81 +246,105 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            float x[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + (s ? COL_S1 : COL_S0) + c * 32, x + c * 32);
+            float x[HC];
+            const uint32_t s_col = (s ? COL_S1 : COL_S0) + half * HC;
+            tmem_ld32(lane_addr + s_col, x);
+            tmem_ld32(lane_addr + s_col + 32, x + 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[s]));
 
-            const int kbase = j * BN;
-            if (kbase + BN - 1 > cut + qt * BM) {
+            const int kbase = j * BN + half * HC;
+            if (kbase + HC - 1 > cut + qt * BM) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (kbase + c > qslot) x[c] = -INFINITY;
+                for (int c = 0; c < HC; ++c) x[c] = (kbase + c > qslot) ? -INFINITY : x[c];
             }
-            float mx = -INFINITY;
+            // row maximum: 8 independent chains here, then the partner warp's half
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, x[c]);
+            for (int q = 0; q < 8; ++q) m8[q] = x[q];
+#pragma unroll
+            for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+#pragma unroll
+            for (int w8 = 4; w8 > 0; w8 >>= 1)
+#pragma unroll
+                for (int q = 0; q < w8; ++q) m8[q] = fmaxf(m8[q], m8[q + w8]);
+            bars->red_max[s][half][row] = m8[0];
+            mbar_arrive(smem_u32(&bars->xchg[sub][s]));
+            if (!warp_wait(smem_u32(&bars->xchg[sub][s]), (j >> 1) & 1, a.err)) {
+                ok = false;
+                break;
+            }
+            const float mx = fmaxf(m8[0], bars->red_max[s][half ^ 1][row]);
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + RESCALE_LOG2 || (j == 0);
             const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
-            if (j > 0) {
-                // PV of the previous tile must be done: O is rescaled below and P is rewritten.
-                if (!warp_wait(smem_u32(&bars->o_ready), (j - 1) & 1, a.err)) {
+            if (grow && j > 0 && m_run > -INFINITY) {
+                // O holds the sum over earlier tiles: wait for PV of tile j-1, then rescale this half.
+                if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, a.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (grow && m_run > -INFINITY) {
-                    const float corr = fast_exp2(m_run - m_new);
-                    l_run *= corr;
+                const float corr = fast_exp2(m_run - m_new);
+                l_run *= corr;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(lane_addr + COL_O + c * 32, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < HC / 32; ++c) {
+                    float o[32];
+                    const uint32_t oa = lane_addr + COL_O + half * HC + c * 32;
+                    tmem_ld32(oa, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= corr;
-                        tmem_st32(lane_addr + COL_O + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] *= corr;
+                    tmem_st32(oa, o);
                 }
+                tmem_wait_st();
             }
             m_run = m_new;
             const float mu = m_run == -INFINITY ? 0.f : m_run;
+            // P in registers first: the exponentials overlap the previous tile's PV.
+            uint32_t pk[HC / 2];
+            float l8[8];
 #pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                uint32_t pk[4];
+            for (int q = 0; q < 8; ++q) l8[q] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(fmaf(x[ch * 8 + 2 * e], sl2, -mu));
-                    const float p1 = fast_exp2(fmaf(x[ch * 8 + 2 * e + 1], sl2, -mu));
-                    l_run += p0 + p1;
-                    pk[e] = pack_bf16(p0, p1);
-                }
-                const uint32_t addr = smem_u32(prow + (ch >> 3) * HALF + ((((ch & 7) ^ (row & 7))) << 4));
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[0]), "r"(pk[1]),
-                             "r"(pk[2]), "r"(pk[3])
-                             : "memory");
+            for (int e = 0; e < HC / 2; ++e) {
+                const float p0 = fast_exp2(fmaf(x[2 * e], sl2, -mu));
+                const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl2, -mu));
+                l8[e & 7] += p0 + p1;
+                pk[e] = pack_bf16(p0, p1);
             }
-            fence_proxy_async_smem();
+#pragma unroll
+            for (int w8 = 4; w8 > 0; w8 >>= 1)
+#pragma unroll
+                for (int q = 0; q < w8; ++q) l8[q] += l8[q + w8];
+            l_run += l8[0];
+            // P buffer s was last read by the PV of tile j-2.
+            if (j >= 2 && !warp_wait(smem_u32(&bars->pv_done[s]), ((j >> 1) - 1) & 1, a.err)) {
+                ok = false;
+                break;
+            }
+            tmem_st32u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[s]));
         }
+        bars->red_sum[half][row] = l_run;
+        mbar_arrive(smem_u32(&bars->fin[sub]));
+        if (!warp_wait(smem_u32(&bars->fin[sub]), 0, a.err)) ok = false;
         if (ok && n > 0) {
-            if (!warp_wait(smem_u32(&bars->o_ready), (n - 1) & 1, a.err)) {
+            if (!warp_wait(smem_u32(&bars->pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, a.err)) {
                 ok = false;
             } else {
                 tc_fence_after();
-                const float inv = 1.0f / l_run;
-                float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D;
+                const float inv = 1.0f / (bars->red_sum[0][row] + bars->red_sum[1][row]);
+                float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D + half * HC;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < HC / 32; ++c) {
                     float o[32];
-                    tmem_ld32(lane_addr + COL_O + c * 32, o);
+                    tmem_ld32(lane_addr + COL_O + half * HC + c * 32, o);
                     tmem_wait_ld();
                     if (i < rows_b) {
 #pragma unroll

@@ -112,3 +112,50 @@ def test_first_step_returns_the_value():
     """t = 1: the single weight is 1 and the output is the (rounded) new value row."""
     cache, outs, (q, k, v) = run_decode("bf16", 128, 4, 4, [0], 1, C=8)
     np.testing.assert_allclose(outs[0][0, :, 0], v[0, :, 0], atol=1e-6)
+
+
+def test_appended_keys_bit_exact_at_volume():
+    """Millions of appended bf16 key elements, at small and large positions, equal the
+    oracle's float64 rotation rounded to bf16 bit for bit (this exercises the rare
+    elements whose float32 rotation lands next to a bf16 rounding boundary)."""
+    need_gpu()
+    B, H, T, D = 2, 8, 4096, 128
+    start = [0, 28000]
+    kd = device_tensor(W.normal_np((B, H, T, D), 81), "bf16")
+    vd = device_tensor(W.normal_np((B, H, T, D), 82), "bf16")
+    cache = KVCache(B, H, T, D, dtype="bf16", rope_base=BASE, rope_max_positions=32768)
+    cache.prefill_suffix(0, None, kd, vd, start_pos=start, out=False)
+    Ks, Vs, Ps = storage_np(cache)
+    k, v = to_np(kd), to_np(vd)
+    for b in range(B):
+        pos = start[b] + np.arange(T)
+        K, V = A.stored_rows(k[b], v[b], pos[None, :], BASE, "bf16")
+        np.testing.assert_array_equal(Ks[b], K)
+        np.testing.assert_array_equal(Vs[b], V)
+        assert Ps[b].tolist() == pos.tolist()
+    cache.check()
+
+
+def test_bf16_without_rope_stores_inputs_unchanged():
+    """rope_base = 0 switches the rotation off: stored keys are the input keys, bit for bit
+    (signed zeros included), and the decode output matches the oracle."""
+    need_gpu()
+    B, H, D, L0 = 2, 4, 128, [3, 70]
+    k = W.normal_np((B, H, max(L0) + 1, D), 83)
+    k[0, 0, 0, :8] = [0.0, -0.0, 0.0, -0.0, -0.0, 0.0, 1.0, -1.0]
+    kd = device_tensor(k, "bf16")
+    vd = device_tensor(W.normal_np((B, H, max(L0) + 1, D), 84), "bf16")
+    qd = device_tensor(W.normal_np((B, H, max(L0) + 1, D), 85), "bf16")
+    cache = KVCache(B, H, 128, D, dtype="bf16", rope_base=0.0)
+    cache.prefill_suffix(0, None, kd[:, :, :max(L0)].contiguous(), vd[:, :, :max(L0)].contiguous(), seqlen=L0,
+                         out=False)
+    idx = torch.tensor(L0, device="cuda")
+    sel = lambda x: x[torch.arange(B, device="cuda"), :, idx][:, :, None, :].contiguous()
+    out = to_np(cache.append_attend(0, sel(qd), sel(kd), sel(vd)))
+    Ks, _, _ = cache.storage(0)
+    kn, vn, qn = to_np(kd), to_np(vd), to_np(qd)
+    for b in range(B):
+        n = L0[b] + 1
+        assert torch.equal(Ks[b, :, :n].view(torch.int16).cpu(), kd[b, :, :n].view(torch.int16).cpu())
+        ref = A.decode_steps_reference(qn[b, :, L0[b]][None], kn[b, :, :n], vn[b, :, :n], L0[b], 0, "bf16")
+        assert np.abs(out[b, :, 0] - ref[0]).max() <= TOL["bf16"]
