@@ -216,6 +216,7 @@ void free_all(kvc_handle* h) {
     cudaFree(h->part_ml);
     cudaFree(h->qrot_chunk);
     cudaFree(h->work_counter);
+    cudaFree(h->lane_ticket);
     h->ring.destroy();
     for (auto& t : h->timers) {
         for (auto e : t.start) cudaEventDestroy(e);
@@ -401,7 +402,8 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
               alloc((void**)&h->err_d, sizeof(uint32_t)) &&
               alloc((void**)&h->nonfinite_d, 2 * sizeof(unsigned long long)) &&
               alloc(&h->qrot, (size_t)c.batch * c.heads_q * c.head_dim * acc) &&
-              alloc((void**)&h->work_counter, 64);
+              alloc((void**)&h->work_counter, 64) &&
+              alloc((void**)&h->lane_ticket, (size_t)c.batch * c.heads_kv * sizeof(unsigned));
     if (ok && c.rope_base > 0.0)
         ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2)) &&
              alloc((void**)&h->rope_f, (size_t)maxpos * (c.head_dim / 2) * sizeof(float2));
@@ -422,6 +424,8 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
     if ((e = cudaMemset(h->len_d, 0, LB * sizeof(int32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
     if ((e = cudaMemset(h->next_d, 0, LB * sizeof(int32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
     if ((e = cudaMemset(h->err_d, 0, sizeof(uint32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->lane_ticket, 0, (size_t)c.batch * c.heads_kv * sizeof(unsigned))) != cudaSuccess)
+        return abort_cuda(e, "cudaMemset");
     if ((e = cudaHostAlloc((void**)&h->nonfinite_h, 2 * sizeof(unsigned long long), cudaHostAllocDefault)) !=
         cudaSuccess)
         return abort_cuda(e, "cudaHostAlloc");
@@ -587,6 +591,32 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         if (max_splits > 1 && (st = ensure_partials(h, max_splits)) != KVC_OK) return st;
     }
 
+    // One launch per step (append, attend, merge splits, commit lengths) up to 16
+    // query heads per key/value head; beyond that the merge done by one CTA per
+    // lane costs more than a separate merge kernel spread over every query head.
+    if (fast && h->opt_decode_fused && B <= kFusedMaxB && Hq / Hkv <= 16) {
+        DecodeLaunch dl{};
+        dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
+        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
+        dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
+        dl.fused = 1;
+        dl.q_in = (const __nv_bfloat16*)q->data; dl.k_in = (const __nv_bfloat16*)k->data;
+        dl.v_in = (const __nv_bfloat16*)v->data;
+        dl.K = (__nv_bfloat16*)h->K_layer(layer); dl.V = (__nv_bfloat16*)h->V_layer(layer);
+        dl.positions = h->pos_layer(layer);
+        dl.len_out = h->len_layer(layer); dl.next_out = h->next_layer(layer);
+        dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
+        for (int b = 0; b < B; ++b) {
+            dl.old_len[b] = lenh[b];
+            dl.pos[b] = nexth[b];
+        }
+        KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
+        for (int b = 0; b < B; ++b) {
+            lenh[b] += 1;
+            nexth[b] += 1;
+        }
+        return KVC_OK;
+    }
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
     if (fast) {
         DecodeLaunch dl{};
@@ -756,6 +786,7 @@ kvc_status kvc_reset(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaSetDevice(h->cfg.device));
     KVC_CUDA(h, cudaMemsetAsync(h->len_d, 0, n * sizeof(int32_t), s));
     KVC_CUDA(h, cudaMemsetAsync(h->next_d, 0, n * sizeof(int32_t), s));
+    KVC_CUDA(h, cudaMemsetAsync(h->lane_ticket, 0, (size_t)h->B() * h->Hkv() * sizeof(unsigned), s));
     std::fill(h->len_h.begin(), h->len_h.end(), 0);
     std::fill(h->next_h.begin(), h->next_h.end(), 0);
     return KVC_OK;
@@ -865,6 +896,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_TIMING:
             h->timing = value != 0;
+            return KVC_OK;
+        case KVC_OPT_DECODE_FUSED:
+            h->opt_decode_fused = value != 0;
             return KVC_OK;
     }
     return fail(h, KVC_ERR_CONFIG, "unknown option %d", option);

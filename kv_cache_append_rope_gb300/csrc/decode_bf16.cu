@@ -21,6 +21,13 @@
 // are merged through shared memory and the split's (O, max, sum) is written
 // to scratch, or the normalised output when the lane has a single split.  A
 // second kernel merges the splits of every query head by log-sum-exp.
+//
+// Fused step (one launch per decode step): the old lengths and RoPE positions
+// arrive as kernel parameters (host mirrors); the producer warp of each lane's
+// last split rotates and stores the new key row (bit-exact bf16 rounding) and
+// the value row before its TMA loads read them; the consumers rotate the new
+// queries in registers; the last CTA of a lane to finish (an atomic ticket, no
+// waiting) merges the splits; one CTA per sequence commits the new length.
 #include <cuda.h>
 
 #include "device_common.cuh"
@@ -46,16 +53,32 @@ template <int MT> struct Cfg;
 template <> struct Cfg<1> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
 template <> struct Cfg<2> { static constexpr int STAGES = 4; static constexpr int MINB = 1; };
 
-template <int MT>
+// Rotated query pair (c, c+1) of row `row` (< G) of this lane, as float32 (fused step).
+__device__ __forceinline__ float2 fused_q_pair(const DecodeLaunch& a, int b, int qh, int c, int pos) {
+    const __nv_bfloat162 v = *(const __nv_bfloat162*)(a.q_in + ((int64_t)b * a.Hq + qh) * D + c);
+    const float x = __low2float(v), y = __high2float(v);
+    if (!a.rope_f) return make_float2(x, y);
+    const float2 cs = a.rope_f[(int64_t)pos * (D / 2) + c / 2];
+    return make_float2(fmaf(x, cs.x, -(y * cs.y)), fmaf(y, cs.x, x * cs.y));
+}
+
+template <int MT, bool FUSED>
 __global__ void __launch_bounds__(THREADS, Cfg<MT>::MINB)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   DecodeLaunch a) {
+                   const __grid_constant__ DecodeLaunch a) {
     constexpr int STAGES = Cfg<MT>::STAGES;
     const int split = blockIdx.x;
     const int lane_kv = blockIdx.y;
     const int b = lane_kv / a.Hkv;
     const int hkv = lane_kv - b * a.Hkv;
-    const int t = a.len[b] + 1;
+    // Fused step: the old length and position come from the host mirrors, so no
+    // kernel of the step reads the length this kernel commits.
+    const int old_len = FUSED ? a.old_len[b] : a.len[b];
+    const int t = old_len + 1;
+    if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0) {
+        a.len_out[b] = old_len + 1;
+        a.next_out[b] = a.pos[b] + 1;
+    }
     const int r0 = split * a.split_rows;
     if (r0 >= t) return;
     const int r1 = min(t, r0 + a.split_rows);
@@ -67,7 +90,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
-    volatile int* s_err = (volatile int*)(empty + STAGES);
+    volatile int* s_err = (volatile int*)(empty + STAGES);   // s_err[1]: last-CTA flag
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -87,6 +110,36 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
     if (warp == NCW) {
         // ---------------- producer ----------------
+        if (FUSED && split == nsplit_lane - 1) {
+            // The new row (slot old_len) belongs to this split: rotate and store the
+            // key (bit-exact bf16 rounding), store the value and the position, then
+            // order these generic-proxy writes before this warp's TMA reads of them.
+            const int pos = a.pos[b];
+            const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
+            const int64_t dst = (((int64_t)b * a.Hkv + hkv) * a.C + old_len) * D + lane * 4;
+            const uint2 kraw = *(const uint2*)(a.k_in + src);
+            const uint2 vraw = *(const uint2*)(a.v_in + src);
+            const __nv_bfloat16* kin = (const __nv_bfloat16*)&kraw;
+            __nv_bfloat16 kout[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float xf = __bfloat162float(kin[2 * e]), yf = __bfloat162float(kin[2 * e + 1]);
+                if (a.rope_f) {
+                    const int j = lane * 2 + e;
+                    const float2 cs = a.rope_f[(int64_t)pos * (D / 2) + j];
+                    kout[2 * e] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, false);
+                    kout[2 * e + 1] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, true);
+                } else {
+                    kout[2 * e] = kin[2 * e];
+                    kout[2 * e + 1] = kin[2 * e + 1];
+                }
+            }
+            *(uint2*)(a.K + dst) = *(const uint2*)kout;
+            *(uint2*)(a.V + dst) = vraw;
+            if (hkv == 0 && lane == 0) a.positions[(int64_t)b * a.C + old_len] = pos;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncwarp();
+        }
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
@@ -120,13 +173,23 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const int ra = mt * 16 + qa, rb = ra + 8;
             const float* qra = a.qrot + ((int64_t)b * a.Hq + hkv * G + ra) * D;
             const float* qrb = a.qrot + ((int64_t)b * a.Hq + hkv * G + rb) * D;
+            const int qpos = FUSED ? a.pos[b] : 0;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int c = ks * 16 + qc;
-                float2 x0 = ra < G ? *(const float2*)(qra + c) : make_float2(0.f, 0.f);
-                float2 x1 = rb < G ? *(const float2*)(qrb + c) : make_float2(0.f, 0.f);
-                float2 x2 = ra < G ? *(const float2*)(qra + c + 8) : make_float2(0.f, 0.f);
-                float2 x3 = rb < G ? *(const float2*)(qrb + c + 8) : make_float2(0.f, 0.f);
+                float2 x0, x1, x2, x3;
+                if (FUSED) {
+                    const float2 z = make_float2(0.f, 0.f);
+                    x0 = ra < G ? fused_q_pair(a, b, hkv * G + ra, c, qpos) : z;
+                    x1 = rb < G ? fused_q_pair(a, b, hkv * G + rb, c, qpos) : z;
+                    x2 = ra < G ? fused_q_pair(a, b, hkv * G + ra, c + 8, qpos) : z;
+                    x3 = rb < G ? fused_q_pair(a, b, hkv * G + rb, c + 8, qpos) : z;
+                } else {
+                    x0 = ra < G ? *(const float2*)(qra + c) : make_float2(0.f, 0.f);
+                    x1 = rb < G ? *(const float2*)(qrb + c) : make_float2(0.f, 0.f);
+                    x2 = ra < G ? *(const float2*)(qra + c + 8) : make_float2(0.f, 0.f);
+                    x3 = rb < G ? *(const float2*)(qrb + c + 8) : make_float2(0.f, 0.f);
+                }
                 qf[mt][ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
                 qf[mt][ks][1] = pack_bf16(x1.x * qscale, x1.y * qscale);
                 qf[mt][ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
@@ -301,6 +364,37 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             if (dim == 0) a.part_ml[idx] = make_float2(M, L);
         }
     }
+    if (!FUSED || nsplit_lane == 1) return;
+
+    // Fused step: the last CTA of this lane to finish merges every split (a ticket,
+    // no waiting), then resets the ticket for the next step.
+    __threadfence();
+    __syncthreads();
+    volatile int* s_last = s_err + 1;
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(&a.lane_ticket[lane_kv], 1u);
+        *s_last = prev == (unsigned)(nsplit_lane - 1);
+    }
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    for (int u = threadIdx.x; u < G * D; u += THREADS) {
+        const int g = u / D, dim = u - g * D;
+        const int64_t qh = (int64_t)b * a.Hq + hkv * G + g;
+        const float2* ml = a.part_ml + qh * a.max_splits;
+        const float* po = a.part_o + qh * a.max_splits * D + dim;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit_lane; ++sp) M = fmaxf(M, __ldcg(&ml[sp].x));
+        float L = 0.f, O = 0.f;
+        for (int sp = 0; sp < nsplit_lane; ++sp) {
+            const float2 v = __ldcg(&ml[sp]);
+            const float f = fast_exp2(v.x - M);
+            L += v.y * f;
+            O += __ldcg(po + (int64_t)sp * D) * f;
+        }
+        a.out[qh * D + dim] = O / L;
+    }
+    if (threadIdx.x == 0) a.lane_ticket[lane_kv] = 0;
 }
 
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
@@ -322,17 +416,18 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     a.out[(int64_t)qh * D + threadIdx.x] = O / L;
 }
 
-template <int MT>
+template <int MT, bool FUSED>
 cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<Cfg<MT>::STAGES>();
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_bf16_kernel<MT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(a.max_splits, a.B * a.Hkv);
-    decode_bf16_kernel<MT><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
+    decode_bf16_kernel<MT, FUSED><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
     return cudaGetLastError();
 }
 
@@ -347,8 +442,9 @@ int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;
-    if (G <= 16) return launch_mt<1>(a, s);
-    if (G <= 32) return launch_mt<2>(a, s);
+    if (a.fused && a.B > kFusedMaxB) return cudaErrorInvalidValue;
+    if (G <= 16) return a.fused ? launch_mt<1, true>(a, s) : launch_mt<1, false>(a, s);
+    if (G <= 32) return a.fused ? launch_mt<2, true>(a, s) : launch_mt<2, false>(a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -58,6 +58,43 @@ __device__ __forceinline__ void rope_pair_f64(double x, double y, double c, doub
     yr = __dadd_rn(__dmul_rn(x, s), __dmul_rn(y, c));
 }
 
+// ---- bf16 keys: float32 rotation with a per-element exactness proof ----------
+//
+// The stored key is defined as the float64 evaluation of (x c - y s, x s + y c),
+// every product and sum rounded separately, rounded once to bf16.  With r the
+// float32 result and E a bound on |r - X| (X the float64 value), rounding to
+// nearest is monotone, so RN(r - E) == RN(r + E) implies RN(X) == RN(r).
+// Elements where a bf16 rounding boundary lies within E (about one in a
+// thousand) are evaluated in float64.
+
+// The rare exact evaluation, kept out of line so that the common path carries no
+// (predicated) float64 instructions.
+static __device__ __noinline__ __nv_bfloat16 rope_bf16_fallback(float xf, float yf, const double2* table, int64_t ti,
+                                                         bool second) {
+    double2 cs = make_double2(1.0, 0.0);
+    if (table) cs = table[ti];
+    double xr, yr;
+    rope_pair_f64((double)xf, (double)yf, cs.x, cs.y, xr, yr);
+    return f64_to_bf16_rn(second ? yr : xr);
+}
+
+// One component of the rotated pair (second: x s + y c, else x c - y s) in
+// float32 with one fused multiply-add; the bound covers the float32 rounding of
+// cos/sin, of the other product and of the fused operation with a factor of 4
+// to spare (each is at most 2^-24 relative to the terms' magnitudes).
+static __device__ __forceinline__ __nv_bfloat16 rope_bf16_exact(float xf, float yf, float cf, float sf,
+                                                        const double2* table, int pos, int pairs, int j,
+                                                        bool second) {
+    const float t2 = second ? xf * sf : yf * sf;
+    const float t1a = second ? yf : xf;
+    const float r = second ? fmaf(t1a, cf, t2) : fmaf(t1a, cf, -t2);
+    const float bound = 0x1p-20f * (fabsf(t1a * cf) + fabsf(t2) + fabsf(r)) + 0x1p-140f;
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r - bound);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(r + bound);
+    if (__builtin_expect(__bfloat16_as_ushort(lo) == __bfloat16_as_ushort(hi), 1)) return lo;
+    return rope_bf16_fallback(xf, yf, table, (int64_t)pos * pairs + j, second);
+}
+
 // ---- warp reductions -------------------------------------------------------
 
 template <typename A> __device__ __forceinline__ A warp_sum(A v) {

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,6 +63,7 @@ struct Handle {
     void* qrot_chunk = nullptr;    // [B][H_q][S][d_h] rotated queries of a chunk
     size_t qrot_chunk_bytes = 0;
     int* work_counter = nullptr;   // dynamic tile scheduler counter
+    unsigned* lane_ticket = nullptr;  // [B*H_kv] split counters of the fused decode step
 
     // TMA descriptors over each layer's keys and values (bf16, d_h = 128):
     // 64-row boxes for decode, 128-row boxes for the suffix-chunk kernel
@@ -84,6 +86,7 @@ struct Handle {
     int64_t opt_split_rows = 0;
     int64_t opt_force_generic = 0;
     int64_t opt_suffix_kernel = 0;
+    int64_t opt_decode_fused = 1;
 
     int B() const { return cfg.batch; }
     int Hq() const { return cfg.heads_q; }
@@ -124,14 +127,28 @@ struct GenericAttendLaunch {
 };
 cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaStream_t s);
 
+constexpr int kFusedMaxB = 256;   // sequences whose lengths travel as kernel parameters
+
 struct DecodeLaunch {
     const CUtensorMap* tmK; const CUtensorMap* tmV;
-    const float* qrot;       // [B,H_q,128]
-    const int32_t* len;      // [B] old length: t = len + 1
+    const float* qrot;       // [B,H_q,128] rotated queries (separate-kernel step)
+    const int32_t* len;      // [B] old length: t = len + 1 (separate-kernel step)
     float* part_o; float2* part_ml;
     float* out;              // [B,H_q,128]
     uint32_t* err;
     int B, Hq, Hkv, C, split_rows, max_splits;
+    // Fused step (append + attend + split merge + length commit in one launch).
+    int fused;
+    const __nv_bfloat16* q_in;           // [B,H_q,128] new queries, unrotated
+    const __nv_bfloat16* k_in;           // [B,H_kv,128] new keys, unrotated
+    const __nv_bfloat16* v_in;           // [B,H_kv,128] new values
+    __nv_bfloat16* K; __nv_bfloat16* V;  // the layer's storage
+    int32_t* positions;                  // [B][C]
+    int32_t* len_out; int32_t* next_out; // device lengths / next positions to commit
+    const float2* rope_f; const double2* rope;
+    unsigned* lane_ticket;               // [B*H_kv] split counters, zero between launches
+    int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
+    int32_t pos[kFusedMaxB];
 };
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);

@@ -27,34 +27,6 @@
 
 namespace kvc {
 
-// r = a * b1 - c * d1 (sub) or a * b1 + c * d1 in float32 with one fused
-// multiply-add; the bound below covers the float32 rounding of cos/sin, of
-// the product c * d1 and of the fused operation with a factor of 4 to spare
-// (each is at most 2^-24 relative to the terms' magnitudes).
-// The rare exact evaluation, kept out of line so that the common path carries no
-// (predicated) float64 instructions.
-__device__ __noinline__ __nv_bfloat16 rope_bf16_fallback(float xf, float yf, const double2* table, int64_t ti,
-                                                         bool second) {
-    double2 cs = make_double2(1.0, 0.0);
-    if (table) cs = table[ti];
-    double xr, yr;
-    rope_pair_f64((double)xf, (double)yf, cs.x, cs.y, xr, yr);
-    return f64_to_bf16_rn(second ? yr : xr);
-}
-
-__device__ __forceinline__ __nv_bfloat16 rope_bf16_exact(float xf, float yf, float cf, float sf,
-                                                        const double2* table, int pos, int pairs, int j,
-                                                        bool second) {
-    const float t2 = second ? xf * sf : yf * sf;
-    const float t1a = second ? yf : xf;
-    const float r = second ? fmaf(t1a, cf, t2) : fmaf(t1a, cf, -t2);
-    const float bound = 0x1p-20f * (fabsf(t1a * cf) + fabsf(t2) + fabsf(r)) + 0x1p-140f;
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r - bound);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(r + bound);
-    if (__builtin_expect(__bfloat16_as_ushort(lo) == __bfloat16_as_ushort(hi), 1)) return lo;
-    return rope_bf16_fallback(xf, yf, table, (int64_t)pos * pairs + j, second);
-}
-
 template <typename T, int P>
 struct alignas((2 * P * sizeof(T)) >= 16 ? 16 : (2 * P * sizeof(T))) Pack { T v[2 * P]; };
 

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 BASE = 10000.0
 
 
-def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0):
+def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0, fused=True):
     """Prefill ragged prefixes, run `steps` decode steps; return (cache, outs, inputs)."""
     need_gpu()
     B = len(L0)
@@ -34,6 +34,8 @@ def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, see
         cache.set_option(L.OPT_FORCE_GENERIC, 1)
     if split_rows:
         cache.set_option(L.OPT_DECODE_SPLIT_ROWS, split_rows)
+    if not fused:
+        cache.set_option(L.OPT_DECODE_FUSED, 0)
     S = max(max(L0), 1)
     cache.prefill_suffix(0, qd[:, :, :S].contiguous(), kd[:, :, :S].contiguous(), vd[:, :, :S].contiguous(),
                          seqlen=L0, out=False)
@@ -159,3 +161,20 @@ def test_bf16_without_rope_stores_inputs_unchanged():
         assert torch.equal(Ks[b, :, :n].view(torch.int16).cpu(), kd[b, :, :n].view(torch.int16).cpu())
         ref = A.decode_steps_reference(qn[b, :, L0[b]][None], kn[b, :, :n], vn[b, :, :n], L0[b], 0, "bf16")
         assert np.abs(out[b, :, 0] - ref[0]).max() <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("Hkv,split_rows", [(8, 0), (2, 64), (1, 128)])
+def test_fused_and_separate_decode_steps_agree(Hkv, split_rows):
+    """One launch per step (append + attend + merge + commit) against the separate
+    kernels: both match the oracle; stored rows, positions and lengths are identical."""
+    L0, steps = [1, 64, 257, 100], 3
+    caches, outs = [], []
+    for fused in (True, False):
+        cache, o, qkv = run_decode("bf16", 128, 32, Hkv, L0, steps, C=400, split_rows=split_rows, fused=fused)
+        check_against_oracle("bf16", cache, o, qkv, L0, steps)
+        caches.append(cache)
+        outs.append(np.stack(o))
+    for x, y in zip(storage_np(caches[0]), storage_np(caches[1])):
+        np.testing.assert_array_equal(x, y)
+    assert caches[0].get_lengths(0) == caches[1].get_lengths(0)
+    assert np.abs(outs[0] - outs[1]).max() < 5e-3
