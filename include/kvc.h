@@ -264,8 +264,9 @@ typedef enum kvc_option {
     KVC_OPT_FORCE_GENERIC = 2,     /* 1 = use the dtype-generic CUDA-core kernels even for bf16, d_h = 128 */
     KVC_OPT_SUFFIX_KERNEL = 3,     /* 0 = automatic, 1 = generic, 2 = tensor-core tile kernel */
     KVC_OPT_TIMING = 4,            /* 1 = record a CUDA event pair around every kernel launch */
-    KVC_OPT_DECODE_FUSED = 5       /* 1 (default) = one launch per bf16 decode step when B <= 256 and
-                                      H_q / H_kv <= 16; 0 = separate append, attend, merge and commit kernels */
+    KVC_OPT_DECODE_FUSED = 5       /* 1 (default) = bf16 decode steps with B <= 256 append, attend and
+                                      commit in one launch (plus a merge launch when H_q / H_kv > 16);
+                                      0 = separate append, attend, merge and commit kernels */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

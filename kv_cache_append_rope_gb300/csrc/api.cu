@@ -581,9 +581,11 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         } else {
             const int G = Hq / Hkv;
             const int64_t target = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(G) * 4;
+            // about four waves of CTAs, but at least 256 rows per query head served
+            // (a CTA's fixed work -- queries, pipeline fill, merge -- grows with G)
             int64_t r = (total_keys * Hkv + target - 1) / target;
+            r = std::max<int64_t>(r, 256 * G);
             r = (r + 63) / 64 * 64;
-            r = std::max<int64_t>(r, 256);
             r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
             split_rows = (int)r;
         }
@@ -591,10 +593,10 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         if (max_splits > 1 && (st = ensure_partials(h, max_splits)) != KVC_OK) return st;
     }
 
-    // One launch per step (append, attend, merge splits, commit lengths) up to 16
-    // query heads per key/value head; beyond that the merge done by one CTA per
-    // lane costs more than a separate merge kernel spread over every query head.
-    if (fast && h->opt_decode_fused && B <= kFusedMaxB && Hq / Hkv <= 16) {
+    // One launch per step (append, attend, merge splits, commit lengths); beyond 16
+    // query heads per key/value head the merge done by one CTA per lane costs more
+    // than a separate merge kernel spread over every query head, so it follows.
+    if (fast && h->opt_decode_fused && B <= kFusedMaxB) {
         DecodeLaunch dl{};
         dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
@@ -606,11 +608,14 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         dl.positions = h->pos_layer(layer);
         dl.len_out = h->len_layer(layer); dl.next_out = h->next_layer(layer);
         dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
+        dl.merge_in_kernel = Hq / Hkv <= 16;
         for (int b = 0; b < B; ++b) {
             dl.old_len[b] = lenh[b];
             dl.pos[b] = nexth[b];
         }
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
+        if (!dl.merge_in_kernel && max_splits > 1)
+            KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
         for (int b = 0; b < B; ++b) {
             lenh[b] += 1;
             nexth[b] += 1;

@@ -14,9 +14,10 @@
 // new row was already appended by the RoPE/append kernel).  One producer warp
 // streams 64-row K and V tiles with TMA (128-byte swizzle, no multicast) into
 // a ring of shared-memory stages guarded by mbarriers; four consumer warps
-// each take 16 rows of every stage and compute S = Q K^T and O += P V with
-// m16n8k16 bf16 tensor-core MMAs (fp32 accumulation), the G query heads
-// padded to 16 (or 32) MMA rows.  The softmax is online per warp (running
+// each own one 16-row MMA tile of the G query heads (padded to 16 or 32 rows)
+// and 16 (one tile) or 32 (two tiles) keys of every stage, and compute
+// S = Q K^T and O += P V with m16n8k16 bf16 tensor-core MMAs (fp32
+// accumulation).  The softmax is online per warp (running
 // max and sum in log2 units, quad shuffles for row maxima); the four warps
 // are merged through shared memory and the split's (O, max, sum) is written
 // to scratch, or the normalised output when the lane has a single split.  A
@@ -27,7 +28,9 @@
 // last split rotates and stores the new key row (bit-exact bf16 rounding) and
 // the value row before its TMA loads read them; the consumers rotate the new
 // queries in registers; the last CTA of a lane to finish (an atomic ticket, no
-// waiting) merges the splits; one CTA per sequence commits the new length.
+// waiting) merges the splits -- or, with more than 16 query heads per lane,
+// the separate merge kernel does, spread over every query head -- and one CTA
+// per sequence commits the new length.
 #include <cuda.h>
 
 #include "device_common.cuh"
@@ -51,7 +54,7 @@ constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 /*align*/ + 256 
 
 template <int MT> struct Cfg;
 template <> struct Cfg<1> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
-template <> struct Cfg<2> { static constexpr int STAGES = 4; static constexpr int MINB = 1; };
+template <> struct Cfg<2> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
 
 // Rotated query pair (c, c+1) of row `row` (< G) of this lane, as float32 (fused step).
 __device__ __forceinline__ float2 fused_q_pair(const DecodeLaunch& a, int b, int qh, int c, int pos) {
@@ -105,8 +108,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     __syncthreads();
 
     int issued = 0;
-    float o[MT][16][4];
-    float m[MT][2], l[MT][2];
+    float o[16][4];
+    float m[2], l[2];
 
     if (warp == NCW) {
         // ---------------- producer ----------------
@@ -163,14 +166,24 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
     } else {
         // ---------------- consumers ----------------
-        const int qa = lane >> 2;          // fragment row (and row + 8)
-        const int qc = (lane & 3) * 2;     // fragment column pair
+        // Each consumer warp owns one 16-row MMA tile of the G query heads and
+        // KW = 16 * MT keys of every 64-key stage: with MT = 2 (G up to 32),
+        // warps 0-1 hold heads 0-15 and warps 2-3 heads 16-31, each pair
+        // splitting the stage's keys, so that every warp keeps one tile of
+        // accumulators in registers and two CTAs fit on an SM.
+        constexpr int KW = 16 * MT;              // keys per warp per stage
+        constexpr int NT = KW / 8;               // n8 tiles of S
+        constexpr int KS = KW / 16;              // k16 steps of P V
+        constexpr int WPM = NCW / MT;            // warps per m tile
+        const int mtw = warp / WPM;
+        const int kofs = (warp % WPM) * KW;
+        const int qa = lane >> 2;                // fragment row (and row + 8)
+        const int qc = (lane & 3) * 2;           // fragment column pair
         // Q fragments, pre-scaled so that scores come out in log2 units.
         const float qscale = 1.4426950408889634f * rsqrtf((float)D);
-        uint32_t qf[MT][8][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int ra = mt * 16 + qa, rb = ra + 8;
+        uint32_t qf[8][4];
+        {
+            const int ra = mtw * 16 + qa, rb = ra + 8;
             const float* qra = a.qrot + ((int64_t)b * a.Hq + hkv * G + ra) * D;
             const float* qrb = a.qrot + ((int64_t)b * a.Hq + hkv * G + rb) * D;
             const int qpos = FUSED ? a.pos[b] : 0;
@@ -190,21 +203,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     x2 = ra < G ? *(const float2*)(qra + c + 8) : make_float2(0.f, 0.f);
                     x3 = rb < G ? *(const float2*)(qrb + c + 8) : make_float2(0.f, 0.f);
                 }
-                qf[mt][ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
-                qf[mt][ks][1] = pack_bf16(x1.x * qscale, x1.y * qscale);
-                qf[mt][ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
-                qf[mt][ks][3] = pack_bf16(x3.x * qscale, x3.y * qscale);
+                qf[ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
+                qf[ks][1] = pack_bf16(x1.x * qscale, x1.y * qscale);
+                qf[ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
+                qf[ks][3] = pack_bf16(x3.x * qscale, x3.y * qscale);
             }
         }
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            m[mt][0] = m[mt][1] = -INFINITY;
-            l[mt][0] = l[mt][1] = 0.f;
+        for (int n = 0; n < 16; ++n)
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[mt][n][e] = 0.f;
-        }
+            for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
 
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % STAGES;
@@ -215,93 +225,83 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
             const uint32_t kt = smem_u32(smem + s * STAGE_BYTES);
             const uint32_t vt = kt + TILE_BYTES;
-            const int key_base = r0 + i * KT + warp * 16;
+            const int key_base = r0 + i * KT + kofs;
 
-            // ---- S = Q K^T for this warp's 16 keys (two n8 tiles)
-            float sc[MT][2][4];
+            // ---- S = Q K^T for this warp's KW keys
+            float sc[NT][4];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int row = warp * 16 + nt * 8 + (lane & 7);
+            for (int nt = 0; nt < NT; ++nt) {
+                const int row = kofs + nt * 8 + (lane & 7);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const int dim0 = kk * 32 + (lane >> 3) * 8;
                     const uint32_t addr = kt + (dim0 >> 6) * HALF_BYTES + swz128(row, (dim0 & 63) >> 3);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        mma_bf16_16816(sc[mt][nt], qf[mt][2 * kk], b0, b1);
-                        mma_bf16_16816(sc[mt][nt], qf[mt][2 * kk + 1], b2, b3);
-                    }
+                    mma_bf16_16816(sc[nt], qf[2 * kk], b0, b1);
+                    mma_bf16_16816(sc[nt], qf[2 * kk + 1], b2, b3);
                 }
             }
             // ---- mask keys beyond this split
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = key_base + nt * 8 + qc + e;
                     if (key >= r1) {
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            sc[mt][nt][e] = -INFINITY;
-                            sc[mt][nt][2 + e] = -INFINITY;
-                        }
+                        sc[nt][e] = -INFINITY;
+                        sc[nt][2 + e] = -INFINITY;
                     }
                 }
-            // ---- online softmax (rows qa and qa + 8 of each m tile)
-            uint32_t pf[MT][4];
+            // ---- online softmax (rows qa and qa + 8 of this m tile)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
+            for (int rr = 0; rr < 2; ++rr) {
+                float mx = -INFINITY;
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    float mx = fmaxf(fmaxf(sc[mt][0][2 * rr], sc[mt][0][2 * rr + 1]),
-                                     fmaxf(sc[mt][1][2 * rr], sc[mt][1][2 * rr + 1]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const float m_new = fmaxf(m[mt][rr], mx);
-                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                    const float corr = fast_exp2(m[mt][rr] - m_use);
-                    m[mt][rr] = m_new;
-                    float ps = 0.f;
+                for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * rr], sc[nt][2 * rr + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m[rr], mx);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float corr = fast_exp2(m[rr] - m_use);
+                m[rr] = m_new;
+                float ps = 0.f;
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float p = fast_exp2(sc[mt][nt][2 * rr + e] - m_use);
-                            sc[mt][nt][2 * rr + e] = p;
-                            ps += p;
-                        }
-                    l[mt][rr] = l[mt][rr] * corr + ps;
-#pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        o[mt][n][2 * rr] *= corr;
-                        o[mt][n][2 * rr + 1] *= corr;
+                    for (int e = 0; e < 2; ++e) {
+                        const float p = fast_exp2(sc[nt][2 * rr + e] - m_use);
+                        sc[nt][2 * rr + e] = p;
+                        ps += p;
                     }
+                l[rr] = l[rr] * corr + ps;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][2 * rr] *= corr;
+                    o[n][2 * rr + 1] *= corr;
                 }
-                pf[mt][0] = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-                pf[mt][1] = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-                pf[mt][2] = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-                pf[mt][3] = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
             }
             // ---- O += P V (V^T fragments through transposing ldmatrix)
-            const int vrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                const int dim = np * 16 + (lane >> 4) * 8;
-                const uint32_t addr = vt + (dim >> 6) * HALF_BYTES + swz128(vrow, (dim & 63) >> 3);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(addr, b0, b1, b2, b3);
+            for (int k2 = 0; k2 < KS; ++k2) {
+                uint32_t pf[4];
+                pf[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
+                pf[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
+                pf[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
+                pf[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+                const int vrow = kofs + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    mma_bf16_16816(o[mt][2 * np], pf[mt], b0, b1);
-                    mma_bf16_16816(o[mt][2 * np + 1], pf[mt], b2, b3);
+                for (int np = 0; np < 8; ++np) {
+                    const int dim = np * 16 + (lane >> 4) * 8;
+                    const uint32_t addr = vt + (dim >> 6) * HALF_BYTES + swz128(vrow, (dim & 63) >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * np], pf, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
                 }
             }
             __syncwarp();
@@ -320,39 +320,37 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         return;
     }
 
-    // ---------------- merge the four consumer warps ----------------
-    float* Om = (float*)smem;                                    // [NCW][MT*16][D]
-    float2* ML = (float2*)(smem + NCW * MT * 16 * D * 4);        // [NCW][MT*16]
+    // ---------------- merge the consumer warps of each m tile ----------------
+    constexpr int WPMr = NCW / MT;                               // warps per m tile
+    float* Om = (float*)smem;                                    // [NCW][16][D]
+    float2* ML = (float2*)(smem + NCW * 16 * D * 4);             // [NCW][16]
     if (warp < NCW) {
         const int qa = lane >> 2, qc = (lane & 3) * 2;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+        for (int rr = 0; rr < 2; ++rr) {
+            float lr = l[rr];
+            lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+            lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+            const int row = qa + rr * 8;
+            float* dst = Om + ((size_t)warp * 16 + row) * D;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                float lr = l[mt][rr];
-                lr += __shfl_xor_sync(0xffffffffu, lr, 1);
-                lr += __shfl_xor_sync(0xffffffffu, lr, 2);
-                const int row = mt * 16 + qa + rr * 8;
-                float* dst = Om + ((size_t)warp * MT * 16 + row) * D;
-#pragma unroll
-                for (int n = 0; n < 16; ++n)
-                    *(float2*)(dst + n * 8 + qc) = make_float2(o[mt][n][2 * rr], o[mt][n][2 * rr + 1]);
-                if ((lane & 3) == 0) ML[warp * MT * 16 + row] = make_float2(m[mt][rr], lr);
-            }
+            for (int n = 0; n < 16; ++n) *(float2*)(dst + n * 8 + qc) = make_float2(o[n][2 * rr], o[n][2 * rr + 1]);
+            if ((lane & 3) == 0) ML[warp * 16 + row] = make_float2(m[rr], lr);
         }
     }
     __syncthreads();
     for (int u = threadIdx.x; u < G * D; u += THREADS) {
         const int g = u / D, dim = u - g * D;
+        const int w0 = (g >> 4) * WPMr, gl = g & 15;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ML[w * MT * 16 + g].x);
+        for (int w = 0; w < WPMr; ++w) M = fmaxf(M, ML[(w0 + w) * 16 + gl].x);
         float O = 0.f, L = 0.f;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-            const float2 ml = ML[w * MT * 16 + g];
+        for (int w = 0; w < WPMr; ++w) {
+            const float2 ml = ML[(w0 + w) * 16 + gl];
             const float f = fast_exp2(ml.x - M);
-            O += Om[((size_t)w * MT * 16 + g) * D + dim] * f;
+            O += Om[((size_t)(w0 + w) * 16 + gl) * D + dim] * f;
             L += ml.y * f;
         }
         const int64_t qh = (int64_t)b * a.Hq + hkv * G + g;
@@ -364,7 +362,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             if (dim == 0) a.part_ml[idx] = make_float2(M, L);
         }
     }
-    if (!FUSED || nsplit_lane == 1) return;
+    if (!FUSED || nsplit_lane == 1 || !a.merge_in_kernel) return;
 
     // Fused step: the last CTA of this lane to finish merges every split (a ticket,
     // no waiting), then resets the ticket for the next step.
@@ -400,7 +398,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     const int qh = blockIdx.x;
     const int b = qh / a.Hq;
-    const int t = a.len[b] + 1;
+    const int t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
     const int ns = (t + a.split_rows - 1) / a.split_rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;

@@ -147,6 +147,7 @@ struct DecodeLaunch {
     int32_t* len_out; int32_t* next_out; // device lengths / next positions to commit
     const float2* rope_f; const double2* rope;
     unsigned* lane_ticket;               // [B*H_kv] split counters, zero between launches
+    int merge_in_kernel;                 // 1: the last CTA of a lane merges its splits
     int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
     int32_t pos[kFusedMaxB];
 };
