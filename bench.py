@@ -42,6 +42,19 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 
+# DRAM traffic of the dominant kernel from ncu captures of smaller cases of the
+# same kernel build (dram__bytes_read.sum + dram__bytes_write.sum per launch),
+# scaled to a full launch: decode traffic grows with the K/V bytes streamed
+# (ratio to the algorithmic bytes), the tile kernel's with the number of
+# sequences (each sequence's K/V comes from DRAM about once, then from L2).
+# Summaries: profiles/decode_bf16_mha_small_full.md,
+# profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
+TRAFFIC = {
+    "mha_decode": ("ratio", 508121088.0 / 499236864.0),
+    "mqa_decode": ("ratio", (217853952.0 + 3947776.0) / 217403392.0),
+    "suffix": ("per_sequence", 375261440.0 + 170027776.0),
+}
+
 
 def parse():
     p = argparse.ArgumentParser()
@@ -407,16 +420,22 @@ def run_ours(args, name, world, rank, local):
 
     # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / event-timed duration
     alg = bench.dominant_algorithmic(dom_launches)
+    traffic = None
+    kind = TRAFFIC.get(bench.config()["workload"])
+    if kind and kind[0] == "ratio":
+        traffic = round(kind[1] * alg / dom_launches)
+    elif kind and kind[0] == "per_sequence":
+        traffic = round(kind[1] * bench.cfg["B"])
     if unit == "GB/s":
         achieved = alg / 1e9 / (dom_ms / 1e3)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None, "kernel": "decode_bf16_kernel",
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": "decode_bf16_kernel",
                 "peak_source": f"{peak_kind} hbm_gbs", "kernel_ms_per_launch": round(dom_ms / dom_launches, 5),
                 "algorithmic_bytes_per_launch": round(alg / dom_launches)}
     else:
         achieved = alg / 1e12 / (dom_ms / 1e3)
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tflops, "unit": "TFLOP/s",
-                "frac": round(achieved / tflops, 4), "traffic": None, "kernel": dom,
+                "frac": round(achieved / tflops, 4), "traffic": traffic, "kernel": dom,
                 "peak_source": f"{peak_kind} bf16_tflops (burst)", "kernel_ms_per_launch": round(dom_ms / dom_launches, 3),
                 "algorithmic_flops_per_launch": round(alg / dom_launches)}
 

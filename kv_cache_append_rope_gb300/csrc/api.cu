@@ -583,8 +583,10 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
             const int64_t target = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(G) * 4;
             // about four waves of CTAs, but at least 256 rows per query head served
             // (a CTA's fixed work -- queries, pipeline fill, merge -- grows with G)
-            int64_t r = (total_keys * Hkv + target - 1) / target;
-            r = std::max<int64_t>(r, 256 * G);
+            // as long as that still leaves one CTA per SM
+            const int64_t keys = total_keys * Hkv;
+            int64_t r = (keys + target - 1) / target;
+            r = std::max<int64_t>(r, std::min<int64_t>(256 * G, keys / sm_count(h->cfg.device)));
             r = (r + 63) / 64 * 64;
             r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
             split_rows = (int)r;
