@@ -358,10 +358,12 @@ def dist_setup(args):
 
 
 def max_over_ranks(x, world):
+    """The largest of every rank's value (NCCL: through the GPU; gloo: on the host)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
