@@ -56,16 +56,17 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;
 constexpr int OFF_V = OFF_K + KST * TILE;
 constexpr int OFF_BAR = OFF_V + VST * TILE;
-constexpr int SMEM_BYTES = OFF_BAR + 4096 + 1024;
-constexpr int NSW = 8;                     // softmax warps: two per TMEM sub-partition
+constexpr int SMEM_BYTES = OFF_BAR + 8192 + 1024;
+constexpr int WPS = 2;                     // softmax warps per TMEM sub-partition
+constexpr int NSW = 4 * WPS;               // softmax warps
 constexpr int THREADS = (2 + NSW) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_P0 = 384, COL_P1 = 448;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct Bars {
-    float red_max[2][2][BM];   // [tile parity][column half][row]: partial row maxima
-    float red_sum[2][BM];      // [column half][row]: partial row sums
+    float red_max[2][WPS][BM]; // [tile parity][column part][row]: partial row maxima
+    float red_sum[WPS][BM];    // [column part][row]: partial row sums
     uint64_t q_full;
     uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
     uint64_t s_full[2], s_free[2];
@@ -79,6 +80,12 @@ struct Bars {
 __device__ __forceinline__ void fail_wait(Bars* bars, uint32_t* err) {
     *(volatile int*)&bars->err = 1;
     atomicOr(err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // A bounded wait taken by every lane of a warp, with one verdict for the whole warp.
@@ -117,9 +124,9 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         }
         mbar_init(smem_u32(&bars->mma_done), 1);
         for (int q = 0; q < 4; ++q) {
-            mbar_init(smem_u32(&bars->xchg[q][0]), 64);
-            mbar_init(smem_u32(&bars->xchg[q][1]), 64);
-            mbar_init(smem_u32(&bars->fin[q]), 64);
+            mbar_init(smem_u32(&bars->xchg[q][0]), 32 * WPS);
+            mbar_init(smem_u32(&bars->xchg[q][1]), 32 * WPS);
+            mbar_init(smem_u32(&bars->fin[q]), 32 * WPS);
         }
         bars->err = 0;
         fence_mbar_init();
@@ -227,11 +234,11 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Warp w (2..9) reads TMEM lanes 32 * (w % 4) .. + 31 (its sub-partition);
-        // warps 2-5 take columns 0-63 of those rows, warps 6-9 columns 64-127.
-        constexpr int HC = BN / 2;                   // columns per warp
+        // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its sub-partition); the
+        // WPS warps of a sub-partition take consecutive column parts of those rows.
+        constexpr int HC = BN / WPS;                 // columns per warp
         const int sub = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - 2) >> 2;            // column part
         const int row = sub * 32 + lane;             // query row inside the tile = TMEM lane
         const int i = qt * BM + row;
         const int qslot = cut + i;
@@ -248,8 +255,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             tc_fence_after();
             float x[HC];
             const uint32_t s_col = (s ? COL_S1 : COL_S0) + half * HC;
-            tmem_ld32(lane_addr + s_col, x);
-            tmem_ld32(lane_addr + s_col + 32, x + 32);
+#pragma unroll
+            for (int c = 0; c < HC / 32; ++c) tmem_ld32(lane_addr + s_col + c * 32, x + c * 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -260,23 +267,30 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 #pragma unroll
                 for (int c = 0; c < HC; ++c) x[c] = (kbase + c > qslot) ? -INFINITY : x[c];
             }
-            // row maximum: 8 independent chains here, then the partner warp's half
+            // row maximum over this part (8 independent chains of 3-input maxima),
+            // then over the other parts of the same rows
             float m8[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) m8[q] = x[q];
 #pragma unroll
-            for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+            for (int c = 8; c + 16 <= HC; c += 16)
 #pragma unroll
-            for (int w8 = 4; w8 > 0; w8 >>= 1)
+                for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[c + q], x[c + 8 + q]);
+            if constexpr ((HC - 8) % 16 != 0) {
 #pragma unroll
-                for (int q = 0; q < w8; ++q) m8[q] = fmaxf(m8[q], m8[q + w8]);
-            bars->red_max[s][half][row] = m8[0];
+                for (int q = 0; q < 8; ++q) m8[q] = fmaxf(m8[q], x[HC - 8 + q]);
+            }
+            float mpart = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            bars->red_max[s][half][row] = mpart;
             mbar_arrive(smem_u32(&bars->xchg[sub][s]));
             if (!warp_wait(smem_u32(&bars->xchg[sub][s]), (j >> 1) & 1, a.err)) {
                 ok = false;
                 break;
             }
-            const float mx = fmaxf(m8[0], bars->red_max[s][half ^ 1][row]);
+            float mx = mpart;
+#pragma unroll
+            for (int q = 0; q < WPS; ++q)
+                if (q != half) mx = fmaxf(mx, bars->red_max[s][q][row]);
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + RESCALE_LOG2 || (j == 0);
             const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
@@ -304,28 +318,33 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             m_run = m_new;
             const float mu = m_run == -INFINITY ? 0.f : m_run;
             // P in registers first: the exponentials overlap the previous tile's PV.
+            // (packed float32x2 FMA for the arguments and packed adds for the sums:
+            // the softmax warps are issue-bound, so fewer instructions matter)
             uint32_t pk[HC / 2];
-            float l8[8];
+            float2 l4[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+            for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
+            const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
 #pragma unroll
             for (int e = 0; e < HC / 2; ++e) {
-                const float p0 = fast_exp2(fmaf(x[2 * e], sl2, -mu));
-                const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl2, -mu));
-                l8[e & 7] += p0 + p1;
+                const float2 arg = __ffma2_rn(make_float2(x[2 * e], x[2 * e + 1]), sl2v, negmu);
+                const float p0 = fast_exp2(arg.x);
+                const float p1 = fast_exp2(arg.y);
+                l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
                 pk[e] = pack_bf16(p0, p1);
             }
-#pragma unroll
-            for (int w8 = 4; w8 > 0; w8 >>= 1)
-#pragma unroll
-                for (int q = 0; q < w8; ++q) l8[q] += l8[q + w8];
-            l_run += l8[0];
+            l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+            l_run += l4[0].x + l4[0].y;
             // P buffer s was last read by the PV of tile j-2.
             if (j >= 2 && !warp_wait(smem_u32(&bars->pv_done[s]), ((j >> 1) - 1) & 1, a.err)) {
                 ok = false;
                 break;
             }
-            tmem_st32u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
+            if constexpr (HC / 2 == 32) {
+                tmem_st32u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
+            } else {
+                tmem_st16u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -339,7 +358,10 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 ok = false;
             } else {
                 tc_fence_after();
-                const float inv = 1.0f / (bars->red_sum[0][row] + bars->red_sum[1][row]);
+                float lsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < WPS; ++q) lsum += bars->red_sum[q][row];
+                const float inv = 1.0f / lsum;
                 float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D + half * HC;
 #pragma unroll
                 for (int c = 0; c < HC / 32; ++c) {
