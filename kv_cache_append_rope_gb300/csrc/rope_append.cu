@@ -113,14 +113,14 @@ __global__ void __launch_bounds__(256) rope_append_kernel(AppendLaunch a) {
     const int64_t total = (int64_t)a.B * heads_all * groups * chunks;
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
-        // consecutive threads: the chunks of one row, then row groups of the same head
-        // (contiguous in memory), then heads, then sequences
+        // consecutive threads: the chunks of one row, then the heads of the same rows
+        // (a warp shares their cos/sin entries in L1), then row groups, then sequences
         const int c = (int)(u % chunks);
         int64_t r = u / chunks;
-        const int ig = (int)(r % groups);
-        r /= groups;
         const int hh = (int)(r % heads_all);
-        const int b = (int)(r / heads_all);
+        r /= heads_all;
+        const int ig = (int)(r % groups);
+        const int b = (int)(r / groups);
         const int rows = a.seqlen ? a.seqlen[b] : a.S;
         const int i0 = ig * kRows;
         if (i0 >= rows) continue;
