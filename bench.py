@@ -195,20 +195,44 @@ class DecodeBench:
         self.hk = self.k.cpu().pin_memory()
         self.hv = self.v.cpu().pin_memory()
         self.hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        self.dq = torch.empty_like(self.q[0])
-        self.dk = torch.empty_like(self.k[0])
-        self.dv = torch.empty_like(self.v[0])
+        # two device input buffers: step i+1 uploads while step i computes
+        self.dq = [torch.empty_like(self.q[0]) for _ in range(2)]
+        self.dk = [torch.empty_like(self.k[0]) for _ in range(2)]
+        self.dv = [torch.empty_like(self.v[0]) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(self.device)
         self.h2d = (self.hq.nbytes + self.hk.nbytes + self.hv.nbytes)
         self.d2h = self.hout.nbytes
 
+    def _upload(self, i):
+        s = i % 2
+        self.dq[s].copy_(self.hq[i], non_blocking=True)
+        self.dk[s].copy_(self.hk[i], non_blocking=True)
+        self.dv[s].copy_(self.hv[i], non_blocking=True)
+
     def e2e_step(self):
+        """Every step: its q/k/v uploaded from pinned host memory and its output read
+        back, on a copy stream overlapping the neighbouring steps' compute."""
+        compute, copy = torch.cuda.current_stream(self.device), self.copy_stream
         self.cache.truncate(self.L0.tolist())
+        uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        copy.wait_stream(compute)
+        with torch.cuda.stream(copy):
+            self._upload(0)
+            uploaded[0].record(copy)
         for i in range(self.steps):
-            self.dq.copy_(self.hq[i], non_blocking=True)
-            self.dk.copy_(self.hk[i], non_blocking=True)
-            self.dv.copy_(self.hv[i], non_blocking=True)
-            self.cache.append_attend(0, self.dq, self.dk, self.dv, out=self.out[i])
-            self.hout[i].copy_(self.out[i], non_blocking=True)
+            s = i % 2
+            compute.wait_event(uploaded[s])
+            self.cache.append_attend(0, self.dq[s], self.dk[s], self.dv[s], out=self.out[i], stream=compute)
+            consumed[s].record(compute)
+            with torch.cuda.stream(copy):
+                if i + 1 < self.steps:
+                    copy.wait_event(consumed[(i + 1) % 2]) if i >= 1 else None
+                    self._upload(i + 1)
+                    uploaded[(i + 1) % 2].record(copy)
+                copy.wait_event(consumed[s])
+                self.hout[i].copy_(self.out[i], non_blocking=True)
+        compute.wait_stream(copy)
 
     def dominant(self):
         return "decode"
@@ -294,16 +318,23 @@ class SuffixBench:
         self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
         self.hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         self.dq, self.dk, self.dv = (torch.empty_like(x) for x in (self.q, self.k, self.v))
+        self.copy_stream = torch.cuda.Stream(self.device)
         self.h2d = self.hq.nbytes + self.hk.nbytes + self.hv.nbytes
         self.d2h = self.hout.nbytes
 
     def e2e_step(self):
+        """Upload q/k/v (three streams of copies in parallel with the cut search on the
+        host), run the step, read the output back."""
         from kv_cache_append_rope_gb300 import kvc
-        cuts = [kvc.lcp(self.cached[b], self.query[b]) for b in range(self.cfg["B"])]
-        self.cache.truncate(cuts)
-        self.dq.copy_(self.hq, non_blocking=True)
+        compute, copy = torch.cuda.current_stream(self.device), self.copy_stream
+        copy.wait_stream(compute)
+        with torch.cuda.stream(copy):
+            self.dq.copy_(self.hq, non_blocking=True)
         self.dk.copy_(self.hk, non_blocking=True)
         self.dv.copy_(self.hv, non_blocking=True)
+        cuts = [kvc.lcp(self.cached[b], self.query[b]) for b in range(self.cfg["B"])]
+        self.cache.truncate(cuts)
+        compute.wait_stream(copy)
         self.cache.prefill_suffix(0, self.dq, self.dk, self.dv, seqlen=self.seqlen, out=self.out)
         self.hout.copy_(self.out, non_blocking=True)
 

@@ -264,9 +264,13 @@ typedef enum kvc_option {
     KVC_OPT_FORCE_GENERIC = 2,     /* 1 = use the dtype-generic CUDA-core kernels even for bf16, d_h = 128 */
     KVC_OPT_SUFFIX_KERNEL = 3,     /* 0 = automatic, 1 = generic, 2 = tensor-core tile kernel */
     KVC_OPT_TIMING = 4,            /* 1 = record a CUDA event pair around every kernel launch */
-    KVC_OPT_DECODE_FUSED = 5       /* 1 (default) = bf16 decode steps with B <= 256 append, attend and
+    KVC_OPT_DECODE_FUSED = 5,      /* 1 (default) = bf16 decode steps with B <= 256 append, attend and
                                       commit in one launch (plus a merge launch when H_q / H_kv > 16);
                                       0 = separate append, attend, merge and commit kernels */
+    KVC_OPT_TEST_STALL = 6         /* test only, applies to the next bf16 d_h = 128 decode step: its producer
+                                      issues no loads, so the consumers' bounded waits give up (about 1 s)
+                                      and the step reports a device error through kvc_check; the step's
+                                      outputs are undefined and the cache should then be reset */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

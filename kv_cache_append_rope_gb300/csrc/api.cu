@@ -611,6 +611,8 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         dl.len_out = h->len_layer(layer); dl.next_out = h->next_layer(layer);
         dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
         dl.merge_in_kernel = Hq / Hkv <= 16;
+        dl.test_stall = (int)h->opt_test_stall;
+        h->opt_test_stall = 0;
         for (int b = 0; b < B; ++b) {
             dl.old_len[b] = lenh[b];
             dl.pos[b] = nexth[b];
@@ -631,6 +633,8 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         dl.qrot = (const float*)h->qrot; dl.len = h->len_layer(layer);
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
+        dl.test_stall = (int)h->opt_test_stall;
+        h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
         if (max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
@@ -906,6 +910,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_DECODE_FUSED:
             h->opt_decode_fused = value != 0;
+            return KVC_OK;
+        case KVC_OPT_TEST_STALL:
+            h->opt_test_stall = value != 0;
             return KVC_OK;
     }
     return fail(h, KVC_ERR_CONFIG, "unknown option %d", option);

@@ -143,7 +143,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
         }
-        if (lane == 0) {
+        if (lane == 0 && !a.test_stall) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
             for (int i = 0; i < ntiles; ++i) {

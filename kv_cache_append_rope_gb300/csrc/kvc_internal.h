@@ -87,6 +87,7 @@ struct Handle {
     int64_t opt_force_generic = 0;
     int64_t opt_suffix_kernel = 0;
     int64_t opt_decode_fused = 1;
+    int64_t opt_test_stall = 0;
 
     int B() const { return cfg.batch; }
     int Hq() const { return cfg.heads_q; }
@@ -148,6 +149,7 @@ struct DecodeLaunch {
     const float2* rope_f; const double2* rope;
     unsigned* lane_ticket;               // [B*H_kv] split counters, zero between launches
     int merge_in_kernel;                 // 1: the last CTA of a lane merges its splits
+    int test_stall;                      // test only: the producer issues no loads (waits run out)
     int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
     int32_t pos[kFusedMaxB];
 };
