@@ -63,7 +63,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="mha_decode",
-                   choices=["mha_decode", "gqa_decode", "mqa_decode", "suffix", "all"])
+                   choices=["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix", "all"])
+    p.add_argument("--graph", action="store_true",
+                   help="decode workloads: lengths kept on the device, each bench step's decode calls "
+                        "captured once in a CUDA graph and replayed")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=0,
@@ -155,7 +158,7 @@ def gpu_index(local_rank):
 # ----------------------------------------------------------------- decode workloads
 
 class DecodeBench:
-    def __init__(self, name, device, batch=0):
+    def __init__(self, name, device, batch=0, graph=False):
         from kv_cache_append_rope_gb300 import workloads as W
         from kv_cache_append_rope_gb300.kvc import KVCache
         cfg = dict(W.CONFIGS[name])
@@ -184,11 +187,43 @@ class DecodeBench:
         # everything else the step must move: q/k/v rows in, new K/V rows written, outputs out
         self.io_bytes = float(steps * B * (Hq * D * 2 + 2 * Hkv * D * 2 + 2 * Hkv * D * 2 + Hq * D * 4))
         self.steps = steps
+        self.graph, self.graph_launches, self.replays = None, 0, 0
+        if graph:
+            self.capture()
 
     def step(self):
         self.cache.truncate(self.L0.tolist())
+        if self.graph is not None:
+            self.graph.replay()
+            self.replays += 1
+            return
         for i in range(self.steps):
             self.cache.append_attend(0, self.q[i], self.k[i], self.v[i], out=self.out[i])
+
+    def capture(self):
+        """Device-held lengths, then the step's decode calls recorded once in a CUDA graph."""
+        from kv_cache_append_rope_gb300 import _lib as L
+        self.cache.set_option(L.OPT_DEVICE_LENGTHS, 1)
+        self.step()                                   # uncaptured: allocates the split scratch
+        torch.cuda.synchronize(self.device)
+        self.cache.truncate(self.L0.tolist())
+        _, before = self.cache.kernel_stats(-1)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(self.steps):
+                self.cache.append_attend(0, self.q[i], self.k[i], self.v[i], out=self.out[i])
+        _, after = self.cache.kernel_stats(-1)
+        self.graph_launches = after - before
+        self.graph = g
+
+    def timing_pass(self):
+        """The step with per-launch events: a captured graph holds none, so replay it eagerly."""
+        g, self.graph = self.graph, None
+        self.step()
+        self.graph = g
+
+    def graph_kernel_launches(self):
+        return self.graph_launches * self.replays
 
     def e2e_setup(self):
         self.hq = self.q.cpu().pin_memory()
@@ -212,6 +247,14 @@ class DecodeBench:
     def e2e_step(self):
         """Every step: its q/k/v uploaded from pinned host memory and its output read
         back, on a copy stream overlapping the neighbouring steps' compute."""
+        if self.graph is not None:
+            # the graph reads the step's fixed input buffers: upload all, replay, read back
+            self.q.copy_(self.hq, non_blocking=True)
+            self.k.copy_(self.hk, non_blocking=True)
+            self.v.copy_(self.hv, non_blocking=True)
+            self.step()
+            self.hout.copy_(self.out, non_blocking=True)
+            return
         compute, copy = torch.cuda.current_stream(self.device), self.copy_stream
         self.cache.truncate(self.L0.tolist())
         uploaded = [torch.cuda.Event(), torch.cuda.Event()]
@@ -250,8 +293,14 @@ class DecodeBench:
         return {"workload": self.name, "B": c["B"], "H_q": c["Hq"], "H_kv": c["Hkv"], "d_h": c["D"], "C": c["C"],
                 "decode_steps_per_step": c["steps"], "old_length_range": [int(self.L0.min()), int(self.L0.max())],
                 "old_length_rule": f"uniform integers in [{c['lo']}, min({c['hi']}, C - steps)] from seed {c['seed']}",
-                "l2": "inputs larger than L2: each decode step streams "
-                      f"{self.kv_bytes / self.steps / 1e9:.2f} GB of K/V (L2 is 0.129 GB)"}
+                "l2": ("inputs larger than L2: each decode step streams "
+                       f"{self.kv_bytes / self.steps / 1e9:.2f} GB of K/V (L2 is 0.129 GB)")
+                if self.kv_bytes / self.steps > 0.129e9 else
+                ("K/V of a decode step fits in L2 "
+                 f"({self.kv_bytes / self.steps / 1e9:.3f} GB); the 64 steps stream "
+                 f"{self.kv_bytes / 1e9:.2f} GB; L2 not flushed between bench steps"),
+                "launch": f"CUDA graph of the {self.steps} decode calls, lengths on the device" if self.graph is not None
+                else "one kvc_append_attend call per decode step"}
 
     def oracle_sample(self, budget_s=15.0):
         """Oracle decode of sampled lanes (all steps); returns (seconds, bytes, description)."""
@@ -373,8 +422,8 @@ class SuffixBench:
 
 # ----------------------------------------------------------------- driver
 
-def make_bench(name, device, batch=0):
-    return SuffixBench(device, batch) if name == "suffix" else DecodeBench(name, device, batch)
+def make_bench(name, device, batch=0, graph=False):
+    return SuffixBench(device, batch) if name == "suffix" else DecodeBench(name, device, batch, graph)
 
 
 def dist_setup(args):
@@ -417,12 +466,14 @@ def run_ours(args, name, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     hbm, tflops, peak_kind = peaks()
-    bench = make_bench(name, device, args.batch)
+    bench = make_bench(name, device, args.batch, args.graph)
     cache = bench.cache
     for _ in range(args.warmup):
         bench.step()
     torch.cuda.synchronize(device)
     cache.reset_stats()
+    if hasattr(bench, "replays"):
+        bench.replays = 0
     stream = torch.cuda.current_stream(device)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # pass 1: the whole step, device-timed, no per-kernel events
@@ -437,12 +488,14 @@ def run_ours(args, name, world, rank, local):
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
     _, launches = cache.kernel_stats(-1)
+    if getattr(bench, "graph", None) is not None:
+        launches += bench.graph_kernel_launches()     # kernels the replayed graphs launched
     # pass 2: the same steps again with a CUDA event pair recorded by the library
     # around every launch on its stream, for the dominant kernel's duration
     cache.reset_stats()
     cache.set_option(L.OPT_TIMING, 1)
     for _ in range(args.steps):
-        bench.step()
+        getattr(bench, "timing_pass", bench.step)()
     torch.cuda.synchronize(device)
     dom = bench.dominant()
     dom_ms, dom_launches = cache.kernel_stats(dom)
@@ -539,7 +592,8 @@ def main():
     if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:
         return                                   # the oracle arm runs on rank 0 only
     world, rank, local = dist_setup(args) if args.impl == "ours" else (1, 0, 0)
-    names = ["mha_decode", "gqa_decode", "mqa_decode", "suffix"] if args.workload == "all" else [args.workload]
+    names = (["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix"] if args.workload == "all"
+             else [args.workload])
     for name in names:
         if args.impl == "reference":
             if rank == 0:

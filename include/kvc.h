@@ -142,7 +142,9 @@ void kvc_destroy(kvc_handle* h);
  *   q   [B, H_q, 1, d_h]   the new query rows (unrotated), storage dtype
  *   k   [B, H_kv, 1, d_h]  the new key rows (unrotated)
  *   v   [B, H_kv, 1, d_h]  the new value rows
- *   out [B, H_q, 1, d_h]   f32 (bf16/f32 storage) or f64 (f64 storage)
+ *   out [B, H_q, 1, d_h]   f32 (bf16/f32 storage) or f64 (f64 storage); with bf16
+ *                          storage and d_h = 128 (the tensor-core decode path) also
+ *                          bf16, each element rounded once from the float32 result
  * For each sequence b with old length n_b and next position p_b (p_b == n_b
  * except after a deliberately stale prefill): q and k are rotated at p_b; the
  * rotated key (rounded once to the storage dtype) and the value are written to
@@ -154,6 +156,9 @@ void kvc_destroy(kvc_handle* h);
  * KVC_ERR_VALUE_SHAPE, KVC_ERR_OUTPUT_SHAPE, KVC_ERR_FULL (some n_b == C),
  * KVC_ERR_POSITION (some p_b >= rope_max_positions), and in checked mode
  * KVC_ERR_NONFINITE_KEY / KVC_ERR_NONFINITE_VALUE.
+ * With KVC_OPT_DEVICE_LENGTHS on, the length and position checks run on the
+ * device instead (see that option) and KVC_ERR_CONFIG is returned when the
+ * cache is not bf16 with d_h = 128 or holds more than 256 sequences.
  */
 kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q,
                              const kvc_tensor* k, const kvc_tensor* v,
@@ -195,7 +200,10 @@ kvc_status kvc_reset(kvc_handle* h, void* stream);
  * [LCP5] listing under "哪些东西必须一起裁剪": for every layer and sequence b,
  * keep rows < cut[b] and set length = next position = cut[b].
  * cut [B] host.  KVC_ERR_CUT (no state change) if some cut[b] < 0 or
- * cut[b] > the current length of sequence b in any layer.
+ * cut[b] > the current length of sequence b in any layer.  With
+ * KVC_OPT_DEVICE_LENGTHS on, the second check runs on the device without a
+ * synchronisation: a cut beyond a length then changes nothing and sets bit 16
+ * of the device error word (kvc_check reports KVC_ERR_DEVICE).
  */
 kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream);
 
@@ -209,9 +217,15 @@ kvc_status kvc_lcp(const int32_t* cached, int64_t n, const int32_t* query, int64
                    int32_t* cut);
 
 /* Host mirrors of one layer's lengths and next positions, each [B] host
- * (either may be NULL). */
+ * (either may be NULL).  After device-length decode steps (KVC_OPT_DEVICE_LENGTHS)
+ * the mirrors lag behind until kvc_sync_lengths, kvc_check, kvc_truncate or
+ * kvc_prefill_suffix reads the device lengths back. */
 kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
                            int32_t* next_positions);
+
+/* Waits for all work on the handle's device, then copies every layer's device
+ * lengths and next positions into the host mirrors.  No other effect. */
+kvc_status kvc_sync_lengths(kvc_handle* h);
 
 /* The handle's configuration (rope_max_positions resolved). */
 kvc_status kvc_get_config(const kvc_handle* h, kvc_config* out);
@@ -267,10 +281,25 @@ typedef enum kvc_option {
     KVC_OPT_DECODE_FUSED = 5,      /* 1 (default) = bf16 decode steps with B <= 256 append, attend and
                                       commit in one launch (plus a merge launch when H_q / H_kv > 16);
                                       0 = separate append, attend, merge and commit kernels */
-    KVC_OPT_TEST_STALL = 6         /* test only, applies to the next bf16 d_h = 128 decode step: its producer
+    KVC_OPT_TEST_STALL = 6,        /* test only, applies to the next bf16 d_h = 128 decode step: its producer
                                       issues no loads, so the consumers' bounded waits give up (about 1 s)
                                       and the step reports a device error through kvc_check; the step's
                                       outputs are undefined and the cache should then be reset */
+    KVC_OPT_DEVICE_LENGTHS = 7     /* 1 = decode steps read the lengths and next positions from device memory
+                                      instead of the host mirrors, so that the launches of a step do not
+                                      depend on them and can be captured in a CUDA graph and replayed:
+                                      kvc_append_attend then enqueues one launch (two with more than 16
+                                      query heads per key/value head), makes no synchronising call and
+                                      no host length check.  The kernel checks every sequence of the layer
+                                      first; if one is full or would rotate beyond the table it changes
+                                      nothing and sets bit 8 of the device error word (kvc_check reports
+                                      KVC_ERR_DEVICE).  The split count is fixed at the call (from the
+                                      lengths last read back) and serves every later length.  Make one
+                                      uncaptured call per layer before capturing, so that the split
+                                      scratch is allocated outside the capture.  kvc_truncate then checks
+                                      its cuts on the device too.  Changing the option, and
+                                      kvc_prefill_suffix and kvc_check while it is on, synchronise the
+                                      device and read the lengths back. */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

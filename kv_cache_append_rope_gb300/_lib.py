@@ -24,13 +24,14 @@ CODE = {v: k for k, v in STATUS.items()}
 DTYPES = {"bf16": 0, "f32": 1, "f64": 2}
 OPT_DECODE_SPLIT_ROWS, OPT_FORCE_GENERIC, OPT_SUFFIX_KERNEL, OPT_TIMING, OPT_DECODE_FUSED = 1, 2, 3, 4, 5
 OPT_TEST_STALL = 6
+OPT_DEVICE_LENGTHS = 7
 KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "generic_attend": 4,
            "bookkeeping": 5}
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
            "kvc_destroy", "kvc_append_attend", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
-           "kvc_lcp", "kvc_get_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
+           "kvc_lcp", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
            "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
 
 
@@ -76,6 +77,7 @@ def _load():
         "kvc_truncate": (ctypes.c_int, [_P, _I32P, _P]),
         "kvc_lcp": (ctypes.c_int, [_I32P, ctypes.c_int64, _I32P, ctypes.c_int64, _I32P]),
         "kvc_get_lengths": (ctypes.c_int, [_P, ctypes.c_int32, _I32P, _I32P]),
+        "kvc_sync_lengths": (ctypes.c_int, [_P]),
         "kvc_get_config": (ctypes.c_int, [_P, ctypes.POINTER(kvc_config)]),
         "kvc_storage": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_P), ctypes.POINTER(_P),
                                        ctypes.POINTER(_P)]),

@@ -217,6 +217,7 @@ void free_all(kvc_handle* h) {
     cudaFree(h->qrot_chunk);
     cudaFree(h->work_counter);
     cudaFree(h->lane_ticket);
+    cudaFree(h->step_ticket);
     h->ring.destroy();
     for (auto& t : h->timers) {
         for (auto e : t.start) cudaEventDestroy(e);
@@ -403,7 +404,8 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
               alloc((void**)&h->nonfinite_d, 2 * sizeof(unsigned long long)) &&
               alloc(&h->qrot, (size_t)c.batch * c.heads_q * c.head_dim * acc) &&
               alloc((void**)&h->work_counter, 64) &&
-              alloc((void**)&h->lane_ticket, (size_t)c.batch * c.heads_kv * sizeof(unsigned));
+              alloc((void**)&h->lane_ticket, (size_t)c.batch * c.heads_kv * sizeof(unsigned)) &&
+              alloc((void**)&h->step_ticket, (size_t)c.layers * sizeof(unsigned));
     if (ok && c.rope_base > 0.0)
         ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2)) &&
              alloc((void**)&h->rope_f, (size_t)maxpos * (c.head_dim / 2) * sizeof(float2));
@@ -425,6 +427,8 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
     if ((e = cudaMemset(h->next_d, 0, LB * sizeof(int32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
     if ((e = cudaMemset(h->err_d, 0, sizeof(uint32_t))) != cudaSuccess) return abort_cuda(e, "cudaMemset");
     if ((e = cudaMemset(h->lane_ticket, 0, (size_t)c.batch * c.heads_kv * sizeof(unsigned))) != cudaSuccess)
+        return abort_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(h->step_ticket, 0, (size_t)c.layers * sizeof(unsigned))) != cudaSuccess)
         return abort_cuda(e, "cudaMemset");
     if ((e = cudaHostAlloc((void**)&h->nonfinite_h, 2 * sizeof(unsigned long long), cudaHostAllocDefault)) !=
         cudaSuccess)
@@ -487,6 +491,21 @@ static kvc_status check_layer(kvc_handle* h, int32_t layer) {
     return KVC_OK;
 }
 
+// After device-length decode steps (and in that mode at any time, since a
+// captured graph may have replayed steps without a host call) the device
+// lengths are authoritative: wait for every enqueued step and read them back
+// into the host mirrors.
+static kvc_status refresh_mirrors(kvc_handle* h) {
+    if (!h->mirrors_stale && !h->opt_device_lengths) return KVC_OK;
+    const size_t n = (size_t)h->cfg.layers * h->B();
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    KVC_CUDA(h, cudaDeviceSynchronize());
+    KVC_CUDA(h, cudaMemcpy(h->len_h.data(), h->len_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    KVC_CUDA(h, cudaMemcpy(h->next_h.data(), h->next_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    h->mirrors_stale = false;
+    return KVC_OK;
+}
+
 static kvc_status ensure_partials(kvc_handle* h, size_t splits) {
     if (h->part_splits >= splits) return KVC_OK;
     cudaDeviceSynchronize();
@@ -545,13 +564,28 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
     if ((st = check_tensor(h, q, "query", KVC_ERR_QUERY_SHAPE, dt, B, Hq, 1, D)) != KVC_OK) return st;
     if ((st = check_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, 1, D)) != KVC_OK) return st;
     if ((st = check_tensor(h, v, "value", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, 1, D)) != KVC_OK) return st;
-    if ((st = check_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_dtype(dt), B, Hq, 1, D)) != KVC_OK)
+    const bool fast = fast_decode_ok(h);
+    // bf16 storage on the tensor-core decode path may also return bf16 outputs
+    const bool out_bf16 = out && out->dtype == KVC_BF16 && dt == KVC_BF16 && fast;
+    if ((st = check_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_bf16 ? KVC_BF16 : out_dtype(dt), B, Hq, 1,
+                           D)) != KVC_OK)
         return st;
+    const bool dev_len = h->opt_device_lengths != 0;
+    if (dev_len && !(fast && h->opt_decode_fused && B <= kFusedMaxB))
+        return fail(h, KVC_ERR_CONFIG,
+                    "device-length decode steps need bf16 storage, d_h = 128, the fused step and at most %d sequences",
+                    kFusedMaxB);
+    if (!dev_len && (st = refresh_mirrors(h)) != KVC_OK) return st;
     int32_t* lenh = &h->len_h[(size_t)layer * B];
     int32_t* nexth = &h->next_h[(size_t)layer * B];
     int max_t = 0;
     int64_t total_keys = 0;
-    for (int b = 0; b < B; ++b) {
+    for (int b = 0; b < B && dev_len; ++b) {
+        // the kernel checks the device lengths; the mirrors only size the splits
+        max_t = std::max(max_t, std::min(lenh[b], C - 1) + 1);
+        total_keys += std::min(lenh[b], C - 1) + 1;
+    }
+    for (int b = 0; b < B && !dev_len; ++b) {
         if (lenh[b] >= C)
             return fail(h, KVC_ERR_FULL, "sequence %d of layer %d already holds %d rows, the capacity", b, layer, C);
         if (h->rope && nexth[b] >= h->max_positions)
@@ -565,7 +599,6 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
     if (h->cfg.checked) {
         if ((st = check_nonfinite(h, k, v, (int64_t)B * Hkv * D, (int64_t)B * Hkv * D, s)) != KVC_OK) return st;
     }
-    const bool fast = fast_decode_ok(h);
     AppendLaunch ap{};
     ap.q = q->data; ap.k = k->data; ap.v = v->data;
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
@@ -592,6 +625,19 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
             split_rows = (int)r;
         }
         max_splits = (max_t + split_rows - 1) / split_rows;
+        if (dev_len) {
+            // A device-length step keeps its grid for every later length (a captured
+            // graph replays it) and each sequence takes max_splits splits of its own
+            // size: as many as the mean length needs at the rows per split chosen
+            // above, but as many as fit in one wave of CTAs and at most one per 64 rows.
+            const int64_t lanes = (int64_t)B * Hkv;
+            const int64_t mean_t = (total_keys + B - 1) / B;
+            int64_t ns = (mean_t + split_rows - 1) / split_rows;
+            // (whole CTAs per lane: rounding the fill up would leave a short second wave)
+            const int64_t fill = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(Hq / Hkv) / lanes;
+            ns = std::min<int64_t>(std::max<int64_t>(ns, fill), (C + 63) / 64);
+            max_splits = (int)std::max<int64_t>(ns, 1);
+        }
         if (max_splits > 1 && (st = ensure_partials(h, max_splits)) != KVC_OK) return st;
     }
 
@@ -601,9 +647,13 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
     if (fast && h->opt_decode_fused && B <= kFusedMaxB) {
         DecodeLaunch dl{};
         dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
-        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
+        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
+        dl.out_bf16 = out_bf16;
         dl.fused = 1;
+        dl.dev_len = dev_len;
+        dl.step_ticket = h->step_ticket + layer;
+        dl.max_positions = h->max_positions;
         dl.q_in = (const __nv_bfloat16*)q->data; dl.k_in = (const __nv_bfloat16*)k->data;
         dl.v_in = (const __nv_bfloat16*)v->data;
         dl.K = (__nv_bfloat16*)h->K_layer(layer); dl.V = (__nv_bfloat16*)h->V_layer(layer);
@@ -613,13 +663,17 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         dl.merge_in_kernel = Hq / Hkv <= 16;
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
-        for (int b = 0; b < B; ++b) {
+        for (int b = 0; b < B && !dev_len; ++b) {
             dl.old_len[b] = lenh[b];
             dl.pos[b] = nexth[b];
         }
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
         if (!dl.merge_in_kernel && max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
+        if (dev_len) {
+            h->mirrors_stale = true;
+            return KVC_OK;
+        }
         for (int b = 0; b < B; ++b) {
             lenh[b] += 1;
             nexth[b] += 1;
@@ -631,8 +685,9 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         DecodeLaunch dl{};
         dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
         dl.qrot = (const float*)h->qrot; dl.len = h->len_layer(layer);
-        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = (float*)out->data; dl.err = h->err_d;
+        dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
+        dl.out_bf16 = out_bf16;
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
@@ -674,6 +729,7 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     if ((st = check_tensor(h, v, "value", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, S, D)) != KVC_OK) return st;
     if (out && (st = check_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_dtype(dt), B, Hq, S, D)) != KVC_OK)
         return st;
+    if ((st = refresh_mirrors(h)) != KVC_OK) return st;
     int32_t* lenh = &h->len_h[(size_t)layer * B];
     int32_t* nexth = &h->next_h[(size_t)layer * B];
     std::vector<int32_t> st_h(B), sl_h(B);
@@ -800,6 +856,7 @@ kvc_status kvc_reset(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemsetAsync(h->lane_ticket, 0, (size_t)h->B() * h->Hkv() * sizeof(unsigned), s));
     std::fill(h->len_h.begin(), h->len_h.end(), 0);
     std::fill(h->next_h.begin(), h->next_h.end(), 0);
+    h->mirrors_stale = false;
     return KVC_OK;
 }
 
@@ -807,9 +864,11 @@ kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream) {
     if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
     if (!cut) return fail(h, KVC_ERR_NULL, "cut array is NULL");
     const int B = h->B(), L = h->cfg.layers;
+    // With device lengths the kernel checks cut <= length itself (no synchronisation).
+    const bool dev_len = h->opt_device_lengths != 0;
     for (int b = 0; b < B; ++b) {
         if (cut[b] < 0) return fail(h, KVC_ERR_CUT, "cut %d of sequence %d is negative", cut[b], b);
-        for (int l = 0; l < L; ++l)
+        for (int l = 0; l < L && !dev_len; ++l)
             if (cut[b] > h->len_h[(size_t)l * B + b])
                 return fail(h, KVC_ERR_CUT, "cut %d of sequence %d exceeds its length %d in layer %d", cut[b], b,
                             h->len_h[(size_t)l * B + b], l);
@@ -821,7 +880,10 @@ kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream) {
     memcpy(hp, cut, B * sizeof(int32_t));
     void* dp;
     KVC_CUDA(h, h->ring.upload(B * sizeof(int32_t), s, &dp));
-    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_truncate(h->len_d, h->next_d, (const int32_t*)dp, L, B, s); }));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
+        return dev_len ? launch_truncate_checked(h->len_d, h->next_d, (const int32_t*)dp, L, B, h->err_d, s)
+                       : launch_truncate(h->len_d, h->next_d, (const int32_t*)dp, L, B, s);
+    }));
     KVC_CUDA(h, h->ring.release(s));
     for (int l = 0; l < L; ++l)
         for (int b = 0; b < B; ++b) {
@@ -853,6 +915,11 @@ kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
     return KVC_OK;
 }
 
+kvc_status kvc_sync_lengths(kvc_handle* h) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    return refresh_mirrors(h);
+}
+
 kvc_status kvc_get_config(const kvc_handle* h, kvc_config* out) {
     if (!h || !out) return KVC_ERR_NULL;
     *out = h->cfg;
@@ -880,8 +947,16 @@ kvc_status kvc_check(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemcpy(next.data(), h->next_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
     KVC_CUDA(h, cudaMemcpy(&err, h->err_d, sizeof(uint32_t), cudaMemcpyDeviceToHost));
     if (err)
-        return fail(h, KVC_ERR_DEVICE, "device error word 0x%x (1: slot out of range, 2: bounded wait timed out, 4: tensor memory)",
+        return fail(h, KVC_ERR_DEVICE,
+                    "device error word 0x%x (1: slot out of range, 2: bounded wait timed out, 4: tensor memory, "
+                    "8: cache full or position beyond the table in a device-length step, "
+                    "16: cut beyond a length in a device-checked truncate)",
                     err);
+    if (h->mirrors_stale || h->opt_device_lengths) {
+        h->len_h = len;
+        h->next_h = next;
+        h->mirrors_stale = false;
+    }
     for (size_t i = 0; i < n; ++i)
         if (len[i] != h->len_h[i] || next[i] != h->next_h[i])
             return fail(h, KVC_ERR_DEVICE, "device length/next position (%d, %d) of entry %zu differ from the host (%d, %d)",
@@ -914,6 +989,12 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
         case KVC_OPT_TEST_STALL:
             h->opt_test_stall = value != 0;
             return KVC_OK;
+        case KVC_OPT_DEVICE_LENGTHS: {
+            kvc_status st = refresh_mirrors(h);
+            if (st != KVC_OK) return st;
+            h->opt_device_lengths = value != 0;
+            return KVC_OK;
+        }
     }
     return fail(h, KVC_ERR_CONFIG, "unknown option %d", option);
 }

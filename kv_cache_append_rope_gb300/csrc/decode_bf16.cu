@@ -65,35 +65,85 @@ __device__ __forceinline__ float2 fused_q_pair(const DecodeLaunch& a, int b, int
     return make_float2(fmaf(x, cs.x, -(y * cs.y)), fmaf(y, cs.x, x * cs.y));
 }
 
-template <int MT, bool FUSED>
+// Final output element: float32, or rounded to bf16 when the caller asked for bf16 output.
+__device__ __forceinline__ void store_out(const DecodeLaunch& a, int64_t i, float x) {
+    if (a.out_bf16)
+        ((__nv_bfloat16*)a.out)[i] = __float2bfloat16_rn(x);
+    else
+        ((float*)a.out)[i] = x;
+}
+
+// MODE 0: separate-kernel step; 1: fused step, lengths from the host mirrors;
+// 2: fused step, lengths from device memory.
+template <int MT, int MODE>
 __global__ void __launch_bounds__(THREADS, Cfg<MT>::MINB)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ DecodeLaunch a) {
     constexpr int STAGES = Cfg<MT>::STAGES;
+    constexpr bool FUSED = MODE >= 1;
     const int split = blockIdx.x;
     const int lane_kv = blockIdx.y;
     const int b = lane_kv / a.Hkv;
     const int hkv = lane_kv - b * a.Hkv;
-    // Fused step: the old length and position come from the host mirrors, so no
-    // kernel of the step reads the length this kernel commits.
-    const int old_len = FUSED ? a.old_len[b] : a.len[b];
-    const int t = old_len + 1;
-    if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0) {
-        a.len_out[b] = old_len + 1;
-        a.next_out[b] = a.pos[b] + 1;
-    }
-    const int r0 = split * a.split_rows;
-    if (r0 >= t) return;
-    const int r1 = min(t, r0 + a.split_rows);
-    const int ntiles = (r1 - r0 + KT - 1) / KT;
-    const int G = a.Hq / a.Hkv;
-    const int nsplit_lane = (t + a.split_rows - 1) / a.split_rows;
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
     volatile int* s_err = (volatile int*)(empty + STAGES);   // s_err[1]: last-CTA flag
+
+    // Fused step: the old length and position come from the host mirrors, so no
+    // kernel of the step reads the length this kernel commits.
+    int old_len, pos, split_rows = a.split_rows;
+    if constexpr (MODE == 2) {
+        // Device-length step (the launch parameters do not depend on the lengths,
+        // so it can be captured in a CUDA graph and replayed): every CTA reads its
+        // sequence's length and position, and checks every sequence, from device
+        // memory, then takes a ticket; the last CTA of the grid to do so -- all the
+        // others have read by then -- commits every sequence.  A step in which
+        // some sequence is full or would rotate beyond the table is rejected
+        // whole, as the host checks reject it in the other modes.
+        old_len = __ldcg(a.len_out + b);
+        pos = __ldcg(a.next_out + b);
+        int bad = 0;
+        for (int i = threadIdx.x; i < a.B; i += THREADS) {
+            const int L = __ldcg(a.len_out + i), P = __ldcg(a.next_out + i);
+            bad |= (L < 0) | (L >= a.C) | (P < 0) | (a.rope_f != nullptr && P >= a.max_positions);
+        }
+        const bool reject = __syncthreads_or(bad) != 0;
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(a.step_ticket, 1u);
+            s_err[1] = prev == gridDim.x * gridDim.y - 1;
+        }
+        __syncthreads();
+        if (s_err[1]) {
+            for (int i = threadIdx.x; i < a.B && !reject; i += THREADS) {
+                a.len_out[i] = __ldcg(a.len_out + i) + 1;
+                a.next_out[i] = __ldcg(a.next_out + i) + 1;
+            }
+            if (threadIdx.x == 0) {
+                *a.step_ticket = 0;
+                if (reject) atomicOr(a.err, (uint32_t)DEV_ERR_FULL);
+            }
+        }
+        if (reject) return;
+        // every sequence takes max_splits splits, sized from its own length
+        const int tt = old_len + 1;
+        split_rows = ((tt + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
+    } else {
+        old_len = FUSED ? a.old_len[b] : a.len[b];
+        pos = FUSED ? a.pos[b] : 0;
+        if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0) {
+            a.len_out[b] = old_len + 1;
+            a.next_out[b] = pos + 1;
+        }
+    }
+    const int t = old_len + 1;
+    const int r0 = split * split_rows;
+    if (r0 >= t) return;
+    const int r1 = min(t, r0 + split_rows);
+    const int ntiles = (r1 - r0 + KT - 1) / KT;
+    const int G = a.Hq / a.Hkv;
+    const int nsplit_lane = (t + split_rows - 1) / split_rows;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -117,7 +167,6 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             // The new row (slot old_len) belongs to this split: rotate and store the
             // key (bit-exact bf16 rounding), store the value and the position, then
             // order these generic-proxy writes before this warp's TMA reads of them.
-            const int pos = a.pos[b];
             const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
             const int64_t dst = (((int64_t)b * a.Hkv + hkv) * a.C + old_len) * D + lane * 4;
             const uint2 kraw = *(const uint2*)(a.k_in + src);
@@ -186,7 +235,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const int ra = mtw * 16 + qa, rb = ra + 8;
             const float* qra = a.qrot + ((int64_t)b * a.Hq + hkv * G + ra) * D;
             const float* qrb = a.qrot + ((int64_t)b * a.Hq + hkv * G + rb) * D;
-            const int qpos = FUSED ? a.pos[b] : 0;
+            const int qpos = pos;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int c = ks * 16 + qc;
@@ -355,7 +404,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         const int64_t qh = (int64_t)b * a.Hq + hkv * G + g;
         if (nsplit_lane == 1) {
-            a.out[qh * D + dim] = O / L;
+            store_out(a, qh * D + dim, O / L);
         } else {
             const int64_t idx = qh * a.max_splits + split;
             a.part_o[idx * D + dim] = O;
@@ -390,7 +439,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             L += v.y * f;
             O += __ldcg(po + (int64_t)sp * D) * f;
         }
-        a.out[qh * D + dim] = O / L;
+        store_out(a, qh * D + dim, O / L);
     }
     if (threadIdx.x == 0) a.lane_ticket[lane_kv] = 0;
 }
@@ -398,8 +447,16 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     const int qh = blockIdx.x;
     const int b = qh / a.Hq;
-    const int t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
-    const int ns = (t + a.split_rows - 1) / a.split_rows;
+    int t, rows = a.split_rows;
+    if (a.dev_len) {
+        // after the step's commit (after a rejected step the output is undefined)
+        t = __ldcg(a.len_out + b);
+        rows = ((t + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
+        if (t <= 0) return;
+    } else {
+        t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
+    }
+    const int ns = (t + rows - 1) / rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
     float M = -INFINITY;
@@ -411,21 +468,21 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
         L += ml[s].y * f;
         O += po[(int64_t)s * D] * f;
     }
-    a.out[(int64_t)qh * D + threadIdx.x] = O / L;
+    store_out(a, (int64_t)qh * D + threadIdx.x, O / L);
 }
 
-template <int MT, bool FUSED>
+template <int MT, int MODE>
 cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<Cfg<MT>::STAGES>();
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
-            cudaFuncSetAttribute(decode_bf16_kernel<MT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+            cudaFuncSetAttribute(decode_bf16_kernel<MT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(a.max_splits, a.B * a.Hkv);
-    decode_bf16_kernel<MT, FUSED><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
+    decode_bf16_kernel<MT, MODE><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
     return cudaGetLastError();
 }
 
@@ -441,8 +498,9 @@ int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;
     if (a.fused && a.B > kFusedMaxB) return cudaErrorInvalidValue;
-    if (G <= 16) return a.fused ? launch_mt<1, true>(a, s) : launch_mt<1, false>(a, s);
-    if (G <= 32) return a.fused ? launch_mt<2, true>(a, s) : launch_mt<2, false>(a, s);
+    const int mode = a.fused ? (a.dev_len ? 2 : 1) : 0;
+    if (G <= 16) return mode == 2 ? launch_mt<1, 2>(a, s) : mode == 1 ? launch_mt<1, 1>(a, s) : launch_mt<1, 0>(a, s);
+    if (G <= 32) return mode == 2 ? launch_mt<2, 2>(a, s) : mode == 1 ? launch_mt<2, 1>(a, s) : launch_mt<2, 0>(a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -11,7 +11,10 @@ namespace kvc {
 enum DeviceError : uint32_t {
     DEV_ERR_SLOT = 1u,        // an append slot or position fell outside its buffer
     DEV_ERR_WAIT_TIMEOUT = 2u,// a bounded mbarrier wait gave up
-    DEV_ERR_TMEM = 4u         // tensor-memory allocation returned an unusable address
+    DEV_ERR_TMEM = 4u,        // tensor-memory allocation returned an unusable address
+    DEV_ERR_FULL = 8u,        // a device-length decode step met a full sequence or a position
+                              // beyond the RoPE table and was rejected as a whole
+    DEV_ERR_CUT = 16u         // a device-checked truncate met a cut beyond a length
 };
 
 // ---- storage dtype traits ------------------------------------------------

@@ -64,6 +64,7 @@ struct Handle {
     size_t qrot_chunk_bytes = 0;
     int* work_counter = nullptr;   // dynamic tile scheduler counter
     unsigned* lane_ticket = nullptr;  // [B*H_kv] split counters of the fused decode step
+    unsigned* step_ticket = nullptr;  // [L] CTA counters of device-length decode steps
 
     // TMA descriptors over each layer's keys and values (bf16, d_h = 128):
     // 64-row boxes for decode, 128-row boxes for the suffix-chunk kernel
@@ -88,6 +89,8 @@ struct Handle {
     int64_t opt_suffix_kernel = 0;
     int64_t opt_decode_fused = 1;
     int64_t opt_test_stall = 0;
+    int64_t opt_device_lengths = 0;
+    bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 
     int B() const { return cfg.batch; }
     int Hq() const { return cfg.heads_q; }
@@ -135,9 +138,10 @@ struct DecodeLaunch {
     const float* qrot;       // [B,H_q,128] rotated queries (separate-kernel step)
     const int32_t* len;      // [B] old length: t = len + 1 (separate-kernel step)
     float* part_o; float2* part_ml;
-    float* out;              // [B,H_q,128]
+    void* out;               // [B,H_q,128] float, or bf16 when out_bf16
     uint32_t* err;
     int B, Hq, Hkv, C, split_rows, max_splits;
+    int out_bf16;
     // Fused step (append + attend + split merge + length commit in one launch).
     int fused;
     const __nv_bfloat16* q_in;           // [B,H_q,128] new queries, unrotated
@@ -150,6 +154,13 @@ struct DecodeLaunch {
     unsigned* lane_ticket;               // [B*H_kv] split counters, zero between launches
     int merge_in_kernel;                 // 1: the last CTA of a lane merges its splits
     int test_stall;                      // test only: the producer issues no loads (waits run out)
+    // Device-length step: old lengths and positions are read from len_out /
+    // next_out instead of old_len / pos, every sequence uses max_splits splits
+    // (rows per split from its own length), and the grid's last CTA to read
+    // the lengths commits them.
+    int dev_len;
+    unsigned* step_ticket;               // zero between launches
+    int max_positions;
     int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
     int32_t pos[kFusedMaxB];
 };
@@ -161,6 +172,8 @@ cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, cons
                           int uniform_rows, int B, cudaStream_t s);
 cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                             cudaStream_t s);
+cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
+                                    uint32_t* err, cudaStream_t s);
 cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,
                              cudaStream_t s);
 

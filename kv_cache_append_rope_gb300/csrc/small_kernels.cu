@@ -46,6 +46,31 @@ cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int
     return cudaGetLastError();
 }
 
+// The same, with the host-side check moved to the device (lengths kept on the
+// device): one block first checks every layer's length against the cut and
+// changes nothing -- setting an error bit instead -- if some cut exceeds one.
+__global__ void truncate_checked_kernel(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
+                                        uint32_t* err) {
+    const int n = layers * B;
+    int bad = 0;
+    for (int u = threadIdx.x; u < n; u += blockDim.x) bad |= cut[u % B] > len[u];
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) atomicOr(err, (uint32_t)DEV_ERR_CUT);
+        return;
+    }
+    for (int u = threadIdx.x; u < n; u += blockDim.x) {
+        const int c = cut[u % B];
+        len[u] = c;
+        next[u] = c;
+    }
+}
+
+cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
+                                    uint32_t* err, cudaStream_t s) {
+    truncate_checked_kernel<<<1, 1024, 0, s>>>(len, next, cut, layers, B, err);
+    return cudaGetLastError();
+}
+
 template <typename T>
 __global__ void nonfinite_kernel(const T* x, int64_t n, unsigned long long* first) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;

@@ -139,6 +139,10 @@ class KVCache:
         self._check(L.lib.kvc_get_lengths(self._h, layer, ln, nx))
         return list(ln), list(nx)
 
+    def sync_lengths(self):
+        """kvc_sync_lengths: read the device lengths back into the host mirrors."""
+        self._check(L.lib.kvc_sync_lengths(self._h))
+
     def storage(self, layer=0):
         """Views of one layer's device storage: keys, values [B, H_kv, C, d_h], positions [B, C]."""
         k, v, p = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()

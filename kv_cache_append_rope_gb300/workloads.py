@@ -10,6 +10,9 @@ Configurations (sizes as the workloads are stated):
 * prefix_reuse 2-layer single-head decoder, d = 16, vocab 32, f64, seeds 7/11/23
 * mha_decode   B = 32, H = 32, d_h = 128, bf16, C = 8192, old lengths uniform in
                [1, 8191] (capped so 64 steps fit), 64 decode steps
+* mha_decode_short  B = 128, H = 32, d_h = 128, bf16, C = 1024, old lengths uniform
+               in [1, 256], 64 steps: short decode steps (~0.27 GB of K/V, ~40 us),
+               where the gaps between launches are a visible share
 * gqa_decode   B = 64, H_q = 32, H_kv = 8 or 1, d_h = 128, bf16, C = 32768,
                lengths uniform in [16384, 32767] (capped so 32 steps fit), 32 steps
 * suffix       B = 8, H = 32, d_h = 128, bf16, cached prefix 16384 tokens with
@@ -20,6 +23,7 @@ import torch
 
 CONFIGS = {
     "mha_decode": dict(B=32, Hq=32, Hkv=32, D=128, C=8192, lo=1, hi=8191, steps=64, seed=3),
+    "mha_decode_short": dict(B=128, Hq=32, Hkv=32, D=128, C=1024, lo=1, hi=256, steps=64, seed=3),
     "gqa_decode": dict(B=64, Hq=32, Hkv=8, D=128, C=32768, lo=16384, hi=32767, steps=32, seed=4),
     "mqa_decode": dict(B=64, Hq=32, Hkv=1, D=128, C=32768, lo=16384, hi=32767, steps=32, seed=4),
     "suffix": dict(B=8, Hq=32, Hkv=32, D=128, prefix=16384, appended=512, vocab=32000, seed=5),
