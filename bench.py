@@ -50,8 +50,8 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # Summaries: profiles/decode_bf16_mha_small_full.md,
 # profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
 TRAFFIC = {
-    "mha_decode": ("ratio", (503474944.0 + 4777728.0) / 499236864.0),
-    "mqa_decode": ("ratio", (217880832.0 + 4119296.0) / 217403392.0),
+    "mha_decode": ("ratio", (503465472.0 + 4657152.0) / 499236864.0),
+    "mqa_decode": ("ratio", (217849856.0 + 4154880.0) / 217403392.0),
     "suffix": ("per_sequence", 375259136.0 + 169486080.0),
 }
 

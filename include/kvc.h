@@ -66,7 +66,8 @@ typedef enum kvc_status {
     KVC_ERR_POSITION = 18,                  /* a RoPE position outside [0, max_positions) */
     KVC_ERR_CONFIG = 19,                    /* invalid geometry or option */
     KVC_ERR_CUDA = 20,                      /* a CUDA runtime call failed (no device, ...) */
-    KVC_ERR_DEVICE = 21                     /* a kernel reported a fault or a timed-out wait */
+    KVC_ERR_DEVICE = 21,                    /* a kernel reported a fault or a timed-out wait */
+    KVC_ERR_TICKET = 22                     /* a prepared-step ticket no longer matches its cache */
 } kvc_status;
 
 typedef enum kvc_dtype {
@@ -100,6 +101,15 @@ typedef struct kvc_tensor {
     int32_t ndim;
     int64_t shape[4];
 } kvc_tensor;
+
+/* A prepared decode step of one layer (kvc_prepare_attend), committed by
+ * kvc_commit.  Plain data owned by the caller; only the library writes it. */
+typedef struct kvc_ticket {
+    const void* handle;   /* the handle that prepared it */
+    int32_t layer;
+    int32_t reserved;
+    uint64_t version;     /* the layer's state version when it was prepared */
+} kvc_ticket;
 
 typedef struct kvc_handle kvc_handle;
 
@@ -163,6 +173,37 @@ void kvc_destroy(kvc_handle* h);
 kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q,
                              const kvc_tensor* k, const kvc_tensor* v,
                              const kvc_tensor* out, void* stream);
+
+/*
+ * The same step without its commit ([Ch37] listing "Evaluate one newest query
+ * across the retained rows plus the candidate key/value row before committing
+ * the append": the prepared result carries its candidate rows and the length it
+ * expects; chapter 38, as that listing's comment announces, prepares one such
+ * ticket per decoder block, finishes the model, checks that every ticket still
+ * targets its cache and only then commits the whole stack).  Arguments,
+ * checks and errors as kvc_append_attend; `out` receives the attention output
+ * over the retained rows plus the candidate row.  The rotated key and the value
+ * are staged in slot n_b -- beyond the logical length, so no call sees them --
+ * and the length and next position stay unchanged until kvc_commit.
+ * *ticket (caller-owned) records the layer and its state version.  Any later
+ * change of the layer (an append, prepare, prefill, truncate, reset or commit
+ * of it) makes the ticket stale.  Not available with KVC_OPT_DEVICE_LENGTHS
+ * (KVC_ERR_CONFIG).
+ */
+kvc_status kvc_prepare_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q,
+                              const kvc_tensor* k, const kvc_tensor* v,
+                              const kvc_tensor* out, kvc_ticket* ticket, void* stream);
+
+/*
+ * Commits n prepared steps at once: every ticket must come from `h`, name a
+ * distinct layer and still match that layer's state version; then every
+ * named layer's lengths and next positions advance by one, all in one
+ * enqueued launch.  KVC_ERR_TICKET (nothing committed) when a ticket is
+ * stale, foreign or repeats a layer; KVC_ERR_NULL for a NULL array with n > 0.
+ * n == 0 commits nothing.  Dropping a ticket discards its step (the staged
+ * rows stay beyond the length).
+ */
+kvc_status kvc_commit(kvc_handle* h, const kvc_ticket* tickets, int32_t n, void* stream);
 
 /*
  * Append a chunk of rows per sequence and attend it causally against the

@@ -17,7 +17,7 @@ STATUS = {
     7: "KVC_ERR_FULL", 8: "KVC_ERR_KEY_SHAPE", 9: "KVC_ERR_VALUE_SHAPE", 10: "KVC_ERR_QUERY_SHAPE",
     11: "KVC_ERR_OUTPUT_SHAPE", 12: "KVC_ERR_DTYPE", 13: "KVC_ERR_LAYER", 14: "KVC_ERR_NONFINITE_KEY",
     15: "KVC_ERR_NONFINITE_VALUE", 16: "KVC_ERR_CUT", 17: "KVC_ERR_EMPTY_QUERY", 18: "KVC_ERR_POSITION",
-    19: "KVC_ERR_CONFIG", 20: "KVC_ERR_CUDA", 21: "KVC_ERR_DEVICE",
+    19: "KVC_ERR_CONFIG", 20: "KVC_ERR_CUDA", 21: "KVC_ERR_DEVICE", 22: "KVC_ERR_TICKET",
 }
 CODE = {v: k for k, v in STATUS.items()}
 
@@ -30,7 +30,7 @@ KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "gen
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
-           "kvc_destroy", "kvc_append_attend", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
+           "kvc_destroy", "kvc_append_attend", "kvc_prepare_attend", "kvc_commit", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
            "kvc_lcp", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
            "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
 
@@ -54,6 +54,11 @@ class kvc_tensor(ctypes.Structure):
                 ("shape", ctypes.c_int64 * 4)]
 
 
+class kvc_ticket(ctypes.Structure):
+    _fields_ = [("handle", ctypes.c_void_p), ("layer", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("version", ctypes.c_uint64)]
+
+
 _P = ctypes.c_void_p
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _TP = ctypes.POINTER(kvc_tensor)
@@ -72,6 +77,9 @@ def _load():
         "kvc_create_ex": (ctypes.c_int, [ctypes.POINTER(kvc_config), ctypes.POINTER(_P)]),
         "kvc_destroy": (None, [_P]),
         "kvc_append_attend": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _TP, _TP, _P]),
+        "kvc_prepare_attend": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _TP, _TP,
+                                              ctypes.POINTER(kvc_ticket), _P]),
+        "kvc_commit": (ctypes.c_int, [_P, ctypes.POINTER(kvc_ticket), ctypes.c_int32, _P]),
         "kvc_prefill_suffix": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _TP, _I32P, _I32P, _TP, _P]),
         "kvc_reset": (ctypes.c_int, [_P, _P]),
         "kvc_truncate": (ctypes.c_int, [_P, _I32P, _P]),

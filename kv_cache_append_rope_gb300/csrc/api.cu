@@ -321,6 +321,7 @@ const char* kvc_status_string(kvc_status s) {
         case KVC_ERR_CONFIG: return "invalid configuration";
         case KVC_ERR_CUDA: return "CUDA error";
         case KVC_ERR_DEVICE: return "device-side error";
+        case KVC_ERR_TICKET: return "stale or foreign ticket";
     }
     return "unknown status";
 }
@@ -473,6 +474,7 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
     }
     h->len_h.assign(LB, 0);
     h->next_h.assign(LB, 0);
+    h->layer_version.assign(c.layers, 0);
     *out = h;
     return KVC_OK;
 }
@@ -551,11 +553,20 @@ static kvc_status check_nonfinite(kvc_handle* h, const kvc_tensor* k, const kvc_
     return KVC_OK;
 }
 
-kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
-                             const kvc_tensor* v, const kvc_tensor* out, void* stream) {
+}  // extern "C"
+
+namespace kvc {
+namespace {
+
+// One decode step of one layer; `commit` false prepares it (kvc_prepare_attend):
+// the candidate rows are staged in slot n_b and the lengths are left unchanged.
+kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                              const kvc_tensor* v, const kvc_tensor* out, bool commit, void* stream) {
     if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
     kvc_status st;
     if ((st = check_layer(h, layer)) != KVC_OK) return st;
+    if (!commit && h->opt_device_lengths)
+        return fail(h, KVC_ERR_CONFIG, "prepared steps need the host length mirrors (device-length mode is on)");
     const int B = h->B(), Hq = h->Hq(), Hkv = h->Hkv(), D = h->D(), C = h->C();
     const int dt = h->cfg.dtype;
     if (q && q->ndim == 4 && q->shape[2] != 1)
@@ -661,6 +672,7 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         dl.len_out = h->len_layer(layer); dl.next_out = h->next_layer(layer);
         dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
         dl.merge_in_kernel = Hq / Hkv <= 16;
+        dl.no_commit = !commit;
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         for (int b = 0; b < B && !dev_len; ++b) {
@@ -670,11 +682,12 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
         if (!dl.merge_in_kernel && max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
+        h->layer_version[layer] += 1;
         if (dev_len) {
             h->mirrors_stale = true;
             return KVC_OK;
         }
-        for (int b = 0; b < B; ++b) {
+        for (int b = 0; b < B && commit; ++b) {
             lenh[b] += 1;
             nexth[b] += 1;
         }
@@ -700,12 +713,73 @@ kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, 
         g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D;
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
+    h->layer_version[layer] += 1;
+    if (!commit) return KVC_OK;
     KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
         return launch_commit(h->len_layer(layer), h->next_layer(layer), h->next_layer(layer), nullptr, 1, B, s);
     }));
     for (int b = 0; b < B; ++b) {
         lenh[b] += 1;
         nexth[b] += 1;
+    }
+    return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                             const kvc_tensor* v, const kvc_tensor* out, void* stream) {
+    return append_attend_impl(h, layer, q, k, v, out, true, stream);
+}
+
+kvc_status kvc_prepare_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                              const kvc_tensor* v, const kvc_tensor* out, kvc_ticket* ticket, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (!ticket) return fail(h, KVC_ERR_NULL, "ticket pointer is NULL");
+    kvc_status st = append_attend_impl(h, layer, q, k, v, out, false, stream);
+    if (st != KVC_OK) return st;
+    ticket->handle = h;
+    ticket->layer = layer;
+    ticket->reserved = 0;
+    ticket->version = h->layer_version[layer];
+    return KVC_OK;
+}
+
+kvc_status kvc_commit(kvc_handle* h, const kvc_ticket* tickets, int32_t n, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (n < 0) return fail(h, KVC_ERR_TICKET, "ticket count %d is negative", n);
+    if (n > 0 && !tickets) return fail(h, KVC_ERR_NULL, "ticket array is NULL");
+    const int L = h->cfg.layers, B = h->B();
+    std::vector<char> seen(L, 0);
+    for (int i = 0; i < n; ++i) {
+        const kvc_ticket& t = tickets[i];
+        if (t.handle != h) return fail(h, KVC_ERR_TICKET, "ticket %d was prepared by another cache", i);
+        if (t.layer < 0 || t.layer >= L) return fail(h, KVC_ERR_TICKET, "ticket %d names layer %d", i, t.layer);
+        if (seen[t.layer]) return fail(h, KVC_ERR_TICKET, "tickets repeat layer %d", t.layer);
+        seen[t.layer] = 1;
+        if (t.version != h->layer_version[t.layer])
+            return fail(h, KVC_ERR_TICKET, "ticket %d of layer %d is stale: the layer changed after it was prepared",
+                        i, t.layer);
+    }
+    if (n == 0) return KVC_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    for (int i0 = 0; i0 < n; i0 += kCommitMaxLayers) {
+        CommitLayers cl{};
+        cl.n = std::min(n - i0, kCommitMaxLayers);
+        for (int i = 0; i < cl.n; ++i) cl.layer[i] = tickets[i0 + i].layer;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_commit_layers(h->len_d, h->next_d, cl, B, s); }));
+    }
+    for (int i = 0; i < n; ++i) {
+        const int l = tickets[i].layer;
+        h->layer_version[l] += 1;
+        for (int b = 0; b < B; ++b) {
+            h->len_h[(size_t)l * B + b] += 1;
+            h->next_h[(size_t)l * B + b] += 1;
+        }
     }
     return KVC_OK;
 }
@@ -843,6 +917,7 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         lenh[b] += sl_h[b];
         nexth[b] = st_h[b] + sl_h[b];
     }
+    h->layer_version[layer] += 1;
     return KVC_OK;
 }
 
@@ -856,6 +931,7 @@ kvc_status kvc_reset(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemsetAsync(h->lane_ticket, 0, (size_t)h->B() * h->Hkv() * sizeof(unsigned), s));
     std::fill(h->len_h.begin(), h->len_h.end(), 0);
     std::fill(h->next_h.begin(), h->next_h.end(), 0);
+    for (auto& v : h->layer_version) v += 1;
     h->mirrors_stale = false;
     return KVC_OK;
 }
@@ -885,11 +961,13 @@ kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream) {
                        : launch_truncate(h->len_d, h->next_d, (const int32_t*)dp, L, B, s);
     }));
     KVC_CUDA(h, h->ring.release(s));
-    for (int l = 0; l < L; ++l)
+    for (int l = 0; l < L; ++l) {
+        h->layer_version[l] += 1;
         for (int b = 0; b < B; ++b) {
             h->len_h[(size_t)l * B + b] = cut[b];
             h->next_h[(size_t)l * B + b] = cut[b];
         }
+    }
     return KVC_OK;
 }
 

@@ -132,7 +132,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     } else {
         old_len = FUSED ? a.old_len[b] : a.len[b];
         pos = FUSED ? a.pos[b] : 0;
-        if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0) {
+        if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0 && !a.no_commit) {
             a.len_out[b] = old_len + 1;
             a.next_out[b] = pos + 1;
         }

@@ -90,6 +90,7 @@ struct Handle {
     int64_t opt_decode_fused = 1;
     int64_t opt_test_stall = 0;
     int64_t opt_device_lengths = 0;
+    std::vector<uint64_t> layer_version;  // [L] bumped by every change of a layer's state or staged slot
     bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 
     int B() const { return cfg.batch; }
@@ -153,6 +154,7 @@ struct DecodeLaunch {
     const float2* rope_f; const double2* rope;
     unsigned* lane_ticket;               // [B*H_kv] split counters, zero between launches
     int merge_in_kernel;                 // 1: the last CTA of a lane merges its splits
+    int no_commit;                       // 1: a prepared step: leave the lengths to kvc_commit
     int test_stall;                      // test only: the producer issues no loads (waits run out)
     // Device-length step: old lengths and positions are read from len_out /
     // next_out instead of old_len / pos, every sequence uses max_splits splits
@@ -172,6 +174,9 @@ cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, cons
                           int uniform_rows, int B, cudaStream_t s);
 cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                             cudaStream_t s);
+constexpr int kCommitMaxLayers = 64;      // layers one commit launch advances
+struct CommitLayers { int32_t layer[kCommitMaxLayers]; int n; };
+cudaError_t launch_commit_layers(int32_t* len, int32_t* next, const CommitLayers& layers, int B, cudaStream_t s);
 cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                                     uint32_t* err, cudaStream_t s);
 cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,

@@ -31,6 +31,22 @@ cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, cons
     return cudaGetLastError();
 }
 
+// kvc_commit: every listed layer advances by one row, in one launch.
+__global__ void commit_layers_kernel(int32_t* len, int32_t* next, const CommitLayers layers, int B) {
+    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < layers.n * B; u += gridDim.x * blockDim.x) {
+        const int64_t i = (int64_t)layers.layer[u / B] * B + u % B;
+        len[i] += 1;
+        next[i] += 1;
+    }
+}
+
+cudaError_t launch_commit_layers(int32_t* len, int32_t* next, const CommitLayers& layers, int B, cudaStream_t s) {
+    const int n = layers.n * B;
+    if (n <= 0) return cudaSuccess;
+    commit_layers_kernel<<<(n + 255) / 256 < 64 ? (n + 255) / 256 : 64, 256, 0, s>>>(len, next, layers, B);
+    return cudaGetLastError();
+}
+
 __global__ void truncate_kernel(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B) {
     const int u = blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= layers * B) return;

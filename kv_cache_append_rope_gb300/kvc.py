@@ -112,6 +112,21 @@ class KVCache:
                                             ctypes.byref(dv), ctypes.byref(do), _stream(stream)))
         return out
 
+    def prepare_attend(self, layer, q, k, v, out=None, stream=None):
+        """kvc_prepare_attend: a decode step without its commit; returns (out, ticket)."""
+        if out is None:
+            out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
+        dq, dk, dv, do = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
+        ticket = L.kvc_ticket()
+        self._check(L.lib.kvc_prepare_attend(self._h, layer, ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                             ctypes.byref(do), ctypes.byref(ticket), _stream(stream)))
+        return out, ticket
+
+    def commit(self, tickets, stream=None):
+        """kvc_commit: advance every ticket's layer by one row, or none of them."""
+        arr = (L.kvc_ticket * len(tickets))(*tickets)
+        self._check(L.lib.kvc_commit(self._h, arr, len(tickets), _stream(stream)))
+
     def prefill_suffix(self, layer, q, k, v, start_pos=None, seqlen=None, out=True, stream=None):
         """kvc_prefill_suffix.  ``out``: a tensor, True (allocate) or None/False (append only)."""
         if out is True:

@@ -14,6 +14,12 @@ reading (listed in DESIGN.md):
 * no RoPE.  The weights (E [vocab, d] and per layer Wq, Wk, Wv, Wo) are
   inputs: the tests draw them ~ N(0, 1/16) from the seeded generator module.
 
+The RoPE variant (``rope_base`` given) is the same model with the absolute
+sinusoid replaced by rotary positions, as [Ch37] "Append along the position
+axis" uses them: h = E[id]; q and k of a row are rotated at the row's position
+before attention, and the cache keeps the rotated keys.  Its greedy next token
+reads the final hidden row through the tied vocabulary head (logits = h E^T).
+
 The cache is the dict of the truncation listing under "Âì™‰∫õ‰∏úË•øÂøÖÈ°ª‰∏ÄËµ∑Ë£ÅÂâ™":
 {'next_position': int, 'layers': [(k [T, d], v [T, d], positions [T])]}.
 """
@@ -21,6 +27,7 @@ The cache is the dict of the truncation listing under "Âì™‰∫õ‰∏úË•øÂøÖÈ°ª‰∏ÄËµ∑Ë
 import numpy as np
 
 from .attention import causal_attention
+from .rope import rotate
 
 
 def sinusoidal_positions(positions, d):
@@ -35,14 +42,22 @@ def sinusoidal_positions(positions, d):
 
 
 class ToyDecoder:
-    def __init__(self, E, W):
+    def __init__(self, E, W, rope_base=None):
         self.E = np.asarray(E, dtype=np.float64)
         self.W = [tuple(np.asarray(w, dtype=np.float64) for w in layer) for layer in W]
         self.vocab, self.d = self.E.shape
         self.n_layers = len(self.W)
+        self.rope_base = rope_base
 
     def embed(self, ids, positions):
-        return self.E[np.asarray(ids, dtype=np.int64)] + sinusoidal_positions(positions, self.d)
+        rows = self.E[np.asarray(ids, dtype=np.int64)]
+        if self.rope_base is not None:
+            return rows
+        return rows + sinusoidal_positions(positions, self.d)
+
+    def logits(self, h):
+        """Tied vocabulary head: scores of every id for hidden rows ``h``."""
+        return np.asarray(h, dtype=np.float64) @ self.E.T
 
     def project(self, layer, h):
         Wq, Wk, Wv, _ = self.W[layer]
@@ -71,6 +86,9 @@ class ToyDecoder:
         new_layers = []
         for layer, (kc, vc, pc) in enumerate(cache["layers"]):
             q, k, v = self.project(layer, h)
+            if self.rope_base is not None:
+                q = rotate(q, positions, self.rope_base)
+                k = rotate(k, positions, self.rope_base)
             K = np.concatenate([kc, k], axis=0)
             V = np.concatenate([vc, v], axis=0)
             a = causal_attention(q, K, V, kc.shape[0] + np.arange(n))

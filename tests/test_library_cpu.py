@@ -69,6 +69,9 @@ def test_null_arguments(kvc_lib):
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_create_ex(None, ctypes.byref(h))] == "KVC_ERR_NULL"
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_append_attend(None, 0, None, None, None, None, None)] == "KVC_ERR_NULL"
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_truncate(None, None, None)] == "KVC_ERR_NULL"
+    assert kvc_lib.STATUS[kvc_lib.lib.kvc_prepare_attend(None, 0, None, None, None, None, None, None)] == "KVC_ERR_NULL"
+    assert kvc_lib.STATUS[kvc_lib.lib.kvc_commit(None, None, 0, None)] == "KVC_ERR_NULL"
+    assert kvc_lib.STATUS[kvc_lib.lib.kvc_sync_lengths(None)] == "KVC_ERR_NULL"
     kvc_lib.lib.kvc_destroy(None)
 
 
