@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 1
+#define KVC_ABI_VERSION 2
 
 typedef enum kvc_status {
     KVC_OK = 0,
@@ -92,6 +92,9 @@ typedef struct kvc_config {
     double rope_base;           /* > 0: theta_j = base^(-2j/d_h); 0: no rotation */
     int32_t checked;            /* nonzero: reject NaN/Inf keys and values (adds a device sync per call) */
     int32_t device;             /* CUDA device ordinal */
+    int32_t window;             /* 0: full causal attention; W >= 1: sliding window -- the row at
+                                   slot s attends slots s - W + 1 .. s only ([LCP5] "为什么滑窗部分
+                                   命中必须回退"); storage keeps every row up to C */
 } kvc_config;
 
 /* A contiguous row-major tensor on the device.  ndim <= 4. */
@@ -256,6 +259,16 @@ kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream);
  */
 kvc_status kvc_lcp(const int32_t* cached, int64_t n, const int32_t* query, int64_t m,
                    int32_t* cut);
+
+/*
+ * [LCP5] "为什么滑窗部分命中必须回退": the cut for a sliding-window cache.  A
+ * window cache has lost the early rows of its history, so only a full match of
+ * the cached ids with a query that continues past them reuses it (cut = n);
+ * every other case recomputes (cut = 0).  window == 0 gives kvc_lcp.  Host
+ * only; errors as kvc_lcp, plus KVC_ERR_CONFIG for window < 0.
+ */
+kvc_status kvc_lcp_window(const int32_t* cached, int64_t n, const int32_t* query, int64_t m,
+                          int32_t window, int32_t* cut);
 
 /* Host mirrors of one layer's lengths and next positions, each [B] host
  * (either may be NULL).  After device-length decode steps (KVC_OPT_DEVICE_LENGTHS)

@@ -365,6 +365,7 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
     if (!(c.rope_base >= 0.0) || !std::isfinite(c.rope_base))
         return fail(nullptr, KVC_ERR_CONFIG, "RoPE base must be finite and >= 0");
     if (c.rope_max_positions < 0) return fail(nullptr, KVC_ERR_CONFIG, "rope_max_positions must be >= 0");
+    if (c.window < 0) return fail(nullptr, KVC_ERR_CONFIG, "sliding window must be 0 (none) or >= 1, got %d", c.window);
     const int maxpos = c.rope_max_positions ? c.rope_max_positions : c.capacity;
     if (c.capacity > maxpos)
         return fail(nullptr, KVC_ERR_CAPACITY_EXCEEDS_POSITIONS,
@@ -591,10 +592,12 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     int32_t* nexth = &h->next_h[(size_t)layer * B];
     int max_t = 0;
     int64_t total_keys = 0;
+    const int W = h->cfg.window;
+    auto keys_of = [&](int t) { return W > 0 ? std::min(t, W) : t; };   // rows one query reads
     for (int b = 0; b < B && dev_len; ++b) {
         // the kernel checks the device lengths; the mirrors only size the splits
-        max_t = std::max(max_t, std::min(lenh[b], C - 1) + 1);
-        total_keys += std::min(lenh[b], C - 1) + 1;
+        max_t = std::max(max_t, keys_of(std::min(lenh[b], C - 1) + 1));
+        total_keys += keys_of(std::min(lenh[b], C - 1) + 1);
     }
     for (int b = 0; b < B && !dev_len; ++b) {
         if (lenh[b] >= C)
@@ -602,8 +605,8 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         if (h->rope && nexth[b] >= h->max_positions)
             return fail(h, KVC_ERR_POSITION, "sequence %d would be rotated at position %d, beyond the %d-position table",
                         b, nexth[b], h->max_positions);
-        max_t = std::max(max_t, lenh[b] + 1);
-        total_keys += lenh[b] + 1;
+        max_t = std::max(max_t, keys_of(lenh[b] + 1));
+        total_keys += keys_of(lenh[b] + 1);
     }
     cudaStream_t s = (cudaStream_t)stream;
     KVC_CUDA(h, cudaSetDevice(h->cfg.device));
@@ -661,6 +664,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;
+        dl.window = W;
         dl.fused = 1;
         dl.dev_len = dev_len;
         dl.step_ticket = h->step_ticket + layer;
@@ -701,6 +705,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;
+        dl.window = W;
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
@@ -710,7 +715,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         GenericAttendLaunch g{};
         g.qrot = h->qrot; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = nullptr; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D; g.window = W;
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     h->layer_version[layer] += 1;
@@ -838,7 +843,10 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             for (int hq = 0; hq < Hq; ++hq)
                 for (int qt = 0; qt * 128 < sl_h[b]; ++qt) {
                     const int q_end = std::min(qt * 128 + 128, sl_h[b]);
-                    work.push_back(make_int4(b, hq, qt, (lenh[b] + q_end + 127) / 128));
+                    // key tiles j0 .. (last row's slot) / 128; j0 > 0 only with a sliding window
+                    const int W = h->cfg.window;
+                    const int j0 = W > 0 ? std::max(0, lenh[b] + qt * 128 - W + 1) / 128 : 0;
+                    work.push_back(make_int4(b, hq, qt, (lenh[b] + q_end + 127) / 128 - j0));
                 }
         // Group the query tiles of each (sequence, head) so they stream its K/V together
         // (L2 reuse); groups by total work, longest first; inside a group longest first.
@@ -899,14 +907,14 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         sl.slot0 = h->len_layer(layer); sl.seqlen = seqlen_d;
         sl.work = work_d; sl.n_work = (int)work.size(); sl.counter = h->work_counter;
         sl.out = (float*)out->data; sl.err = h->err_d;
-        sl.B = B; sl.Hq = Hq; sl.Hkv = Hkv; sl.S = S; sl.C = C;
+        sl.B = B; sl.Hq = Hq; sl.Hkv = Hkv; sl.S = S; sl.C = C; sl.window = h->cfg.window;
         sl.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
         KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc(sl, (int)work.size(), s); }));
     } else if (out && !use_tc) {
         GenericAttendLaunch g{};
         g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = seqlen_d; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D; g.window = h->cfg.window;
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
@@ -979,6 +987,23 @@ kvc_status kvc_lcp(const int32_t* cached, int64_t n, const int32_t* query, int64
     const int64_t lim = std::min(n, m);
     while (L < lim && cached[L] == query[L]) ++L;
     const int64_t c = std::min(L, m - 1);
+    if (c > INT32_MAX) return KVC_ERR_CUT;
+    *cut = (int32_t)c;
+    return KVC_OK;
+}
+
+kvc_status kvc_lcp_window(const int32_t* cached, int64_t n, const int32_t* query, int64_t m, int32_t window,
+                          int32_t* cut) {
+    if (window < 0) return KVC_ERR_CONFIG;
+    if (window == 0) return kvc_lcp(cached, n, query, m, cut);
+    if (!cut) return KVC_ERR_NULL;
+    if (m <= 0) return KVC_ERR_EMPTY_QUERY;
+    if (!query || (n > 0 && !cached) || n < 0) return KVC_ERR_NULL;
+    int64_t L = 0;
+    const int64_t lim = std::min(n, m);
+    while (L < lim && cached[L] == query[L]) ++L;
+    // the window is reused whole or not at all
+    const int64_t c = (L == n && m > n) ? n : 0;
     if (c > INT32_MAX) return KVC_ERR_CUT;
     *cut = (int32_t)c;
     return KVC_OK;

@@ -4,7 +4,8 @@
 // newest query across the retained rows plus the candidate key/value row
 // before committing the append": s_j = q.k_j / sqrt(d_h), numerically stable
 // softmax, output sum_j a_j v_j.  [LCP5] section "先看一次历史编辑": a chunk
-// row at slot n + i attends slots 0 .. n + i.
+// row at slot n + i attends slots 0 .. n + i (with a sliding window of W, section
+// "为什么滑窗部分命中必须回退", only slots n + i - W + 1 .. n + i).
 //
 // One warp per query row (b, h, i) streams its t = slot0[b] + i + 1 key/value
 // rows with an online (running max, running sum) softmax.  The accumulator is
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(GenericAttendLaunch
         acc[e] = (A)0;
     }
     A m = -INFINITY, l = 0;
-    for (int j = 0; j < t; ++j) {
+    const int lo = a.window > 0 && t > a.window ? t - a.window : 0;   // sliding window: the last `window` slots
+    for (int j = lo; j < t; ++j) {
         const T* kr = Kl + (int64_t)j * a.d;
         A dot = 0;
 #pragma unroll

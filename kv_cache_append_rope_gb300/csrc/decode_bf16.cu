@@ -126,9 +126,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
         }
         if (reject) return;
-        // every sequence takes max_splits splits, sized from its own length
+        // every sequence takes max_splits splits, sized from its own (windowed) key count
         const int tt = old_len + 1;
-        split_rows = ((tt + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
+        const int nk = a.window > 0 ? min(tt, a.window) : tt;
+        split_rows = ((nk + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
     } else {
         old_len = FUSED ? a.old_len[b] : a.len[b];
         pos = FUSED ? a.pos[b] : 0;
@@ -138,12 +139,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
     }
     const int t = old_len + 1;
-    const int r0 = split * split_rows;
+    // keys lo .. t-1: every retained row, or the `window` most recent ones
+    const int lo = a.window > 0 ? max(0, t - a.window) : 0;
+    const int r0 = lo + split * split_rows;
     if (r0 >= t) return;
     const int r1 = min(t, r0 + split_rows);
     const int ntiles = (r1 - r0 + KT - 1) / KT;
     const int G = a.Hq / a.Hkv;
-    const int nsplit_lane = (t + split_rows - 1) / split_rows;
+    const int nsplit_lane = (t - lo + split_rows - 1) / split_rows;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -451,12 +454,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     if (a.dev_len) {
         // after the step's commit (after a rejected step the output is undefined)
         t = __ldcg(a.len_out + b);
-        rows = ((t + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
         if (t <= 0) return;
+        const int nk = a.window > 0 ? min(t, a.window) : t;
+        rows = ((nk + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
     } else {
         t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
     }
-    const int ns = (t + rows - 1) / rows;
+    const int nkeys = a.window > 0 ? min(t, a.window) : t;
+    const int ns = (nkeys + rows - 1) / rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
     float M = -INFINITY;

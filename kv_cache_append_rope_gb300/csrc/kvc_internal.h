@@ -129,6 +129,7 @@ struct GenericAttendLaunch {
     const int32_t* seqlen;   // [B] device or null
     void* out;               // [B,H_q,S,d] float or double
     int B, Hq, Hkv, S, C, d;
+    int window;              // 0, or each row attends its `window` most recent slots
 };
 cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaStream_t s);
 
@@ -143,6 +144,7 @@ struct DecodeLaunch {
     uint32_t* err;
     int B, Hq, Hkv, C, split_rows, max_splits;
     int out_bf16;
+    int window;              // 0, or the query attends only its `window` most recent slots
     // Fused step (append + attend + split merge + length commit in one launch).
     int fused;
     const __nv_bfloat16* q_in;           // [B,H_q,128] new queries, unrotated
@@ -193,6 +195,8 @@ struct SuffixLaunch {
     float* out;                  // [B,H_q,S,128]
     uint32_t* err;
     int B, Hq, Hkv, S, C;
+    int window;                  // 0, or each row attends its `window` most recent slots; the work
+                                 // item's key tiles then start at tile (cut + 128 q_tile - window + 1) / 128
     float scale_log2;            // log2(e) / sqrt(d_h)
 };
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);

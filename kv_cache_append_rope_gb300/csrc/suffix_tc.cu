@@ -6,7 +6,9 @@
 // prefix plus the suffix rows up to itself.  [Ch37] listing "Evaluate one newest
 // query across the retained rows plus the candidate key/value row before
 // committing the append" fixes the score scale 1/sqrt(d_h) and the
-// max-subtracted softmax.  A long suffix is a dense Q K^T / P V contraction,
+// max-subtracted softmax.  With a sliding window of W slots ([LCP5]
+// "为什么滑窗部分命中必须回退") row cut + i sees slots cut + i - W + 1 .. cut + i:
+// its key tiles start later and the first ones are masked from below too.  A long suffix is a dense Q K^T / P V contraction,
 // which is why this kernel uses tcgen05 tiles.
 //
 // One CTA per work item (sequence b, query head h, 128-row query tile qt).
@@ -105,6 +107,9 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     const int g = h / (a.Hq / a.Hkv);
     const int cut = a.slot0[b];
     const int rows_b = a.seqlen[b];
+    // first key tile: 0, or with a sliding window the tile holding the earliest slot
+    // any row of this query tile sees (its first row's slot - window + 1)
+    const int j0 = a.window > 0 ? max(0, cut + qt * BM - a.window + 1) / BN : 0;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
@@ -171,8 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 }
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, TILE);
-                tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + j * BN, fb);
-                tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + j * BN, fb);
+                tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + (j0 + j) * BN, fb);
+                tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + (j0 + j) * BN, fb);
                 issued = j + 1;
             }
             // Our own copies must have landed before the CTA's shared memory is released.
@@ -262,10 +267,14 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[s]));
 
-            const int kbase = j * BN + half * HC;
-            if (kbase + HC - 1 > cut + qt * BM) {
+            const int kbase = (j0 + j) * BN + half * HC;
+            // causal mask (keys after the row's slot) on diagonal tiles; with a window also
+            // the keys before slot - window + 1 on the first tiles
+            const bool past_window = a.window > 0 && kbase < cut + qt * BM + BM - a.window;
+            if (kbase + HC - 1 > cut + qt * BM || past_window) {
+                const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
 #pragma unroll
-                for (int c = 0; c < HC; ++c) x[c] = (kbase + c > qslot) ? -INFINITY : x[c];
+                for (int c = 0; c < HC; ++c) x[c] = (kbase + c > qslot || kbase + c < klo) ? -INFINITY : x[c];
             }
             // row maximum over this part (8 independent chains of 3-input maxima),
             // then over the other parts of the same rows

@@ -59,7 +59,7 @@ class KVCache:
     """A kvc_handle: per-layer [B, H_kv, C, d_h] key/value storage on one GPU."""
 
     def __init__(self, batch, heads_q, capacity, head_dim, layers=1, heads_kv=None, dtype="bf16",
-                 rope_base=10000.0, rope_max_positions=0, checked=False, device=0):
+                 rope_base=10000.0, rope_max_positions=0, checked=False, device=0, window=0):
         cfg = L.kvc_config()
         cfg.batch, cfg.heads_q = batch, heads_q
         cfg.heads_kv = heads_q if heads_kv is None else heads_kv
@@ -69,6 +69,7 @@ class KVCache:
         cfg.rope_base = float(rope_base)
         cfg.checked = int(bool(checked))
         cfg.device = device
+        cfg.window = window
         self._h = ctypes.c_void_p()
         L.check(L.lib.kvc_create_ex(ctypes.byref(cfg), ctypes.byref(self._h)))
         got = L.kvc_config()
@@ -203,10 +204,14 @@ def _ids(ids):
     return (L.int_array(ids) if len(ids) else None), None
 
 
-def lcp(cached_ids, query_ids):
-    """kvc_lcp: cut = min(longest common prefix, len(query) - 1), on the host."""
+def lcp(cached_ids, query_ids, window=0):
+    """kvc_lcp: cut = min(longest common prefix, len(query) - 1), on the host;
+    kvc_lcp_window for a sliding-window cache (window > 0)."""
     cut = ctypes.c_int32()
     a, keep_a = _ids(cached_ids)
     b, keep_b = _ids(query_ids)
-    L.check(L.lib.kvc_lcp(a, len(cached_ids), b, len(query_ids), ctypes.byref(cut)))
+    if window:
+        L.check(L.lib.kvc_lcp_window(a, len(cached_ids), b, len(query_ids), int(window), ctypes.byref(cut)))
+    else:
+        L.check(L.lib.kvc_lcp(a, len(cached_ids), b, len(query_ids), ctypes.byref(cut)))
     return cut.value

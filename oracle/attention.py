@@ -26,6 +26,10 @@ Readings where the pages are silent (each also listed in the design doc):
   attention only): query head h reads key/value head h // G, G = H_q / H_kv.
 * The causal mask of a suffix chunk is by slot index: suffix row i (slot
   cut + i) sees slots 0 .. cut + i, whatever positions were recorded.
+* Sliding window ([LCP5] "为什么滑窗部分命中必须回退": a window-4 cache keeps
+  only the last four rows, positions 4..7 of 8): with window W >= 1 the row
+  at slot s sees only slots s - W + 1 .. s (its W most recent rows, itself
+  included); W = 0 means no window.
 """
 
 import math
@@ -59,11 +63,12 @@ def attend_newest(q, K, V):
     return w, w @ V
 
 
-def causal_attention(Q, K, V, query_slots):
+def causal_attention(Q, K, V, query_slots, window=0):
     """Masked scaled dot-product attention.
 
     ``Q`` [n, d] query rows, ``K``/``V`` [T, d] key/value rows in slot order;
-    query row i attends slots 0 .. query_slots[i] (inclusive).  Returns [n, d].
+    query row i attends slots 0 .. query_slots[i] (inclusive), and with
+    ``window`` W >= 1 only slots query_slots[i] - W + 1 and later.  Returns [n, d].
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -71,7 +76,10 @@ def causal_attention(Q, K, V, query_slots):
     slots = np.asarray(query_slots, dtype=np.int64)
     scale = 1.0 / math.sqrt(Q.shape[-1])
     s = (Q @ K.T) * scale
-    visible = np.arange(K.shape[0])[None, :] <= slots[:, None]
+    j = np.arange(K.shape[0])[None, :]
+    visible = j <= slots[:, None]
+    if window:
+        visible &= j > slots[:, None] - window
     s = np.where(visible, s, -np.inf)
     return stable_softmax(s) @ V
 
@@ -113,12 +121,13 @@ def decode_reference(q_unrot, q_position, k_unrot, v_unrot, k_positions, base, d
     return out
 
 
-def decode_steps_reference(q_steps, k_unrot, v_unrot, prefix_len, base, dtype):
+def decode_steps_reference(q_steps, k_unrot, v_unrot, prefix_len, base, dtype, window=0):
     """Consecutive decode steps of one sequence, each recomputed from its prefix.
 
     q_steps [steps, H_q, d]: the query of step i sits at position prefix_len + i.
     k_unrot, v_unrot [H_kv, prefix_len + steps, d]: row j sits at position j.
-    Step i attends rows 0 .. prefix_len + i.  Returns [steps, H_q, d].
+    Step i attends rows 0 .. prefix_len + i (with ``window`` W >= 1 only the
+    last W of them).  Returns [steps, H_q, d].
     """
     q_steps = np.asarray(q_steps, dtype=np.float64)
     steps, Hq, _ = q_steps.shape
@@ -129,14 +138,15 @@ def decode_steps_reference(q_steps, k_unrot, v_unrot, prefix_len, base, dtype):
     out = np.empty_like(q_steps)
     for i in range(steps):
         t = prefix_len + i + 1
+        lo = max(0, t - window) if window else 0
         qr = rotate(q_steps[i], np.full(Hq, t - 1), base)
         for h in range(Hq):
             g = kv_head_of(h, Hq, Hkv)
-            out[i, h] = attend_newest(qr[h], K[g, :t], V[g, :t])[1]
+            out[i, h] = attend_newest(qr[h], K[g, lo:t], V[g, lo:t])[1]
     return out
 
 
-def suffix_reference(q_unrot, k_unrot, v_unrot, positions, cut, base, dtype, rows=None):
+def suffix_reference(q_unrot, k_unrot, v_unrot, positions, cut, base, dtype, rows=None, window=0):
     """Suffix-chunk attention of one sequence, by full masked recomputation.
 
     Slots 0 .. cut-1 are the retained prefix, slots cut .. T-1 the suffix.
@@ -144,7 +154,8 @@ def suffix_reference(q_unrot, k_unrot, v_unrot, positions, cut, base, dtype, row
     [H_kv, T, d] every row, ``positions`` [T] the position recorded for each
     slot (normally the slot index; a stale next_position shifts the suffix).
     Suffix row i is rotated at positions[cut + i] and attends slots 0 .. cut+i.
-    ``rows`` optionally selects suffix rows.  Returns [H_q, len(rows), d].
+    ``rows`` optionally selects suffix rows; ``window`` as in causal_attention.
+    Returns [H_q, len(rows), d].
     """
     q_unrot = np.asarray(q_unrot, dtype=np.float64)
     Hq, S, _ = q_unrot.shape
@@ -158,7 +169,7 @@ def suffix_reference(q_unrot, k_unrot, v_unrot, positions, cut, base, dtype, row
     out = np.empty((Hq, rows.size, q_unrot.shape[-1]))
     for h in range(Hq):
         g = kv_head_of(h, Hq, Hkv)
-        out[h] = causal_attention(qr[h], K[g], V[g], cut + rows)
+        out[h] = causal_attention(qr[h], K[g], V[g], cut + rows, window)
     return out
 
 

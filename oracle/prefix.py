@@ -12,6 +12,8 @@
   positions[:cut] and next_position becomes cut.
 * table and text under "27 例得到的计算量与误差": projection rows of the
   continuation are layers x 3 (Q, K, V) x (len(query) - cut).
+* section "为什么滑窗部分命中必须回退": the conservative reuse rule of a
+  sliding-window cache (lcp_cut_window).
 """
 
 import numbers
@@ -47,6 +49,26 @@ def lcp_cut(cached_ids, query_ids):
     if len(cached_ids):
         _validate_ids(cached_ids, "cached")
     return min(longest_common_prefix(cached_ids, query_ids), len(query_ids) - 1)
+
+
+def lcp_cut_window(cached_ids, query_ids, window):
+    """The cut for a sliding-window cache ([LCP5] "为什么滑窗部分命中必须回退").
+
+    A window cache no longer holds the early rows of its history, so a prefix
+    of it cannot stand for a prefix of the history: the window is reused only
+    when the whole cached sequence matches and the query continues past it
+    (cut = len(cached)); any partial hit recomputes from the start (cut = 0).
+    ``window`` == 0 is the full-attention rule (lcp_cut).
+    """
+    if not window:
+        return lcp_cut(cached_ids, query_ids)
+    _validate_ids(query_ids, "query")
+    if len(cached_ids):
+        _validate_ids(cached_ids, "cached")
+    n = len(cached_ids)
+    if longest_common_prefix(cached_ids, query_ids) == n and len(query_ids) > n:
+        return n
+    return 0
 
 
 def projection_rows(layers, query_len, cut):

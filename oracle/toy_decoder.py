@@ -19,6 +19,8 @@ sinusoid replaced by rotary positions, as [Ch37] "Append along the position
 axis" uses them: h = E[id]; q and k of a row are rotated at the row's position
 before attention, and the cache keeps the rotated keys.  Its greedy next token
 reads the final hidden row through the tied vocabulary head (logits = h E^T).
+With ``window`` W >= 1 every row attends only its W most recent rows ([LCP5]
+"为什么滑窗部分命中必须回退" uses a window of 4).
 
 The cache is the dict of the truncation listing under "哪些东西必须一起裁剪":
 {'next_position': int, 'layers': [(k [T, d], v [T, d], positions [T])]}.
@@ -42,12 +44,13 @@ def sinusoidal_positions(positions, d):
 
 
 class ToyDecoder:
-    def __init__(self, E, W, rope_base=None):
+    def __init__(self, E, W, rope_base=None, window=0):
         self.E = np.asarray(E, dtype=np.float64)
         self.W = [tuple(np.asarray(w, dtype=np.float64) for w in layer) for layer in W]
         self.vocab, self.d = self.E.shape
         self.n_layers = len(self.W)
         self.rope_base = rope_base
+        self.window = window           # sliding window of W slots per row (0: none)
 
     def embed(self, ids, positions):
         rows = self.E[np.asarray(ids, dtype=np.int64)]
@@ -91,7 +94,7 @@ class ToyDecoder:
                 k = rotate(k, positions, self.rope_base)
             K = np.concatenate([kc, k], axis=0)
             V = np.concatenate([vc, v], axis=0)
-            a = causal_attention(q, K, V, kc.shape[0] + np.arange(n))
+            a = causal_attention(q, K, V, kc.shape[0] + np.arange(n), self.window)
             h = self.mix(layer, h, a)
             new_layers.append((K, V, np.concatenate([pc, positions])))
         return h, {"next_position": start + n, "layers": new_layers}

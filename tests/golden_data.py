@@ -38,5 +38,5 @@ def lcp5_table():
             example[tok[0]] = float(tok[1])
         else:
             table[tok[0]] = dict(query_len=int(tok[1]), cut=int(tok[2]), rows=int(tok[3]),
-                                 full_rows=int(tok[4]), in_scope=tok[5] == "yes")
+                                 full_rows=int(tok[4]), in_scope=tok[5] == "yes", policy=tok[5])
     return table, example

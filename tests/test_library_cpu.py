@@ -24,7 +24,7 @@ def test_every_declared_symbol_is_exported(kvc_lib):
     for n in names:
         assert hasattr(kvc_lib.lib, n), n
     assert set(names) == set(kvc_lib.EXPORTS)
-    assert kvc_lib.lib.kvc_abi_version() == 1
+    assert kvc_lib.lib.kvc_abi_version() == 2
 
 
 def test_status_strings(kvc_lib):
@@ -80,6 +80,23 @@ def _lcp(kvc_lib, a, b):
     st = kvc_lib.lib.kvc_lcp(kvc_lib.int_array(a) if a else None, len(a),
                              kvc_lib.int_array(b) if b else None, len(b), ctypes.byref(cut))
     return kvc_lib.STATUS[st], cut.value
+
+
+def test_lcp_window_matches_oracle(kvc_lib):
+    """kvc_lcp_window against oracle.prefix.lcp_cut_window on random small id lists."""
+    rng = np.random.default_rng(21)
+    for _ in range(2000):
+        a = rng.integers(0, 3, rng.integers(0, 9)).tolist()
+        b = rng.integers(0, 3, rng.integers(1, 9)).tolist()
+        w = int(rng.integers(0, 4))
+        cut = ctypes.c_int32(-1)
+        st = kvc_lib.lib.kvc_lcp_window(kvc_lib.int_array(a) if a else None, len(a), kvc_lib.int_array(b), len(b),
+                                        w, ctypes.byref(cut))
+        assert kvc_lib.STATUS[st] == "KVC_OK"
+        assert cut.value == P.lcp_cut_window(a, b, w)
+    cut = ctypes.c_int32(-1)
+    assert kvc_lib.STATUS[kvc_lib.lib.kvc_lcp_window(None, 0, kvc_lib.int_array([1]), 1, -1,
+                                                     ctypes.byref(cut))] == "KVC_ERR_CONFIG"
 
 
 def test_lcp_matches_oracle_and_table(kvc_lib):
