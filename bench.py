@@ -64,6 +64,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="mha_decode",
                    choices=["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix", "all"])
+    p.add_argument("--block-rows", type=int, default=0,
+                   help="paged storage with blocks of this many rows (a multiple of 64); 0 = contiguous")
     p.add_argument("--graph", action="store_true",
                    help="decode workloads: lengths kept on the device, each bench step's decode calls "
                         "captured once in a CUDA graph and replayed")
@@ -158,7 +160,7 @@ def gpu_index(local_rank):
 # ----------------------------------------------------------------- decode workloads
 
 class DecodeBench:
-    def __init__(self, name, device, batch=0, graph=False):
+    def __init__(self, name, device, batch=0, graph=False, block_rows=0):
         from kv_cache_append_rope_gb300 import workloads as W
         from kv_cache_append_rope_gb300.kvc import KVCache
         cfg = dict(W.CONFIGS[name])
@@ -168,7 +170,7 @@ class DecodeBench:
         B, Hq, Hkv, D, C, steps = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["C"], cfg["steps"]
         self.L0 = W.old_lengths(cfg["seed"], B, cfg["lo"], cfg["hi"], C, steps)
         self.cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype="bf16", rope_base=10000.0,
-                             device=device.index or 0)
+                             device=device.index or 0, block_rows=block_rows)
         S = int(self.L0.max())
         seed = cfg["seed"] * 1000
         # unrotated prefix rows (kept for the oracle sample), appended without attending
@@ -300,7 +302,9 @@ class DecodeBench:
                  f"({self.kv_bytes / self.steps / 1e9:.3f} GB); the 64 steps stream "
                  f"{self.kv_bytes / 1e9:.2f} GB; L2 not flushed between bench steps"),
                 "launch": f"CUDA graph of the {self.steps} decode calls, lengths on the device" if self.graph is not None
-                else "one kvc_append_attend call per decode step"}
+                else "one kvc_append_attend call per decode step",
+                "storage": (f"paged, {self.cache.config.block_rows}-row blocks" if self.cache.config.block_rows
+                            else "contiguous")}
 
     def oracle_sample(self, budget_s=15.0):
         """Oracle decode of sampled lanes (all steps); returns (seconds, bytes, description)."""
@@ -331,7 +335,7 @@ class DecodeBench:
 # ----------------------------------------------------------------- suffix workload
 
 class SuffixBench:
-    def __init__(self, device, batch=0):
+    def __init__(self, device, batch=0, block_rows=0):
         from kv_cache_append_rope_gb300 import workloads as W
         from kv_cache_append_rope_gb300.kvc import KVCache
         c = dict(W.CONFIGS["suffix"])
@@ -341,7 +345,8 @@ class SuffixBench:
         B, H, D = c["B"], c["Hq"], c["D"]
         self.T = c["prefix"] + c["appended"]
         self.cached, self.query, self.edit = W.edited_histories(c["seed"], B, c["prefix"], c["appended"], c["vocab"])
-        self.cache = KVCache(B, H, self.T, D, dtype="bf16", rope_base=10000.0, device=device.index or 0)
+        self.cache = KVCache(B, H, self.T, D, dtype="bf16", rope_base=10000.0, device=device.index or 0,
+                             block_rows=block_rows)
         seed = c["seed"] * 1000
         self.k_prefix = W.normal((B, H, c["prefix"], D), seed + 1, device=device)
         self.v_prefix = W.normal((B, H, c["prefix"], D), seed + 2, device=device)
@@ -402,7 +407,9 @@ class SuffixBench:
                 "appended_tokens": c["appended"], "C": self.T, "cuts": self.cuts,
                 "flops_per_step": self.flops,
                 "l2": "inputs larger than L2: the K/V prefix alone is "
-                      f"{self.k_prefix.nbytes * 2 / 1e9:.1f} GB"}
+                      f"{self.k_prefix.nbytes * 2 / 1e9:.1f} GB",
+                "storage": (f"paged, {self.cache.config.block_rows}-row blocks" if self.cache.config.block_rows
+                            else "contiguous")}
 
     def oracle_sample(self, budget_s=15.0):
         from oracle import attention as A
@@ -422,8 +429,10 @@ class SuffixBench:
 
 # ----------------------------------------------------------------- driver
 
-def make_bench(name, device, batch=0, graph=False):
-    return SuffixBench(device, batch) if name == "suffix" else DecodeBench(name, device, batch, graph)
+def make_bench(name, device, batch=0, graph=False, block_rows=0):
+    if name == "suffix":
+        return SuffixBench(device, batch, block_rows)
+    return DecodeBench(name, device, batch, graph, block_rows)
 
 
 def dist_setup(args):
@@ -466,7 +475,7 @@ def run_ours(args, name, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     hbm, tflops, peak_kind = peaks()
-    bench = make_bench(name, device, args.batch, args.graph)
+    bench = make_bench(name, device, args.batch, args.graph, args.block_rows)
     cache = bench.cache
     for _ in range(args.warmup):
         bench.step()

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 2
+#define KVC_ABI_VERSION 3
 
 typedef enum kvc_status {
     KVC_OK = 0,
@@ -95,6 +95,14 @@ typedef struct kvc_config {
     int32_t window;             /* 0: full causal attention; W >= 1: sliding window -- the row at
                                    slot s attends slots s - W + 1 .. s only ([LCP5] "为什么滑窗部分
                                    命中必须回退"); storage keeps every row up to C */
+    int32_t block_rows;         /* 0: contiguous [B, H_kv, C, d_h] storage per layer.  P > 0 (a
+                                   power of two >= 64): paged storage -- each layer holds a pool of
+                                   blocks [blocks, H_kv, P, d_h] and one block table [B][ceil(C/P)]
+                                   (shared by all layers) maps each sequence's logical blocks to
+                                   physical ones; blocks are taken from the pool as rows are
+                                   appended, returned by truncate/reset, and can be shared between
+                                   sequences (kvc_share_prefix, copy-on-write) */
+    int32_t blocks;             /* paged: physical blocks per layer pool; 0 means B * ceil(C/P) */
 } kvc_config;
 
 /* A contiguous row-major tensor on the device.  ndim <= 4. */
@@ -166,7 +174,8 @@ void kvc_destroy(kvc_handle* h);
  * n_b += 1 and p_b += 1.
  * Errors (no state change): KVC_ERR_LAYER, KVC_ERR_NULL, KVC_ERR_DTYPE,
  * KVC_ERR_QUERY_SHAPE (including more than one token), KVC_ERR_KEY_SHAPE,
- * KVC_ERR_VALUE_SHAPE, KVC_ERR_OUTPUT_SHAPE, KVC_ERR_FULL (some n_b == C),
+ * KVC_ERR_VALUE_SHAPE, KVC_ERR_OUTPUT_SHAPE, KVC_ERR_FULL (some n_b == C, or a
+ * paged pool without the free blocks the step needs),
  * KVC_ERR_POSITION (some p_b >= rope_max_positions), and in checked mode
  * KVC_ERR_NONFINITE_KEY / KVC_ERR_NONFINITE_VALUE.
  * With KVC_OPT_DEVICE_LENGTHS on, the length and position checks run on the
@@ -281,12 +290,33 @@ kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
  * lengths and next positions into the host mirrors.  No other effect. */
 kvc_status kvc_sync_lengths(kvc_handle* h);
 
+/*
+ * Paged storage ([LCP5] "这一轮留下的工程判断": blocked storage as the next step of
+ * prefix reuse; section "查询流程与缓存所有权", step 4 keeps the reusable rows of a
+ * cached entry and computes only the rest).  Sequence `dst` (empty in every
+ * layer) takes the first `rows` rows of sequence `src` (rows <= src's length
+ * in every layer) in every layer by sharing src's blocks -- no copy; a shared
+ * block is copied only when either sequence later writes into it.  dst's
+ * positions are copied from src; its length and next position become `rows`.
+ * KVC_ERR_CONFIG for contiguous storage or dst == src; KVC_ERR_CUT when dst
+ * is not empty or rows exceeds src's length; no state change on error.
+ */
+kvc_status kvc_share_prefix(kvc_handle* h, int32_t dst, int32_t src, int32_t rows, void* stream);
+
+/*
+ * Paged storage: the host copy of the block table, [B][ceil(C/P)] physical
+ * block ids (-1: no block), and the number of unused blocks in the pool.
+ * Either pointer may be NULL.  KVC_ERR_CONFIG for contiguous storage.
+ */
+kvc_status kvc_block_table(const kvc_handle* h, int32_t* table, int32_t* free_blocks);
+
 /* The handle's configuration (rope_max_positions resolved). */
 kvc_status kvc_get_config(const kvc_handle* h, kvc_config* out);
 
 /* Device pointers of one layer's storage, for audits: keys and values
- * [B, H_kv, C, d_h] storage dtype, positions [B, C] int32.  Owned by the
- * handle; valid until kvc_destroy.  Any output pointer may be NULL. */
+ * [B, H_kv, C, d_h] storage dtype (paged: the pool [blocks, H_kv, P, d_h]),
+ * positions [B, C] int32.  Owned by the handle; valid until kvc_destroy.  Any
+ * output pointer may be NULL. */
 kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** values,
                        int32_t** positions);
 
@@ -353,7 +383,9 @@ typedef enum kvc_option {
                                       scratch is allocated outside the capture.  kvc_truncate then checks
                                       its cuts on the device too.  Changing the option, and
                                       kvc_prefill_suffix and kvc_check while it is on, synchronise the
-                                      device and read the lengths back. */
+                                      device and read the lengths back.  Paged storage cannot use it
+                                      (blocks are taken on the host as rows are appended):
+                                      KVC_ERR_CONFIG. */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

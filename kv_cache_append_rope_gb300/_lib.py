@@ -31,7 +31,7 @@ KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "gen
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
            "kvc_destroy", "kvc_append_attend", "kvc_prepare_attend", "kvc_commit", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
-           "kvc_lcp", "kvc_lcp_window", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
+           "kvc_lcp", "kvc_lcp_window", "kvc_share_prefix", "kvc_block_table", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
            "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
 
 
@@ -46,7 +46,8 @@ class kvc_config(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads_q", ctypes.c_int32), ("heads_kv", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("layers", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("rope_max_positions", ctypes.c_int32), ("rope_base", ctypes.c_double),
-                ("checked", ctypes.c_int32), ("device", ctypes.c_int32), ("window", ctypes.c_int32)]
+                ("checked", ctypes.c_int32), ("device", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("block_rows", ctypes.c_int32), ("blocks", ctypes.c_int32)]
 
 
 class kvc_tensor(ctypes.Structure):
@@ -85,6 +86,8 @@ def _load():
         "kvc_truncate": (ctypes.c_int, [_P, _I32P, _P]),
         "kvc_lcp": (ctypes.c_int, [_I32P, ctypes.c_int64, _I32P, ctypes.c_int64, _I32P]),
         "kvc_lcp_window": (ctypes.c_int, [_I32P, ctypes.c_int64, _I32P, ctypes.c_int64, ctypes.c_int32, _I32P]),
+        "kvc_share_prefix": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P]),
+        "kvc_block_table": (ctypes.c_int, [_P, _I32P, _I32P]),
         "kvc_get_lengths": (ctypes.c_int, [_P, ctypes.c_int32, _I32P, _I32P]),
         "kvc_sync_lengths": (ctypes.c_int, [_P]),
         "kvc_get_config": (ctypes.c_int, [_P, ctypes.POINTER(kvc_config)]),

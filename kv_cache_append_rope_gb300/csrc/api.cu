@@ -218,6 +218,7 @@ void free_all(kvc_handle* h) {
     cudaFree(h->work_counter);
     cudaFree(h->lane_ticket);
     cudaFree(h->step_ticket);
+    cudaFree(h->table_d);
     h->ring.destroy();
     for (auto& t : h->timers) {
         for (auto e : t.start) cudaEventDestroy(e);
@@ -366,20 +367,35 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
         return fail(nullptr, KVC_ERR_CONFIG, "RoPE base must be finite and >= 0");
     if (c.rope_max_positions < 0) return fail(nullptr, KVC_ERR_CONFIG, "rope_max_positions must be >= 0");
     if (c.window < 0) return fail(nullptr, KVC_ERR_CONFIG, "sliding window must be 0 (none) or >= 1, got %d", c.window);
+    if (c.block_rows < 0 || (c.block_rows && (c.block_rows < 64 || (c.block_rows & (c.block_rows - 1)))))
+        return fail(nullptr, KVC_ERR_CONFIG, "block rows must be 0 (contiguous) or a power of two >= 64, got %d",
+                    c.block_rows);
+    if (c.blocks < 0) return fail(nullptr, KVC_ERR_CONFIG, "block count must be >= 0, got %d", c.blocks);
+    const bool paged = c.block_rows > 0;
+    const int nblk = paged ? (int)(((int64_t)c.capacity + c.block_rows - 1) / c.block_rows) : 0;
+    if (paged && c.blocks == 0) {
+        if ((int64_t)c.batch * nblk > INT32_MAX) return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW, "too many blocks");
+        c.blocks = c.batch * nblk;
+    }
+    if (!paged) c.blocks = 0;
     const int maxpos = c.rope_max_positions ? c.rope_max_positions : c.capacity;
     if (c.capacity > maxpos)
         return fail(nullptr, KVC_ERR_CAPACITY_EXCEEDS_POSITIONS,
                     "capacity %d is larger than the %d positions the RoPE table covers", c.capacity, maxpos);
     c.rope_max_positions = maxpos;
 
-    size_t layer_elems, all_elems, bytes, t;
-    if (!mul_ok(c.batch, c.heads_kv, &t) || !mul_ok(t, c.capacity, &t) || !mul_ok(t, c.head_dim, &layer_elems) ||
+    size_t layer_elems, all_elems, bytes, t, store_rows;
+    // rows of one layer's key (or value) array: [B][H_kv][C], or the pool [blocks][H_kv][P]
+    const bool rows_ok = paged ? mul_ok(c.blocks, c.heads_kv, &t) && mul_ok(t, c.block_rows, &store_rows)
+                               : mul_ok(c.batch, c.heads_kv, &t) && mul_ok(t, c.capacity, &store_rows);
+    if (!rows_ok || !mul_ok(store_rows, c.head_dim, &layer_elems) ||
         !mul_ok(layer_elems, c.layers, &all_elems) || !mul_ok(all_elems, dtype_size(c.dtype), &bytes))
         return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW,
                     "element count overflows for batch %d, %d heads, capacity %d, head width %d, %d layers", c.batch,
                     c.heads_kv, c.capacity, c.head_dim, c.layers);
-    if ((uint64_t)c.batch * c.heads_kv * c.capacity > (uint64_t)INT32_MAX)
-        return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW, "batch * heads_kv * capacity must fit in 31 bits");
+    if ((uint64_t)c.batch * c.heads_kv * c.capacity > (uint64_t)INT32_MAX || store_rows > (uint64_t)INT32_MAX)
+        return fail(nullptr, KVC_ERR_ELEMENT_OVERFLOW,
+                    "batch * heads_kv * capacity (and the pool's rows) must fit in 31 bits");
 
     cudaError_t e = cudaSetDevice(c.device);
     if (e != cudaSuccess) return fail(nullptr, KVC_ERR_CUDA, "cudaSetDevice(%d) failed: %s", c.device, cudaGetErrorString(e));
@@ -408,6 +424,7 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
               alloc((void**)&h->work_counter, 64) &&
               alloc((void**)&h->lane_ticket, (size_t)c.batch * c.heads_kv * sizeof(unsigned)) &&
               alloc((void**)&h->step_ticket, (size_t)c.layers * sizeof(unsigned));
+    if (ok && paged) ok = alloc((void**)&h->table_d, (size_t)c.batch * nblk * sizeof(int32_t));
     if (ok && c.rope_base > 0.0)
         ok = alloc((void**)&h->rope, (size_t)maxpos * (c.head_dim / 2) * sizeof(double2)) &&
              alloc((void**)&h->rope_f, (size_t)maxpos * (c.head_dim / 2) * sizeof(float2));
@@ -432,6 +449,16 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
         return abort_cuda(e, "cudaMemset");
     if ((e = cudaMemset(h->step_ticket, 0, (size_t)c.layers * sizeof(unsigned))) != cudaSuccess)
         return abort_cuda(e, "cudaMemset");
+    if (paged) {
+        h->nblk = nblk;
+        h->nblocks = c.blocks;
+        h->table_h.assign((size_t)c.batch * nblk, -1);
+        h->refcnt.assign(c.blocks, 0);
+        h->free_blocks.resize(c.blocks);
+        for (int i = 0; i < c.blocks; ++i) h->free_blocks[i] = c.blocks - 1 - i;   // handed out 0, 1, 2, ...
+        if ((e = cudaMemset(h->table_d, 0xff, (size_t)c.batch * nblk * sizeof(int32_t))) != cudaSuccess)
+            return abort_cuda(e, "cudaMemset");
+    }
     if ((e = cudaHostAlloc((void**)&h->nonfinite_h, 2 * sizeof(unsigned long long), cudaHostAllocDefault)) !=
         cudaSuccess)
         return abort_cuda(e, "cudaHostAlloc");
@@ -465,7 +492,7 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
         h->tmap_k128.resize(c.layers);
         h->tmap_v128.resize(c.layers);
         bool all = true;
-        const uint64_t rows = (uint64_t)c.batch * c.heads_kv * c.capacity;
+        const uint64_t rows = store_rows;
         for (int l = 0; l < c.layers && all; ++l)
             all = encode_rows_map(&h->tmap_k[l], h->K_layer(l), rows, 64) &&
                   encode_rows_map(&h->tmap_v[l], h->V_layer(l), rows, 64) &&
@@ -507,6 +534,80 @@ static kvc_status refresh_mirrors(kvc_handle* h) {
     KVC_CUDA(h, cudaMemcpy(h->next_h.data(), h->next_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
     h->mirrors_stale = false;
     return KVC_OK;
+}
+
+// ---- paged storage: block allocation on the host, copies on the device -------------
+
+static kvc_status upload_table(kvc_handle* h, cudaStream_t s) {
+    if (!h->table_dirty) return KVC_OK;
+    const size_t bytes = h->table_h.size() * sizeof(int32_t);
+    void* hp;
+    KVC_CUDA(h, h->ring.acquire(bytes, &hp));
+    memcpy(hp, h->table_h.data(), bytes);
+    KVC_CUDA(h, cudaMemcpyAsync(h->table_d, hp, bytes, cudaMemcpyHostToDevice, s));
+    KVC_CUDA(h, h->ring.release(s));
+    h->table_dirty = false;
+    return KVC_OK;
+}
+
+// Gives every sequence b blocks for rows [from[b], to[b]) -- a block that is shared
+// with another sequence is first copied (copy-on-write) -- then uploads the table.
+// All or nothing: KVC_ERR_FULL, with no change, when the pool is short.
+static kvc_status ensure_blocks(kvc_handle* h, const int32_t* from, const int32_t* to, cudaStream_t s) {
+    if (!h->paged()) return KVC_OK;
+    const int B = h->B(), P = h->cfg.block_rows, nb = h->nblk;
+    int64_t need = 0;
+    for (int b = 0; b < B; ++b)
+        for (int j = from[b] / P; from[b] < to[b] && j <= (to[b] - 1) / P; ++j) {
+            const int blk = h->table_h[(size_t)b * nb + j];
+            need += blk < 0 || h->refcnt[blk] > 1;
+        }
+    if (need > (int64_t)h->free_blocks.size())
+        return fail(h, KVC_ERR_FULL, "the block pool has %zu free blocks; the call needs %lld", h->free_blocks.size(),
+                    (long long)need);
+    std::vector<int2> cow;
+    for (int b = 0; b < B; ++b)
+        for (int j = from[b] / P; from[b] < to[b] && j <= (to[b] - 1) / P; ++j) {
+            int32_t& slot = h->table_h[(size_t)b * nb + j];
+            if (slot >= 0 && h->refcnt[slot] == 1) continue;
+            const int fresh = h->free_blocks.back();
+            h->free_blocks.pop_back();
+            h->refcnt[fresh] = 1;
+            if (slot >= 0) {
+                h->refcnt[slot] -= 1;
+                cow.push_back(make_int2(slot, fresh));
+            }
+            slot = fresh;
+            h->table_dirty = true;
+        }
+    if (!cow.empty()) {
+        void* hp;
+        void* dp;
+        const size_t bytes = cow.size() * sizeof(int2);
+        KVC_CUDA(h, h->ring.acquire(bytes, &hp));
+        memcpy(hp, cow.data(), bytes);
+        KVC_CUDA(h, h->ring.upload(bytes, s, &dp));
+        const size_t block_bytes = (size_t)h->Hkv() * P * h->D() * h->elem_size;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
+            return launch_copy_blocks((char*)h->K, (char*)h->V, h->layer_elems * h->elem_size, h->cfg.layers,
+                                      block_bytes, (const int2*)dp, (int)cow.size(), s);
+        }));
+        KVC_CUDA(h, h->ring.release(s));
+    }
+    return upload_table(h, s);
+}
+
+// Returns the blocks of sequence b past its first `keep` rows to the pool.
+static void release_blocks(kvc_handle* h, int b, int keep) {
+    if (!h->paged()) return;
+    const int P = h->cfg.block_rows;
+    for (int j = (keep + P - 1) / P; j < h->nblk; ++j) {
+        int32_t& slot = h->table_h[(size_t)b * h->nblk + j];
+        if (slot < 0) continue;
+        if (--h->refcnt[slot] == 0) h->free_blocks.push_back(slot);
+        slot = -1;
+        h->table_dirty = true;
+    }
 }
 
 static kvc_status ensure_partials(kvc_handle* h, size_t splits) {
@@ -593,7 +694,8 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     int max_t = 0;
     int64_t total_keys = 0;
     const int W = h->cfg.window;
-    auto keys_of = [&](int t) { return W > 0 ? std::min(t, W) : t; };   // rows one query reads
+    // key rows one query's splits cover: from its window start rounded down to a 64-row tile
+    auto keys_of = [&](int t) { return W > 0 ? t - (std::max(0, t - W) & ~63) : t; };
     for (int b = 0; b < B && dev_len; ++b) {
         // the kernel checks the device lengths; the mirrors only size the splits
         max_t = std::max(max_t, keys_of(std::min(lenh[b], C - 1) + 1));
@@ -613,6 +715,11 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     if (h->cfg.checked) {
         if ((st = check_nonfinite(h, k, v, (int64_t)B * Hkv * D, (int64_t)B * Hkv * D, s)) != KVC_OK) return st;
     }
+    if (h->paged()) {
+        std::vector<int32_t> to(B);
+        for (int b = 0; b < B; ++b) to[b] = lenh[b] + 1;
+        if ((st = ensure_blocks(h, lenh, to.data(), s)) != KVC_OK) return st;
+    }
     AppendLaunch ap{};
     ap.q = q->data; ap.k = k->data; ap.v = v->data;
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
@@ -620,6 +727,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     ap.qrot = h->qrot; ap.qrot_kind = dt == KVC_F64 ? 1 : 0;
     ap.rope = h->rope; ap.rope_f = h->rope_f; ap.err = h->err_d;
     ap.B = B; ap.Hq = Hq; ap.Hkv = Hkv; ap.S = 1; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
+    ap.kv = h->layout();
 
     int split_rows = 0, max_splits = 1;
     if (fast) {
@@ -665,6 +773,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;
         dl.window = W;
+        dl.kv = h->layout();
         dl.fused = 1;
         dl.dev_len = dev_len;
         dl.step_ticket = h->step_ticket + layer;
@@ -706,6 +815,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;
         dl.window = W;
+        dl.kv = h->layout();
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
@@ -715,7 +825,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         GenericAttendLaunch g{};
         g.qrot = h->qrot; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = nullptr; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D; g.window = W;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D; g.window = W; g.kv = h->layout();
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     h->layer_version[layer] += 1;
@@ -832,6 +942,11 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         const int64_t nk = (int64_t)B * Hkv * S * D;
         if ((st = check_nonfinite(h, k, v, nk, nk, s)) != KVC_OK) return st;
     }
+    if (h->paged()) {
+        std::vector<int32_t> to(B);
+        for (int b = 0; b < B; ++b) to[b] = lenh[b] + sl_h[b];
+        if ((st = ensure_blocks(h, lenh, to.data(), s)) != KVC_OK) return st;
+    }
     // Attention kernel: the tensor-core tile kernel for bf16 with d_h = 128, else the generic one.
     const bool tc_ok = dt == KVC_BF16 && D == 128 && h->have_tmaps;
     if (out && h->opt_suffix_kernel == 2 && !tc_ok)
@@ -896,14 +1011,17 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = use_tc ? 2 : (dt == KVC_F64 ? 1 : 0);
     ap.rope = h->rope; ap.rope_f = h->rope_f; ap.err = h->err_d;
     ap.B = B; ap.Hq = out ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
+    ap.kv = h->layout();
     // Without an output the query heads are skipped (Hq = 0 in the launch).
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
     if (out && use_tc && !work.empty()) {
         SuffixLaunch sl{};
         if (!encode_rows_map(&sl.tmQ, h->qrot_chunk, (uint64_t)B * Hq * S, 128))
             return fail(h, KVC_ERR_CUDA, "cannot encode the query tensor map");
-        sl.tmK = h->tmap_k128[layer];
-        sl.tmV = h->tmap_v128[layer];
+        // contiguous: 128-row boxes; paged: 64-row boxes, two per key tile
+        sl.tmK = h->paged() ? h->tmap_k[layer] : h->tmap_k128[layer];
+        sl.tmV = h->paged() ? h->tmap_v[layer] : h->tmap_v128[layer];
+        sl.kv = h->layout();
         sl.slot0 = h->len_layer(layer); sl.seqlen = seqlen_d;
         sl.work = work_d; sl.n_work = (int)work.size(); sl.counter = h->work_counter;
         sl.out = (float*)out->data; sl.err = h->err_d;
@@ -914,7 +1032,7 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         GenericAttendLaunch g{};
         g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = seqlen_d; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D; g.window = h->cfg.window;
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D; g.window = h->cfg.window; g.kv = h->layout();
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
@@ -937,6 +1055,9 @@ kvc_status kvc_reset(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemsetAsync(h->len_d, 0, n * sizeof(int32_t), s));
     KVC_CUDA(h, cudaMemsetAsync(h->next_d, 0, n * sizeof(int32_t), s));
     KVC_CUDA(h, cudaMemsetAsync(h->lane_ticket, 0, (size_t)h->B() * h->Hkv() * sizeof(unsigned), s));
+    for (int b = 0; b < h->B(); ++b) release_blocks(h, b, 0);
+    kvc_status st = upload_table(h, s);
+    if (st != KVC_OK) return st;
     std::fill(h->len_h.begin(), h->len_h.end(), 0);
     std::fill(h->next_h.begin(), h->next_h.end(), 0);
     for (auto& v : h->layer_version) v += 1;
@@ -969,6 +1090,9 @@ kvc_status kvc_truncate(kvc_handle* h, const int32_t* cut, void* stream) {
                        : launch_truncate(h->len_d, h->next_d, (const int32_t*)dp, L, B, s);
     }));
     KVC_CUDA(h, h->ring.release(s));
+    for (int b = 0; b < B; ++b) release_blocks(h, b, cut[b]);
+    kvc_status ust = upload_table(h, s);
+    if (ust != KVC_OK) return ust;
     for (int l = 0; l < L; ++l) {
         h->layer_version[l] += 1;
         for (int b = 0; b < B; ++b) {
@@ -1015,6 +1139,53 @@ kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
     const int B = h->B();
     if (lengths) memcpy(lengths, &h->len_h[(size_t)layer * B], B * sizeof(int32_t));
     if (next_positions) memcpy(next_positions, &h->next_h[(size_t)layer * B], B * sizeof(int32_t));
+    return KVC_OK;
+}
+
+kvc_status kvc_share_prefix(kvc_handle* h, int32_t dst, int32_t src, int32_t rows, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (!h->paged()) return fail(h, KVC_ERR_CONFIG, "sharing a prefix needs paged storage (block_rows > 0)");
+    const int B = h->B(), L = h->cfg.layers, P = h->cfg.block_rows;
+    if (dst < 0 || dst >= B || src < 0 || src >= B || dst == src)
+        return fail(h, KVC_ERR_CONFIG, "sequences %d <- %d: need two distinct indices in [0, %d)", dst, src, B);
+    for (int l = 0; l < L; ++l) {
+        if (h->len_h[(size_t)l * B + dst] != 0)
+            return fail(h, KVC_ERR_CUT, "sequence %d holds %d rows in layer %d; it must be empty", dst,
+                        h->len_h[(size_t)l * B + dst], l);
+        if (rows < 0 || rows > h->len_h[(size_t)l * B + src])
+            return fail(h, KVC_ERR_CUT, "%d rows exceed the %d rows of sequence %d in layer %d", rows,
+                        h->len_h[(size_t)l * B + src], src, l);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    release_blocks(h, dst, 0);        // blocks a prepared, uncommitted step may have taken
+    for (int j = 0; j < (rows + P - 1) / P; ++j) {
+        const int blk = h->table_h[(size_t)src * h->nblk + j];
+        h->table_h[(size_t)dst * h->nblk + j] = blk;
+        h->refcnt[blk] += 1;
+        h->table_dirty = true;
+    }
+    kvc_status st = upload_table(h, s);
+    if (st != KVC_OK) return st;
+    const int C = h->C();
+    for (int l = 0; l < L && rows > 0; ++l)
+        KVC_CUDA(h, cudaMemcpyAsync(h->pos_layer(l) + (size_t)dst * C, h->pos_layer(l) + (size_t)src * C,
+                                    (size_t)rows * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s,
+                      [&] { return launch_set_lengths(h->len_d, h->next_d, L, B, dst, rows, s); }));
+    for (int l = 0; l < L; ++l) {
+        h->len_h[(size_t)l * B + dst] = rows;
+        h->next_h[(size_t)l * B + dst] = rows;
+        h->layer_version[l] += 1;
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_block_table(const kvc_handle* h, int32_t* table, int32_t* free_blocks) {
+    if (!h) return KVC_ERR_NULL;
+    if (!h->paged()) return KVC_ERR_CONFIG;
+    if (table) memcpy(table, h->table_h.data(), h->table_h.size() * sizeof(int32_t));
+    if (free_blocks) *free_blocks = (int32_t)h->free_blocks.size();
     return KVC_OK;
 }
 
@@ -1093,6 +1264,8 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             h->opt_test_stall = value != 0;
             return KVC_OK;
         case KVC_OPT_DEVICE_LENGTHS: {
+            if (value && h->paged())
+                return fail(h, KVC_ERR_CONFIG, "device-held lengths need contiguous storage (blocks are taken on the host)");
             kvc_status st = refresh_mirrors(h);
             if (st != KVC_OK) return st;
             h->opt_device_lengths = value != 0;

@@ -37,8 +37,6 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(GenericAttendLaunch
     const int t = a.slot0[b] + i + 1;
     const int g = h / (a.Hq / a.Hkv);
     const A* q = (const A*)a.qrot + row * a.d;
-    const T* Kl = (const T*)a.K + ((int64_t)b * a.Hkv + g) * a.C * a.d;
-    const T* Vl = (const T*)a.V + ((int64_t)b * a.Hkv + g) * a.C * a.d;
     const A scale = (A)1 / sqrt((A)a.d);
 
     A qv[MAXE], acc[MAXE];
@@ -51,7 +49,8 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(GenericAttendLaunch
     A m = -INFINITY, l = 0;
     const int lo = a.window > 0 && t > a.window ? t - a.window : 0;   // sliding window: the last `window` slots
     for (int j = lo; j < t; ++j) {
-        const T* kr = Kl + (int64_t)j * a.d;
+        const int64_t rj = kv_row(a.kv, b, g, j) * a.d;
+        const T* kr = (const T*)a.K + rj;
         A dot = 0;
 #pragma unroll
         for (int e = 0; e < MAXE; ++e) {
@@ -63,7 +62,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(GenericAttendLaunch
         const A corr = exp_acc<A>(m - m_new);
         const A p = exp_acc<A>(s - m_new);
         l = l * corr + p;
-        const T* vr = Vl + (int64_t)j * a.d;
+        const T* vr = (const T*)a.V + rj;
 #pragma unroll
         for (int e = 0; e < MAXE; ++e) {
             const int c = lane + 32 * e;

@@ -56,6 +56,12 @@ template <int MT> struct Cfg;
 template <> struct Cfg<1> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
 template <> struct Cfg<2> { static constexpr int STAGES = 3; static constexpr int MINB = 2; };
 
+// Key rows a query at t - 1 reads, counted from its window start rounded down to a
+// 64-row tile (the splits cover exactly this span).
+__device__ __forceinline__ int key_span(int t, int window) {
+    return window > 0 ? t - (max(0, t - window) & ~(KT - 1)) : t;
+}
+
 // Rotated query pair (c, c+1) of row `row` (< G) of this lane, as float32 (fused step).
 __device__ __forceinline__ float2 fused_q_pair(const DecodeLaunch& a, int b, int qh, int c, int pos) {
     const __nv_bfloat162 v = *(const __nv_bfloat162*)(a.q_in + ((int64_t)b * a.Hq + qh) * D + c);
@@ -127,8 +133,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         if (reject) return;
         // every sequence takes max_splits splits, sized from its own (windowed) key count
-        const int tt = old_len + 1;
-        const int nk = a.window > 0 ? min(tt, a.window) : tt;
+        const int nk = key_span(old_len + 1, a.window);
         split_rows = ((nk + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
     } else {
         old_len = FUSED ? a.old_len[b] : a.len[b];
@@ -139,14 +144,16 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
     }
     const int t = old_len + 1;
-    // keys lo .. t-1: every retained row, or the `window` most recent ones
+    // keys lo .. t-1: every retained row, or the `window` most recent ones; the
+    // splits start at lo rounded down to a tile (keys before lo are masked), so
+    // that a 64-row tile never crosses a block of paged storage
     const int lo = a.window > 0 ? max(0, t - a.window) : 0;
-    const int r0 = lo + split * split_rows;
+    const int r0 = (lo & ~(KT - 1)) + split * split_rows;
     if (r0 >= t) return;
     const int r1 = min(t, r0 + split_rows);
     const int ntiles = (r1 - r0 + KT - 1) / KT;
     const int G = a.Hq / a.Hkv;
-    const int nsplit_lane = (t - lo + split_rows - 1) / split_rows;
+    const int nsplit_lane = (key_span(t, a.window) + split_rows - 1) / split_rows;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -171,7 +178,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             // key (bit-exact bf16 rounding), store the value and the position, then
             // order these generic-proxy writes before this warp's TMA reads of them.
             const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
-            const int64_t dst = (((int64_t)b * a.Hkv + hkv) * a.C + old_len) * D + lane * 4;
+            const int64_t dst = kv_row(a.kv, b, hkv, old_len) * D + lane * 4;
             const uint2 kraw = *(const uint2*)(a.k_in + src);
             const uint2 vraw = *(const uint2*)(a.v_in + src);
             const __nv_bfloat16* kin = (const __nv_bfloat16*)&kraw;
@@ -198,8 +205,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (lane == 0 && !a.test_stall) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
+            // (paged storage: the next tile's block-table entry is loaded one tile ahead,
+            // so its latency overlaps the wait for a free stage)
+            int y_next = (int)kv_row(a.kv, b, hkv, r0);
             for (int i = 0; i < ntiles; ++i) {
                 const int s = i % STAGES;
+                const int y = y_next;
+                if (i + 1 < ntiles) y_next = (int)kv_row(a.kv, b, hkv, r0 + (i + 1) * KT);
                 if (i >= STAGES && !mbar_wait_bounded(smem_u32(&empty[s]), ((i / STAGES) - 1) & 1)) {
                     *s_err = 1;
                     atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
@@ -207,7 +219,6 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 }
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                const int y = lane_kv * a.C + r0 + i * KT;
                 uint8_t* st = smem + s * STAGE_BYTES;
                 tma_load_2d(smem_u32(st), &tmK, 0, y, fb);
                 tma_load_2d(smem_u32(st + HALF_BYTES), &tmK, 64, y, fb);
@@ -304,7 +315,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = key_base + nt * 8 + qc + e;
-                    if (key >= r1) {
+                    if (key >= r1 || key < lo) {
                         sc[nt][e] = -INFINITY;
                         sc[nt][2 + e] = -INFINITY;
                     }
@@ -455,13 +466,11 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
         // after the step's commit (after a rejected step the output is undefined)
         t = __ldcg(a.len_out + b);
         if (t <= 0) return;
-        const int nk = a.window > 0 ? min(t, a.window) : t;
-        rows = ((nk + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
+        rows = ((key_span(t, a.window) + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
     } else {
         t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
     }
-    const int nkeys = a.window > 0 ? min(t, a.window) : t;
-    const int ns = (nkeys + rows - 1) / rows;
+    const int ns = (key_span(t, a.window) + rows - 1) / rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
     float M = -INFINITY;

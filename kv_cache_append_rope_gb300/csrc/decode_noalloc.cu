@@ -157,6 +157,8 @@ extern "C" kvc_status kvc_decode_attend_noalloc(const void* keys, const void* va
     dl.part_ml = (float2*)parts;
     dl.part_o = (float*)(parts + lanes_q * max_splits * sizeof(float2));
     dl.out = out;
+    dl.kv.C = capacity;          // contiguous [B][H_kv][C] rows
+    dl.kv.Hkv = heads_kv;
     dl.err = err;
     dl.B = batch;
     dl.Hq = heads_q;

@@ -13,6 +13,24 @@
 
 namespace kvc {
 
+// Where the stored row of (sequence b, key/value head h, slot) lives in a layer's
+// key (or value) array, in rows of d_h elements.  Contiguous storage is
+// [B][H_kv][C] rows; paged storage is a pool of blocks of P rows, [blocks][H_kv][P],
+// with table[b][slot / P] naming the physical block of each logical block.
+struct KvLayout {
+    const int32_t* table;   // null: contiguous; else [B][nblk] physical block ids (device)
+    int nblk;               // logical blocks per sequence: ceil(C / P)
+    int P;                  // rows per block: a power of two >= 64
+    int shift;              // log2(P)
+    int C, Hkv;
+};
+
+__host__ __device__ inline int64_t kv_row(const KvLayout& L, int b, int h, int slot) {
+    if (!L.table) return ((int64_t)b * L.Hkv + h) * L.C + slot;
+    const int blk = L.table[(int64_t)b * L.nblk + (slot >> L.shift)];
+    return (((int64_t)blk * L.Hkv + h) << L.shift) + (slot & (L.P - 1));
+}
+
 // Host-pinned -> device staging of small per-call argument arrays (start
 // positions, chunk lengths, cuts, work lists).  Each slot is reused only after
 // the event recorded behind its consumers has completed.
@@ -66,6 +84,15 @@ struct Handle {
     unsigned* lane_ticket = nullptr;  // [B*H_kv] split counters of the fused decode step
     unsigned* step_ticket = nullptr;  // [L] CTA counters of device-length decode steps
 
+    // paged storage (cfg.block_rows > 0): one block table for every layer
+    int nblk = 0;                       // logical blocks per sequence
+    int nblocks = 0;                    // physical blocks in each layer's pool
+    std::vector<int32_t> table_h;       // [B][nblk] physical block or -1
+    int32_t* table_d = nullptr;         // device copy
+    bool table_dirty = false;           // table_h changed since the last upload
+    std::vector<int32_t> refcnt;        // [nblocks] sequences holding each block
+    std::vector<int32_t> free_blocks;   // stack of unused blocks
+
     // TMA descriptors over each layer's keys and values (bf16, d_h = 128):
     // 64-row boxes for decode, 128-row boxes for the suffix-chunk kernel
     std::vector<CUtensorMap> tmap_k, tmap_v, tmap_k128, tmap_v128;
@@ -102,6 +129,18 @@ struct Handle {
     char* V_layer(int l) const { return (char*)V + (size_t)l * layer_elems * elem_size; }
     int32_t* pos_layer(int l) const { return positions + (size_t)l * cfg.batch * cfg.capacity; }
     int32_t* len_layer(int l) const { return len_d + (size_t)l * cfg.batch; }
+    bool paged() const { return cfg.block_rows > 0; }
+    KvLayout layout() const {
+        KvLayout L{};
+        L.table = paged() ? table_d : nullptr;
+        L.nblk = nblk;
+        L.P = cfg.block_rows;
+        L.shift = 0;
+        while ((1 << L.shift) < L.P) ++L.shift;
+        L.C = cfg.capacity;
+        L.Hkv = cfg.heads_kv;
+        return L;
+    }
     int32_t* next_layer(int l) const { return next_d + (size_t)l * cfg.batch; }
 };
 
@@ -119,6 +158,7 @@ struct AppendLaunch {
     const float2* rope_f;    // the same table rounded to float32 (bf16 caches)
     uint32_t* err;
     int B, Hq, Hkv, S, C, d, max_positions;
+    KvLayout kv;             // where stored rows live
 };
 cudaError_t launch_rope_append(int dtype, const AppendLaunch& a, cudaStream_t s);
 
@@ -130,6 +170,7 @@ struct GenericAttendLaunch {
     void* out;               // [B,H_q,S,d] float or double
     int B, Hq, Hkv, S, C, d;
     int window;              // 0, or each row attends its `window` most recent slots
+    KvLayout kv;
 };
 cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaStream_t s);
 
@@ -145,6 +186,7 @@ struct DecodeLaunch {
     int B, Hq, Hkv, C, split_rows, max_splits;
     int out_bf16;
     int window;              // 0, or the query attends only its `window` most recent slots
+    KvLayout kv;             // where stored rows live (tiles of 64 rows never cross a block)
     // Fused step (append + attend + split merge + length commit in one launch).
     int fused;
     const __nv_bfloat16* q_in;           // [B,H_q,128] new queries, unrotated
@@ -181,6 +223,10 @@ struct CommitLayers { int32_t layer[kCommitMaxLayers]; int n; };
 cudaError_t launch_commit_layers(int32_t* len, int32_t* next, const CommitLayers& layers, int B, cudaStream_t s);
 cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                                     uint32_t* err, cudaStream_t s);
+// Copies whole blocks (src, dst) = pairs[i] of every layer's key and value pool.
+cudaError_t launch_copy_blocks(char* K, char* V, size_t layer_bytes, int layers, size_t block_bytes,
+                               const int2* pairs, int npairs, cudaStream_t s);
+cudaError_t launch_set_lengths(int32_t* len, int32_t* next, int layers, int B, int b, int value, cudaStream_t s);
 cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,
                              cudaStream_t s);
 
@@ -197,6 +243,7 @@ struct SuffixLaunch {
     int B, Hq, Hkv, S, C;
     int window;                  // 0, or each row attends its `window` most recent slots; the work
                                  // item's key tiles then start at tile (cut + 128 q_tile - window + 1) / 128
+    KvLayout kv;                 // paged: K/V tiles load as two 64-row boxes (tmK/tmV 64-row maps)
     float scale_log2;            // log2(e) / sqrt(d_h)
 };
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);

@@ -38,7 +38,7 @@ __device__ __forceinline__ void rope_one(const AppendLaunch& a, int kind, int b,
     using S = Storage<T>;
     const int pairs_per_row = a.d / 2;
     if (kind == 2) {
-        T* dst = (T*)a.V + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+        T* dst = (T*)a.V + kv_row(a.kv, b, h, slot) * a.d + 2 * P * c;
         *reinterpret_cast<Pack<T, P>*>(dst) = in;
         return;
     }
@@ -67,7 +67,7 @@ __device__ __forceinline__ void rope_one(const AppendLaunch& a, int kind, int b,
             }
         }
         if (kind == 1) {
-            T* dst = (T*)a.K + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+            T* dst = (T*)a.K + kv_row(a.kv, b, h, slot) * a.d + 2 * P * c;
             *reinterpret_cast<Pack<T, P>*>(dst) = ok;
             if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
         } else {
@@ -93,7 +93,7 @@ __device__ __forceinline__ void rope_one(const AppendLaunch& a, int kind, int b,
         Pack<T, P> o;
 #pragma unroll
         for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<T>(xr[e]);
-        T* dst = (T*)a.K + (((int64_t)b * a.Hkv + h) * a.C + slot) * a.d + 2 * P * c;
+        T* dst = (T*)a.K + kv_row(a.kv, b, h, slot) * a.d + 2 * P * c;
         *reinterpret_cast<Pack<T, P>*>(dst) = o;
         if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
     } else {

@@ -87,6 +87,38 @@ cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* 
     return cudaGetLastError();
 }
 
+// Copy-on-write of paged blocks: one CTA per (pair, layer, key/value), 16-byte chunks.
+__global__ void copy_blocks_kernel(char* K, char* V, size_t layer_bytes, size_t block_bytes, const int2* pairs,
+                                   int layers) {
+    const int pair = blockIdx.x / (2 * layers);
+    const int rem = blockIdx.x % (2 * layers);
+    char* pool = (rem & 1 ? V : K) + (size_t)(rem >> 1) * layer_bytes;
+    const int2 p = pairs[pair];
+    const uint4* src = (const uint4*)(pool + (size_t)p.x * block_bytes);
+    uint4* dst = (uint4*)(pool + (size_t)p.y * block_bytes);
+    for (size_t i = threadIdx.x; i < block_bytes / 16; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_copy_blocks(char* K, char* V, size_t layer_bytes, int layers, size_t block_bytes,
+                               const int2* pairs, int npairs, cudaStream_t s) {
+    if (npairs <= 0) return cudaSuccess;
+    copy_blocks_kernel<<<(unsigned)npairs * 2 * layers, 256, 0, s>>>(K, V, layer_bytes, block_bytes, pairs, layers);
+    return cudaGetLastError();
+}
+
+// Length and next position of sequence b in every layer (shared-prefix setup).
+__global__ void set_lengths_kernel(int32_t* len, int32_t* next, int layers, int B, int b, int value) {
+    const int l = blockIdx.x * blockDim.x + threadIdx.x;
+    if (l >= layers) return;
+    len[(int64_t)l * B + b] = value;
+    next[(int64_t)l * B + b] = value;
+}
+
+cudaError_t launch_set_lengths(int32_t* len, int32_t* next, int layers, int B, int b, int value, cudaStream_t s) {
+    set_lengths_kernel<<<(layers + 127) / 128, 128, 0, s>>>(len, next, layers, B, b, value);
+    return cudaGetLastError();
+}
+
 template <typename T>
 __global__ void nonfinite_kernel(const T* x, int64_t n, unsigned long long* first) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;

@@ -65,6 +65,7 @@ constexpr int THREADS = (2 + NSW) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_P0 = 384, COL_P1 = 448;
 constexpr float RESCALE_LOG2 = 8.0f;
+constexpr int kTileCache = 256;            // paged: key tiles whose row coordinates are staged in shared memory
 
 struct Bars {
     float red_max[2][WPS][BM]; // [tile parity][column part][row]: partial row maxima
@@ -77,11 +78,21 @@ struct Bars {
     uint64_t fin[4];           // [sub-partition]: final partial sums
     uint32_t tmem_base;
     int err;
+    int2 ty[kTileCache];       // paged: TMA row coordinates of the two halves of this item's key tiles
 };
 
 __device__ __forceinline__ void fail_wait(Bars* bars, uint32_t* err) {
     *(volatile int*)&bars->err = 1;
     atomicOr(err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+}
+
+// Pool row of a slot in paged storage; a slot past the sequence's blocks (the
+// second half of its last key tile) maps to rows -64..-1, where the TMA
+// load fills zeros (those keys are masked).
+__device__ __forceinline__ int paged_row(const KvLayout& L, int b, int h, int slot) {
+    const int j = slot >> L.shift;
+    const int blk = j < L.nblk ? L.table[(int64_t)b * L.nblk + j] : -1;
+    return blk < 0 ? -64 : ((blk * L.Hkv + h) << L.shift) + (slot & (L.P - 1));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -140,6 +151,13 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
+    // Paged storage: warp 0 looks up the pool rows of both 64-row halves of this item's
+    // key tiles once, in parallel, and stages them in shared memory, so the producers'
+    // path per tile is one shared load (tiles past the staged ones are looked up
+    // directly).
+    if (a.kv.table && warp == 0)
+        for (int e = lane; e < min(n, kTileCache); e += 32)
+            bars->ty[e] = make_int2(paged_row(a.kv, b, g, (j0 + e) * BN), paged_row(a.kv, b, g, (j0 + e) * BN + 64));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -150,7 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         // lane 0 streams Q and the K ring, lane 1 the V ring, so that the K
         // look-ahead never waits behind a V stage that is still being read.
         if (lane < 2) {
-            const int kvrow = (b * a.Hkv + g) * a.C;
+            const int kvrow = (b * a.Hkv + g) * a.C;   // contiguous storage
             const bool is_k = lane == 0;
             const int NS = is_k ? KST : VST;
             uint64_t* full = is_k ? bars->k_full : bars->v_full;
@@ -176,8 +194,21 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 }
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, TILE);
-                tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + (j0 + j) * BN, fb);
-                tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + (j0 + j) * BN, fb);
+                if (!a.kv.table) {
+                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + (j0 + j) * BN, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + (j0 + j) * BN, fb);
+                } else {
+                    // paged: the two 64-row halves of the tile, each inside one block
+                    // (64-row box map; same 128-byte-swizzled layout as one 128-row box)
+                    const int2 yy = j < kTileCache ? bars->ty[j]
+                                                   : make_int2(paged_row(a.kv, b, g, (j0 + j) * BN),
+                                                               paged_row(a.kv, b, g, (j0 + j) * BN + 64));
+                    const int ya = yy.x, yb = yy.y;
+                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, ya, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + 64 * 128), map, 0, yb, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, ya, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF + 64 * 128), map, 64, yb, fb);
+                }
                 issued = j + 1;
             }
             // Our own copies must have landed before the CTA's shared memory is released.

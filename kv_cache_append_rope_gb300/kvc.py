@@ -59,7 +59,8 @@ class KVCache:
     """A kvc_handle: per-layer [B, H_kv, C, d_h] key/value storage on one GPU."""
 
     def __init__(self, batch, heads_q, capacity, head_dim, layers=1, heads_kv=None, dtype="bf16",
-                 rope_base=10000.0, rope_max_positions=0, checked=False, device=0, window=0):
+                 rope_base=10000.0, rope_max_positions=0, checked=False, device=0, window=0,
+                 block_rows=0, blocks=0):
         cfg = L.kvc_config()
         cfg.batch, cfg.heads_q = batch, heads_q
         cfg.heads_kv = heads_q if heads_kv is None else heads_kv
@@ -70,6 +71,7 @@ class KVCache:
         cfg.checked = int(bool(checked))
         cfg.device = device
         cfg.window = window
+        cfg.block_rows, cfg.blocks = block_rows, blocks
         self._h = ctypes.c_void_p()
         L.check(L.lib.kvc_create_ex(ctypes.byref(cfg), ctypes.byref(self._h)))
         got = L.kvc_config()
@@ -155,16 +157,32 @@ class KVCache:
         self._check(L.lib.kvc_get_lengths(self._h, layer, ln, nx))
         return list(ln), list(nx)
 
+    def share_prefix(self, dst, src, rows, stream=None):
+        """kvc_share_prefix: sequence dst (empty) takes src's first rows by sharing its blocks."""
+        self._check(L.lib.kvc_share_prefix(self._h, dst, src, rows, _stream(stream)))
+
+    def block_table(self):
+        """kvc_block_table: (host block table [B, ceil(C/P)] as numpy int32, free blocks)."""
+        c = self.config
+        nblk = -(-c.capacity // c.block_rows)
+        table = np.zeros((c.batch, nblk), dtype=np.int32)
+        free = ctypes.c_int32()
+        self._check(L.lib.kvc_block_table(self._h, table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                          ctypes.byref(free)))
+        return table, free.value
+
     def sync_lengths(self):
         """kvc_sync_lengths: read the device lengths back into the host mirrors."""
         self._check(L.lib.kvc_sync_lengths(self._h))
 
     def storage(self, layer=0):
-        """Views of one layer's device storage: keys, values [B, H_kv, C, d_h], positions [B, C]."""
+        """Views of one layer's device storage: keys, values [B, H_kv, C, d_h] (paged: the pool
+        [blocks, H_kv, P, d_h]), positions [B, C]."""
         k, v, p = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
         self._check(L.lib.kvc_storage(self._h, layer, ctypes.byref(k), ctypes.byref(v), ctypes.byref(p)))
         c = self.config
-        shape = (c.batch, c.heads_kv, c.capacity, c.head_dim)
+        shape = ((c.blocks, c.heads_kv, c.block_rows, c.head_dim) if c.block_rows
+                 else (c.batch, c.heads_kv, c.capacity, c.head_dim))
         code = {0: "<u2", 1: "<f4", 2: "<f8"}[c.dtype]
         with torch.cuda.device(self.device):
             K = torch.as_tensor(_DeviceArray(k.value, shape, code), device=self.device)

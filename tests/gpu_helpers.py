@@ -18,8 +18,23 @@ def to_np(t):
 
 
 def storage_np(cache, layer=0):
+    """Stored keys and values as [B, H_kv, C, d_h] float64 and positions [B, C]; a paged
+    pool is gathered through the block table (slots without a block read as 0)."""
     K, V, P = cache.storage(layer)
-    return to_np(K), to_np(V), P.cpu().numpy()
+    K, V, P = to_np(K), to_np(V), P.cpu().numpy()
+    c = cache.config
+    if not c.block_rows:
+        return K, V, P
+    table, _ = cache.block_table()
+    out = []
+    for pool in (K, V):
+        x = np.zeros((c.batch, c.heads_kv, table.shape[1] * c.block_rows, c.head_dim))
+        for b in range(c.batch):
+            for j, blk in enumerate(table[b]):
+                if blk >= 0:
+                    x[b, :, j * c.block_rows:(j + 1) * c.block_rows] = pool[blk]
+        out.append(x[:, :, :c.capacity])
+    return out[0], out[1], P
 
 
 def device_tensor(a, dtype):

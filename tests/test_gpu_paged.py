@@ -1,0 +1,230 @@
+"""Paged key/value storage (block pool + block table) against the float64 oracle.
+
+[LCP5] "这一轮留下的工程判断" names blocked storage as the next step of prefix reuse
+and section "查询流程与缓存所有权" (step 4) keeps the reusable rows of a cached
+entry and computes only the rest.  With block_rows = P every layer stores rows in
+a pool of P-row blocks and one block table maps each sequence's logical blocks;
+kvc_share_prefix lets a sequence take another's prefix by sharing blocks, with
+copy-on-write when either writes into a shared block.  Every result must equal
+the contiguous layout's: outputs within 1e-12 / 1e-5 / 2e-2 of the oracle, stored
+rows (gathered through the block table), positions and lengths bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import TOL, device_tensor, need_gpu, storage_np, to_np
+from kv_cache_append_rope_gb300 import _lib as L
+from kv_cache_append_rope_gb300 import kvc
+from kv_cache_append_rope_gb300 import workloads as W
+from kv_cache_append_rope_gb300.kvc import KVCache, KVCError
+from oracle import attention as A
+from oracle.toy_decoder import ToyDecoder
+
+pytestmark = pytest.mark.gpu
+BASE = 10000.0
+
+
+def inputs(B, Hq, Hkv, T, D, dtype, seed):
+    return (device_tensor(W.normal_np((B, Hq, T, D), seed), dtype),
+            device_tensor(W.normal_np((B, Hkv, T, D), seed + 1), dtype),
+            device_tensor(W.normal_np((B, Hkv, T, D), seed + 2), dtype))
+
+
+def check_pool(cache, lengths):
+    """Every sequence holds exactly the blocks its length needs; no block is held twice."""
+    table, free = cache.block_table()
+    P = cache.config.block_rows
+    held = []
+    for b, n in enumerate(lengths):
+        need = -(-n // P)
+        assert (table[b, :need] >= 0).all() and (table[b, need:] == -1).all(), (b, table[b])
+        held += table[b, :need].tolist()
+    assert len(held) == len(set(held))
+    assert free == cache.config.blocks - len(held)
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,P,mode,window", [
+    ("bf16", 128, 8, 2, 64, "fused", 0),
+    ("bf16", 128, 8, 2, 256, "fused", 0),
+    ("bf16", 128, 32, 1, 64, "fused", 0),
+    ("bf16", 128, 8, 2, 64, "separate", 0),
+    ("bf16", 128, 8, 2, 64, "fused", 100),
+    ("f64", 16, 4, 2, 64, "generic", 0),
+])
+def test_paged_decode_matches_oracle(dtype, D, Hq, Hkv, P, mode, window):
+    need_gpu()
+    L0, steps = [0, 70, 333, 127], 4
+    B, T = len(L0), max(L0) + steps
+    qd, kd, vd = inputs(B, Hq, Hkv, T, D, dtype, 110)
+    q, k, v = to_np(qd), to_np(kd), to_np(vd)
+    cache = KVCache(B, Hq, 800, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE, window=window, block_rows=P)
+    if mode == "separate":
+        cache.set_option(L.OPT_DECODE_FUSED, 0)
+    # a longer prefill truncated back releases blocks in a scrambled order before the real prefix
+    cache.prefill_suffix(0, None, kd, vd, out=False)
+    cache.truncate([0, 3, 0, 1])
+    S = max(L0)
+    cache.truncate([0, 0, 0, 0])
+    cache.prefill_suffix(0, None, kd[:, :, :S].contiguous(), vd[:, :, :S].contiguous(), seqlen=L0, out=False)
+    idx = lambda i: torch.tensor([l + i for l in L0], device="cuda")
+    row = lambda x, i: x[torch.arange(B, device="cuda"), :, idx(i)][:, :, None, :].contiguous()
+    outs = [to_np(cache.append_attend(0, row(qd, i), row(kd, i), row(vd, i))) for i in range(steps)]
+    Ks, Vs, Ps = storage_np(cache)
+    worst = 0.0
+    for b in range(B):
+        n = L0[b] + steps
+        ref = A.decode_steps_reference(np.transpose(q[b, :, L0[b]:n], (1, 0, 2)), k[b, :, :n], v[b, :, :n],
+                                       L0[b], BASE, dtype, window=window)
+        worst = max(worst, np.abs(np.stack([o[b, :, 0] for o in outs]) - ref).max())
+        K, V = A.stored_rows(k[b, :, :n], v[b, :, :n], np.arange(n)[None], BASE, dtype)
+        np.testing.assert_array_equal(Ks[b, :, :n], K)
+        np.testing.assert_array_equal(Vs[b, :, :n], V)
+        assert Ps[b, :n].tolist() == list(range(n))
+    assert worst <= TOL[dtype], worst
+    check_pool(cache, [l + steps for l in L0])
+    cache.check()
+
+
+@pytest.mark.parametrize("dtype,D,kernel,P,window", [
+    ("bf16", 128, 2, 64, 0), ("bf16", 128, 2, 128, 0), ("bf16", 128, 2, 64, 300), ("bf16", 128, 1, 64, 0),
+    ("f32", 64, 1, 64, 0),
+])
+def test_paged_suffix_chunk_matches_full_recompute(dtype, D, kernel, P, window):
+    need_gpu()
+    T, cuts, Hq, Hkv = 1500, [1200, 37, 640], 4, 2
+    B = len(cuts)
+    qd, kd, vd = inputs(B, Hq, Hkv, T, D, dtype, 120)
+    q, k, v = to_np(qd), to_np(kd), to_np(vd)
+    cache = KVCache(B, Hq, T + 20, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE, window=window, block_rows=P)
+    cache.set_option(L.OPT_SUFFIX_KERNEL, kernel)
+    cache.prefill_suffix(0, qd, kd, vd, out=False)
+    cache.truncate(cuts)
+    check_pool(cache, cuts)
+    S = max(T - c for c in cuts)
+    sel = lambda x: torch.stack([torch.nn.functional.pad(x[b, :, cuts[b]:], (0, 0, 0, S - (T - cuts[b])))
+                                 for b in range(B)]).contiguous()
+    got = to_np(cache.prefill_suffix(0, sel(qd), sel(kd), sel(vd), seqlen=[T - c for c in cuts]))
+    Ks, Vs, _ = storage_np(cache)
+    for b in range(B):
+        ref = A.suffix_reference(q[b, :, cuts[b]:], k[b], v[b], np.arange(T), cuts[b], BASE, dtype, window=window)
+        assert np.abs(got[b, :, :T - cuts[b]] - ref).max() <= TOL[dtype], b
+        K, V = A.stored_rows(k[b], v[b], np.arange(T)[None], BASE, dtype)
+        np.testing.assert_array_equal(Ks[b, :, :T], K)
+        np.testing.assert_array_equal(Vs[b, :, :T], V)
+    check_pool(cache, [T] * B)
+    cache.check()
+
+
+def test_pool_exhaustion_is_rejected_before_any_change():
+    need_gpu()
+    qd, kd, vd = inputs(2, 4, 4, 300, 128, "bf16", 130)
+    cache = KVCache(2, 4, 512, 128, block_rows=64, blocks=6)
+    cache.prefill_suffix(0, None, kd[:, :, :128].contiguous(), vd[:, :, :128].contiguous(), out=False)  # 4 blocks
+    before = (cache.get_lengths(0), cache.block_table())
+    with pytest.raises(KVCError) as e:
+        cache.prefill_suffix(0, None, kd[:, :, 128:300].contiguous(), vd[:, :, 128:300].contiguous(), out=False)
+    assert e.value.name == "KVC_ERR_FULL"
+    after = (cache.get_lengths(0), cache.block_table())
+    assert before[0] == after[0] and (before[1][0] == after[1][0]).all() and before[1][1] == after[1][1] == 2
+    cache.check()
+
+
+def test_shared_prefix_with_copy_on_write():
+    need_gpu()
+    B, Hq, Hkv, D, P = 3, 8, 2, 128, 64
+    T = 310
+    qd, kd, vd = inputs(B, Hq, Hkv, T, D, "bf16", 140)
+    q, k, v = to_np(qd), to_np(kd), to_np(vd)
+    # sequence 1 shares sequence 0's first 200 rows; its own rows follow from k/v row 200 of sequence 1
+    cache = KVCache(B, Hq, 512, D, heads_kv=Hkv, rope_base=BASE, block_rows=P)
+    cache.prefill_suffix(0, None, kd[:, :, :300].contiguous(), vd[:, :, :300].contiguous(), seqlen=[300, 0, 0],
+                         out=False)
+    free0 = cache.block_table()[1]
+    cache.share_prefix(1, 0, 200)
+    table, free = cache.block_table()
+    assert free == free0 and (table[1, :4] == table[0, :4]).all() and (table[1, 4:] == -1).all()
+    assert cache.get_lengths(0) == ([300, 200, 0], [300, 200, 0])
+    with pytest.raises(KVCError):
+        cache.share_prefix(1, 0, 10)                      # sequence 1 is no longer empty
+    # history of each sequence as the oracle sees it
+    hist_k = [k[0, :, :300], k[0, :, :200], np.zeros((Hkv, 0, D))]
+    hist_v = [v[0, :, :300], v[0, :, :200], np.zeros((Hkv, 0, D))]
+    L0 = [300, 200, 0]
+    outs = []
+    for i in range(4):
+        src = [300 + i, 200 + i, i]                       # row of k/v used as each sequence's new row
+        pick = lambda x: x[torch.arange(B, device="cuda"), :, torch.tensor(src, device="cuda")][:, :, None].contiguous()
+        outs.append(to_np(cache.append_attend(0, pick(qd), pick(kd), pick(vd))))
+        for b in range(B):
+            hist_k[b] = np.concatenate([hist_k[b], k[b, :, src[b]:src[b] + 1]], axis=1)
+            hist_v[b] = np.concatenate([hist_v[b], v[b, :, src[b]:src[b] + 1]], axis=1)
+    table, free = cache.block_table()
+    assert table[1, 3] != table[0, 3]                     # sequence 1 copied the shared partial block
+    assert (table[1, :3] == table[0, :3]).all()           # full blocks stay shared
+    Ks, Vs, _ = storage_np(cache)
+    for b in range(B):
+        n = L0[b] + 4
+        qs = np.stack([q[b, :, (300, 200, 0)[b] + i] for i in range(4)])
+        ref = A.decode_steps_reference(qs, hist_k[b], hist_v[b], L0[b], BASE, "bf16")
+        assert np.abs(np.stack([o[b, :, 0] for o in outs]) - ref).max() <= TOL["bf16"], b
+        K, V = A.stored_rows(hist_k[b], hist_v[b], np.arange(n)[None], BASE, "bf16")
+        np.testing.assert_array_equal(Ks[b, :, :n], K)
+        np.testing.assert_array_equal(Vs[b, :, :n], V)
+    cache.check()
+
+
+@pytest.mark.parametrize("seed", [7, 11, 23])
+def test_branch_reuse_by_block_sharing(seed):
+    """[LCP5]: a new query that shares 5 leading ids with a cached history reuses those rows
+    through shared blocks; its continuation equals the uncached forward, and the cached
+    history (whose partial block the new sequence writes into) is unchanged."""
+    need_gpu()
+    E, Wl = W.toy_decoder_weights(seed)
+    model = ToyDecoder(E, Wl, rope_base=BASE)
+    cached = list(range(1, 9))
+    query = [1, 2, 3, 4, 5, 20, 21, 22, 9, 10, 11, 12]
+    t = lambda a: torch.from_numpy(np.asarray(a)).to("cuda", torch.float64)
+    Et, Wt = t(E), [tuple(t(w) for w in layer) for layer in Wl]
+    cache = KVCache(2, 1, 16, 16, layers=2, dtype="f64", rope_base=BASE, block_rows=64)
+
+    def chunk(b, ids):
+        h = Et[torch.as_tensor(ids, device="cuda")]
+        for layer, (Wq, Wk, Wv, Wo) in enumerate(Wt):
+            x = [(h @ w) for w in (Wq, Wk, Wv)]
+            full = [torch.zeros((2, 1, len(ids), 16), dtype=torch.float64, device="cuda") for _ in range(3)]
+            for f, y in zip(full, x):
+                f[b, 0] = y
+            a = cache.prefill_suffix(layer, *full, seqlen=[len(ids) if i == b else 0 for i in range(2)])
+            h = h + torch.tanh(a[b, 0] @ Wo)
+        return to_np(h)
+
+    chunk(0, cached)
+    before = [storage_np(cache, l) for l in range(2)]
+    cut = kvc.lcp(cached, query)
+    assert cut == 5
+    cache.share_prefix(1, 0, cut)
+    h = chunk(1, query[cut:])
+    full, _ = model.forward_full(query)
+    assert np.abs(h - full[cut:]).max() <= 1e-12
+    for l in range(2):
+        after = storage_np(cache, l)
+        np.testing.assert_array_equal(before[l][0][0, :, :8], after[0][0, :, :8])   # sequence 0 untouched
+        np.testing.assert_array_equal(before[l][1][0, :, :8], after[1][0, :, :8])
+    assert cache.get_lengths(1) == ([8, 12], [8, 12])
+    cache.check()
+
+
+def test_paged_refusals():
+    need_gpu()
+    contiguous = KVCache(2, 4, 64, 128)
+    with pytest.raises(KVCError) as e:
+        contiguous.share_prefix(1, 0, 0)
+    assert e.value.name == "KVC_ERR_CONFIG"
+    paged = KVCache(2, 4, 64, 128, block_rows=64)
+    with pytest.raises(KVCError) as e:
+        paged.set_option(L.OPT_DEVICE_LENGTHS, 1)
+    assert e.value.name == "KVC_ERR_CONFIG"
+    with pytest.raises(KVCError) as e:
+        paged.share_prefix(1, 0, 5)                       # sequence 0 holds no rows
+    assert e.value.name == "KVC_ERR_CUT"

@@ -24,7 +24,7 @@ def test_every_declared_symbol_is_exported(kvc_lib):
     for n in names:
         assert hasattr(kvc_lib.lib, n), n
     assert set(names) == set(kvc_lib.EXPORTS)
-    assert kvc_lib.lib.kvc_abi_version() == 2
+    assert kvc_lib.lib.kvc_abi_version() == 3
 
 
 def test_status_strings(kvc_lib):
@@ -52,6 +52,10 @@ def _create(kvc_lib, **kw):
     (dict(heads_q=3, heads_kv=2), "KVC_ERR_CONFIG"),
     (dict(head_dim=3), "KVC_ERR_CONFIG"),
     (dict(dtype=7), "KVC_ERR_CONFIG"),
+    (dict(window=-1), "KVC_ERR_CONFIG"),
+    (dict(block_rows=32), "KVC_ERR_CONFIG"),
+    (dict(block_rows=192), "KVC_ERR_CONFIG"),
+    (dict(block_rows=64, blocks=-1), "KVC_ERR_CONFIG"),
     (dict(batch=2**30, heads_kv=2**30, heads_q=2**30, capacity=2**30, head_dim=256, layers=2**30), None),
 ])
 def test_create_rejections_before_any_cuda_call(kvc_lib, kw, code):
