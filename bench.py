@@ -66,6 +66,8 @@ def parse():
                    choices=["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix", "all"])
     p.add_argument("--block-rows", type=int, default=0,
                    help="paged storage with blocks of this many rows (a multiple of 64); 0 = contiguous")
+    p.add_argument("--split-rows", type=int, default=0,
+                   help="decode: key rows per split (a multiple of 64); 0 = the library's choice")
     p.add_argument("--graph", action="store_true",
                    help="decode workloads: lengths kept on the device, each bench step's decode calls "
                         "captured once in a CUDA graph and replayed")
@@ -477,6 +479,8 @@ def run_ours(args, name, world, rank, local):
     hbm, tflops, peak_kind = peaks()
     bench = make_bench(name, device, args.batch, args.graph, args.block_rows)
     cache = bench.cache
+    if args.split_rows:
+        cache.set_option(L.OPT_DECODE_SPLIT_ROWS, args.split_rows)
     for _ in range(args.warmup):
         bench.step()
     torch.cuda.synchronize(device)

@@ -954,15 +954,20 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     const bool use_tc = out && tc_ok && !h->opt_force_generic && h->opt_suffix_kernel != 1;
     std::vector<int4> work;
     if (use_tc) {
+        // one item per (sequence, query head, pair of 128-row query tiles); its weight is
+        // the number of (query tile, key tile) products, key tiles from the window start
+        // (tile 0 without a window) to the tile of the query tile's last row
+        const int W = h->cfg.window;
+        auto tiles_of = [&](int b, int qt) {
+            if (qt * 128 >= sl_h[b]) return 0;
+            const int q_end = std::min(qt * 128 + 128, sl_h[b]);
+            const int j0 = W > 0 ? std::max(0, lenh[b] + qt * 128 - W + 1) / 128 : 0;
+            return (lenh[b] + q_end + 127) / 128 - j0;
+        };
         for (int b = 0; b < B; ++b)
             for (int hq = 0; hq < Hq; ++hq)
-                for (int qt = 0; qt * 128 < sl_h[b]; ++qt) {
-                    const int q_end = std::min(qt * 128 + 128, sl_h[b]);
-                    // key tiles j0 .. (last row's slot) / 128; j0 > 0 only with a sliding window
-                    const int W = h->cfg.window;
-                    const int j0 = W > 0 ? std::max(0, lenh[b] + qt * 128 - W + 1) / 128 : 0;
-                    work.push_back(make_int4(b, hq, qt, (lenh[b] + q_end + 127) / 128 - j0));
-                }
+                for (int qp = 0; qp * 256 < sl_h[b]; ++qp)
+                    work.push_back(make_int4(b, hq, qp, tiles_of(b, 2 * qp) + tiles_of(b, 2 * qp + 1)));
         // Group the query tiles of each (sequence, head) so they stream its K/V together
         // (L2 reuse); groups by total work, longest first; inside a group longest first.
         std::vector<int64_t> gw((size_t)B * Hq, 0);

@@ -8,37 +8,42 @@
 // committing the append" fixes the score scale 1/sqrt(d_h) and the
 // max-subtracted softmax.  With a sliding window of W slots ([LCP5]
 // "为什么滑窗部分命中必须回退") row cut + i sees slots cut + i - W + 1 .. cut + i:
-// its key tiles start later and the first ones are masked from below too.  A long suffix is a dense Q K^T / P V contraction,
-// which is why this kernel uses tcgen05 tiles.
+// its key tiles start later and the first ones are masked from below too.
+// A long suffix is a dense Q K^T / P V contraction, which is why this kernel
+// uses tcgen05 tiles.
 //
-// One CTA per work item (sequence b, query head h, 128-row query tile qt).
-// Items are grouped by (b, h) -- the query tiles of one head launch together
-// and walk its K/V tiles in step, so each tile comes from DRAM once and from
-// L2 for the rest -- and the groups are ordered by total work, longest first.  Query row i (slot cut + i) attends key slots
-// 0 .. cut + i; key tiles are 128 slots, the last ones masked element-wise.
+// One CTA per work item (sequence b, query head h, pair of 128-row query tiles
+// A = 2p and B = 2p + 1).  Both query tiles use every key/value tile the CTA
+// loads, which halves the key/value bytes each SM takes in per flop (with one
+// query tile per CTA the kernel was bound by that feed).  Items are grouped by
+// (b, h) -- the tile pairs of one head launch together and walk its K/V tiles
+// in step, so each tile comes from DRAM once and from L2 for the rest -- and
+// the groups are ordered by total work, longest first.  Query row i (slot
+// cut + i) attends key slots 0 .. cut + i; key tiles are 128 slots, the
+// diagonal ones masked element-wise.
 //
 // Warp roles (320 threads):
-//   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 the
-//             rotated Q tile once and K tiles into a 3-stage ring, lane 1 V
-//             tiles into a 2-stage ring.
+//   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 both Q
+//             tiles once and K tiles into a 2-stage ring, lane 1 V tiles into
+//             a 2-stage ring.
 //   warp 1    TMEM allocator (512 columns) and, on one elected thread, the MMA
-//             issuer: S = Q K^T into one of two TMEM S buffers (so the next
-//             tile's QK^T overlaps the current softmax), then O += P V into
-//             the TMEM O accumulator with P read from tensor memory, each
-//             completion signalled with tcgen05.commit on an mbarrier.
-// Tensor memory: S0, S1, O (128 columns each), P0, P1 (64 columns each).
-//   warps 2-9 softmax, two warps per TMEM sub-partition, each thread one
-//             query row (= TMEM lane) and one half of its 128 columns, the
-//             pair exchanging row maxima through shared memory (an mbarrier
-//             of 64 arrivals): tcgen05.ld of the S half-row, causal mask,
-//             running max in log2 units, O rescaled through
-//             TMEM only when the max grows by more than 2^8 (the final
-//             division by the running sum makes the stale max exact), P
-//             computed in registers while the previous tile's PV runs, then
-//             written as packed bf16 into one of two 64-column tensor-memory
-//             P buffers (tcgen05.st), from which the PV MMA reads its A
-//             operand, and the normalised O row written to global memory.
-// Every mbarrier wait is bounded (DEV_ERR_WAIT_TIMEOUT), the MMA thread waits
+//             issuer.  Per key tile j: O_A += P_A V_j, then S_A = Q_A K_{j+1}^T,
+//             then O_B += P_B V_j, then S_B = Q_B K_{j+1}^T -- so that while one
+//             query tile's softmax runs, the tensor pipe works for the other
+//             (S = QK^T in the SS form, PV in the TS form with P read from tensor
+//             memory); completions are signalled with tcgen05.commit on mbarriers.
+// Tensor memory: S_A, S_B (128 columns each), O_A, O_B (128 each); P_X, packed
+//             bf16, overwrites the first 64 columns of S_X once the softmax has
+//             read S_X, and the next S_X = Q_X K^T is issued after the PV that
+//             reads P_X (the MMAs of one thread execute in order).
+//   warps 2-5 softmax of tile A, warps 6-9 of tile B: one thread per query row
+//             (= TMEM lane of its sub-partition) owning the whole 128-column row
+//             -- no exchange between warps: tcgen05.ld of S, causal (and
+//             window) mask, running max in log2 units, O rescaled through TMEM
+//             only when the max grows by more than 2^8 (the final division by
+//             the running sum makes the stale max exact), P written with
+//             tcgen05.st, then the normalised O row stored to global memory.
+// Every mbarrier wait is bounded (DEV_ERR_WAIT_TIMEOUT); the MMA thread waits
 // for its own last commit and the TMA thread for its own copies before the
 // allocator warp frees the tensor memory.
 #include <cuda.h>
@@ -51,35 +56,32 @@ namespace kvc {
 namespace {
 
 constexpr int BM = 128, BN = 128, D = 128;
+constexpr int QT = 2;                      // query tiles per CTA sharing each key/value tile
 constexpr int HALF = BM * 128;             // 128 rows x 64 bf16 (one TMA box)
 constexpr int TILE = 2 * HALF;             // 128 rows x 128 bf16
-constexpr int KST = 3, VST = 2;            // K and V ring stages (K is needed first)
+constexpr int KST = 2, VST = 2;            // K and V ring stages
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;
+constexpr int OFF_K = OFF_Q + QT * TILE;
 constexpr int OFF_V = OFF_K + KST * TILE;
 constexpr int OFF_BAR = OFF_V + VST * TILE;
-constexpr int SMEM_BYTES = OFF_BAR + 8192 + 1024;
-constexpr int WPS = 2;                     // softmax warps per TMEM sub-partition
-constexpr int NSW = 4 * WPS;               // softmax warps
+constexpr int SMEM_BYTES = OFF_BAR + 4096 + 1024;
+constexpr int NSW = 4 * QT;                // softmax warps: one per TMEM sub-partition per query tile
 constexpr int THREADS = (2 + NSW) * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_P0 = 384, COL_P1 = 448;
+constexpr uint32_t COL_S = 0, COL_O = 256; // S_X at 128 X, O_X at 256 + 128 X
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr int kTileCache = 256;            // paged: key tiles whose row coordinates are staged in shared memory
 
 struct Bars {
-    float red_max[2][WPS][BM]; // [tile parity][column part][row]: partial row maxima
-    float red_sum[WPS][BM];    // [column part][row]: partial row sums
     uint64_t q_full;
     uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full[2], pv_done[2], mma_done;
-    uint64_t xchg[4][2];       // [sub-partition][tile parity]: the two softmax warps of a row block
-    uint64_t fin[4];           // [sub-partition]: final partial sums
+    uint64_t s_full[QT], p_full[QT];
+    uint64_t o_done;
     uint32_t tmem_base;
     int err;
     int2 ty[kTileCache];       // paged: TMA row coordinates of the two halves of this item's key tiles
 };
+static_assert(sizeof(Bars) <= 4096, "barrier block");
 
 __device__ __forceinline__ void fail_wait(Bars* bars, uint32_t* err) {
     *(volatile int*)&bars->err = 1;
@@ -106,6 +108,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const u
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
 }
 
+// Key tiles [lo, hi) that query tile qt of a sequence reads (empty past its rows).
+__device__ __forceinline__ void tile_range(int qt, int cut, int rows, int window, int& lo, int& hi) {
+    const int r0 = qt * BM;
+    if (r0 >= rows) {
+        lo = hi = 0;
+        return;
+    }
+    const int q_end = min(r0 + BM, rows);
+    lo = window > 0 ? max(0, cut + r0 - window + 1) / BN : 0;
+    hi = (cut + q_end - 1) / BN + 1;
+}
+
 __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_constant__ SuffixLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -114,13 +128,16 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     const int lane = threadIdx.x & 31;
 
     const int4 w = a.work[blockIdx.x];
-    const int b = w.x, h = w.y, qt = w.z, n = w.w;
+    const int b = w.x, h = w.y, qp = w.z;
     const int g = h / (a.Hq / a.Hkv);
     const int cut = a.slot0[b];
     const int rows_b = a.seqlen[b];
-    // first key tile: 0, or with a sliding window the tile holding the earliest slot
-    // any row of this query tile sees (its first row's slot - window + 1)
-    const int j0 = a.window > 0 ? max(0, cut + qt * BM - a.window + 1) / BN : 0;
+    int jlo[QT], jhi[QT];
+#pragma unroll
+    for (int X = 0; X < QT; ++X) tile_range(QT * qp + X, cut, rows_b, a.window, jlo[X], jhi[X]);
+    // the item walks key tiles j_first .. j_first + n - 1 (tile A is never empty; B may be)
+    const int j_first = jlo[0];
+    const int n = max(jhi[0], jhi[1]) - j_first;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
@@ -132,18 +149,11 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             mbar_init(smem_u32(&bars->v_full[s]), 1);
             mbar_init(smem_u32(&bars->v_empty[s]), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&bars->s_full[s]), 1);
-            mbar_init(smem_u32(&bars->s_free[s]), NSW);
-            mbar_init(smem_u32(&bars->p_full[s]), NSW);
-            mbar_init(smem_u32(&bars->pv_done[s]), 1);
+        for (int X = 0; X < QT; ++X) {
+            mbar_init(smem_u32(&bars->s_full[X]), 1);
+            mbar_init(smem_u32(&bars->p_full[X]), 4);
         }
-        mbar_init(smem_u32(&bars->mma_done), 1);
-        for (int q = 0; q < 4; ++q) {
-            mbar_init(smem_u32(&bars->xchg[q][0]), 32 * WPS);
-            mbar_init(smem_u32(&bars->xchg[q][1]), 32 * WPS);
-            mbar_init(smem_u32(&bars->fin[q]), 32 * WPS);
-        }
+        mbar_init(smem_u32(&bars->o_done), 1);
         bars->err = 0;
         fence_mbar_init();
     }
@@ -157,7 +167,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     // directly).
     if (a.kv.table && warp == 0)
         for (int e = lane; e < min(n, kTileCache); e += 32)
-            bars->ty[e] = make_int2(paged_row(a.kv, b, g, (j0 + e) * BN), paged_row(a.kv, b, g, (j0 + e) * BN + 64));
+            bars->ty[e] = make_int2(paged_row(a.kv, b, g, (j_first + e) * BN),
+                                    paged_row(a.kv, b, g, (j_first + e) * BN + 64));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -165,8 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // lane 0 streams Q and the K ring, lane 1 the V ring, so that the K
-        // look-ahead never waits behind a V stage that is still being read.
+        // lane 0 streams both Q tiles and the K ring, lane 1 the V ring, so that the
+        // K look-ahead never waits behind a V stage that is still being read.
         if (lane < 2) {
             const int kvrow = (b * a.Hkv + g) * a.C;   // contiguous storage
             const bool is_k = lane == 0;
@@ -179,11 +190,16 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             uint32_t qb = 0;
             if (is_k) {
                 prefetch_tmap(&a.tmQ);
-                const int qrow = (b * a.Hq + h) * a.S + qt * BM;
                 qb = smem_u32(&bars->q_full);
-                mbar_arrive_expect_tx(qb, TILE);
-                tma_load_2d(smem_u32(smem + OFF_Q), &a.tmQ, 0, qrow, qb);
-                tma_load_2d(smem_u32(smem + OFF_Q + HALF), &a.tmQ, 64, qrow, qb);
+                mbar_arrive_expect_tx(qb, QT * TILE);
+#pragma unroll
+                for (int X = 0; X < QT; ++X) {
+                    // rows past the chunk belong to the next head or lie outside the map
+                    // (filled with zeros); their results are never stored
+                    const int qrow = (b * a.Hq + h) * a.S + (QT * qp + X) * BM;
+                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE), &a.tmQ, 0, qrow, qb);
+                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE + HALF), &a.tmQ, 64, qrow, qb);
+                }
             }
             int issued = 0;
             for (int j = 0; j < n && !*(volatile int*)&bars->err; ++j) {
@@ -195,19 +211,18 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, TILE);
                 if (!a.kv.table) {
-                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + (j0 + j) * BN, fb);
-                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + (j0 + j) * BN, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, kvrow + (j_first + j) * BN, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, kvrow + (j_first + j) * BN, fb);
                 } else {
                     // paged: the two 64-row halves of the tile, each inside one block
                     // (64-row box map; same 128-byte-swizzled layout as one 128-row box)
                     const int2 yy = j < kTileCache ? bars->ty[j]
-                                                   : make_int2(paged_row(a.kv, b, g, (j0 + j) * BN),
-                                                               paged_row(a.kv, b, g, (j0 + j) * BN + 64));
-                    const int ya = yy.x, yb = yy.y;
-                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, ya, fb);
-                    tma_load_2d(smem_u32(ring + s * TILE + 64 * 128), map, 0, yb, fb);
-                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, ya, fb);
-                    tma_load_2d(smem_u32(ring + s * TILE + HALF + 64 * 128), map, 64, yb, fb);
+                                                   : make_int2(paged_row(a.kv, b, g, (j_first + j) * BN),
+                                                               paged_row(a.kv, b, g, (j_first + j) * BN + 64));
+                    tma_load_2d(smem_u32(ring + s * TILE), map, 0, yy.x, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + 64 * 128), map, 0, yy.y, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF), map, 64, yy.x, fb);
+                    tma_load_2d(smem_u32(ring + s * TILE + HALF + 64 * 128), map, 64, yy.y, fb);
                 }
                 issued = j + 1;
             }
@@ -221,197 +236,197 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-            const uint32_t q_s = smem_u32(smem + OFF_Q);
             bool ok = mbar_wait_bounded(smem_u32(&bars->q_full), 0, a.err);
             if (!ok) fail_wait(bars, a.err);
             tc_fence_after();
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j & 1, ks = j % KST;
-                if (!mbar_wait_bounded(smem_u32(&bars->k_full[ks]), (j / KST) & 1, a.err)) return false;
-                if (j >= 2 && !mbar_wait_bounded(smem_u32(&bars->s_free[s]), ((j >> 1) - 1) & 1, a.err)) return false;
-                tc_fence_after();
+            auto active = [&](int X, int jj) { return jj >= jlo[X] && jj < jhi[X]; };
+            // S_X = Q_X K^T from K stage ks
+            auto issue_qk = [&](int X, int ks) {
+                const uint32_t q_s = smem_u32(smem + OFF_Q + X * TILE);
                 const uint32_t k_s = smem_u32(smem + OFF_K + ks * TILE);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-                    tc_mma_ss(tmem + (s ? COL_S1 : COL_S0), smem_desc_sw128(q_s + off, 16, 1024),
+                    tc_mma_ss(tmem + COL_S + X * 128, smem_desc_sw128(q_s + off, 16, 1024),
                               smem_desc_sw128(k_s + off, 16, 1024), idesc_qk, kk > 0);
                 }
-                tc_commit(smem_u32(&bars->s_full[s]));
-                tc_commit(smem_u32(&bars->k_empty[ks]));
-                return true;
+                tc_commit(smem_u32(&bars->s_full[X]));
             };
-            if (ok) ok = issue_qk(0);
+            int pv_count[QT] = {0, 0};
+            if (ok) {
+                if (!mbar_wait_bounded(smem_u32(&bars->k_full[0]), 0, a.err)) ok = false;
+                tc_fence_after();
+                for (int X = 0; ok && X < QT; ++X)
+                    if (active(X, j_first)) issue_qk(X, 0);
+                if (ok) tc_commit(smem_u32(&bars->k_empty[0]));
+            }
             for (int j = 0; ok && j < n; ++j) {
-                if (j + 1 < n && !(ok = issue_qk(j + 1))) break;
-                const int s = j & 1, vs = j % VST;
-                if (!mbar_wait_bounded(smem_u32(&bars->p_full[s]), (j >> 1) & 1, a.err) ||
-                    !mbar_wait_bounded(smem_u32(&bars->v_full[vs]), (j / VST) & 1, a.err)) {
+                const int jj = j_first + j, vs = j % VST;
+                const bool next = j + 1 < n;
+                const int ks1 = (j + 1) % KST;
+                if (!mbar_wait_bounded(smem_u32(&bars->v_full[vs]), (j / VST) & 1, a.err) ||
+                    (next && !mbar_wait_bounded(smem_u32(&bars->k_full[ks1]), ((j + 1) / KST) & 1, a.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t v_s = smem_u32(smem + OFF_V + vs * TILE);
-                const uint32_t p_t = tmem + (s ? COL_P1 : COL_P0);
+                for (int X = 0; ok && X < QT; ++X) {
+                    if (active(X, jj)) {
+                        if (!mbar_wait_bounded(smem_u32(&bars->p_full[X]), pv_count[X] & 1, a.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // A = P from tensor memory (16 keys = 8 columns per step),
-                    // B = V (rows = keys, contiguous head dims: MN-major)
-                    tc_mma_ts(tmem + COL_O, p_t + kk * 8, smem_desc_sw128(v_s + kk * 16 * 128, HALF, 1024),
-                              idesc_pv, (j > 0 || kk > 0));
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // A = P_X from tensor memory (16 keys = 8 columns per step),
+                            // B = V (rows = keys, contiguous head dims: MN-major)
+                            tc_mma_ts(tmem + COL_O + X * 128, tmem + COL_S + X * 128 + kk * 8,
+                                      smem_desc_sw128(v_s + kk * 16 * 128, HALF, 1024), idesc_pv,
+                                      (pv_count[X] > 0 || kk > 0));
+                        }
+                        pv_count[X] += 1;
+                    }
+                    // the next S_X overwrites P_X: issued after the PV that reads it
+                    if (next && active(X, jj + 1)) issue_qk(X, ks1);
                 }
-                tc_commit(smem_u32(&bars->pv_done[s]));
+                if (!ok) break;
                 tc_commit(smem_u32(&bars->v_empty[vs]));
+                if (next) tc_commit(smem_u32(&bars->k_empty[ks1]));
             }
             if (!ok) fail_wait(bars, a.err);
-            // every MMA issued by this thread completes before the tensor memory is freed
-            tc_commit(smem_u32(&bars->mma_done));
-            mbar_wait_bounded(smem_u32(&bars->mma_done), 0);  // no abort: the MMAs always finish
+            // every MMA issued by this thread completes before O is read and the tensor memory freed
+            tc_commit(smem_u32(&bars->o_done));
+            mbar_wait_bounded(smem_u32(&bars->o_done), 0);  // no abort: the MMAs always finish
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its sub-partition); the
-        // WPS warps of a sub-partition take consecutive column parts of those rows.
-        constexpr int HC = BN / WPS;                 // columns per warp
+        // Warps 2-5 take query tile A, 6-9 tile B; warp w reads TMEM lanes
+        // 32 * (w % 4) .. + 31, one query row per thread.
+        const int X = (warp - 2) >> 2;
         const int sub = warp & 3;
-        const int half = (warp - 2) >> 2;            // column part
         const int row = sub * 32 + lane;             // query row inside the tile = TMEM lane
+        const int qt = QT * qp + X;
         const int i = qt * BM + row;
         const int qslot = cut + i;
         const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
+        const uint32_t s_addr = lane_addr + COL_S + X * 128;
+        const uint32_t o_addr = lane_addr + COL_O + X * 128;
         const float sl2 = a.scale_log2;
+        const int tile_slot0 = cut + qt * BM;        // slot of the tile's first row
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int s = j & 1;
-            if (!warp_wait(smem_u32(&bars->s_full[s]), (j >> 1) & 1, a.err)) {
+        int c = 0;
+        for (int jj = jlo[X]; jj < jhi[X]; ++jj, ++c) {
+            if (!warp_wait(smem_u32(&bars->s_full[X]), c & 1, a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[HC];
-            const uint32_t s_col = (s ? COL_S1 : COL_S0) + half * HC;
-#pragma unroll
-            for (int c = 0; c < HC / 32; ++c) tmem_ld32(lane_addr + s_col + c * 32, x + c * 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[s]));
-
-            const int kbase = (j0 + j) * BN + half * HC;
+            // The row is read in two 64-column halves, twice (maximum, then exponentials),
+            // which keeps a thread's registers within the 168 that 10 warps leave it.
+            constexpr int HC = BN / 2;
+            const int kbase = jj * BN;
             // causal mask (keys after the row's slot) on diagonal tiles; with a window also
             // the keys before slot - window + 1 on the first tiles
-            const bool past_window = a.window > 0 && kbase < cut + qt * BM + BM - a.window;
-            if (kbase + HC - 1 > cut + qt * BM || past_window) {
-                const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
+            const bool past_window = a.window > 0 && kbase < tile_slot0 + BM - a.window;
+            const bool masked = kbase + BN - 1 > tile_slot0 || past_window;
+            const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
+            float x[HC];
+            auto load_half = [&](int hf) {
 #pragma unroll
-                for (int c = 0; c < HC; ++c) x[c] = (kbase + c > qslot || kbase + c < klo) ? -INFINITY : x[c];
-            }
-            // row maximum over this part (8 independent chains of 3-input maxima),
-            // then over the other parts of the same rows
+                for (int q = 0; q < HC / 32; ++q) tmem_ld32(s_addr + hf * HC + q * 32, x + q * 32);
+                tmem_wait_ld();
+                if (masked) {
+                    const int kb = kbase + hf * HC;
+#pragma unroll
+                    for (int e = 0; e < HC; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
+                }
+            };
+            // row maximum (8 independent chains of 3-input maxima)
             float m8[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) m8[q] = x[q];
+            for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
 #pragma unroll
-            for (int c = 8; c + 16 <= HC; c += 16)
+            for (int hf = 0; hf < 2; ++hf) {
+                load_half(hf);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[c + q], x[c + 8 + q]);
-            if constexpr ((HC - 8) % 16 != 0) {
+                for (int e = 0; e + 16 <= HC; e += 16)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) m8[q] = fmaxf(m8[q], x[HC - 8 + q]);
+                    for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
             }
-            float mpart = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            bars->red_max[s][half][row] = mpart;
-            mbar_arrive(smem_u32(&bars->xchg[sub][s]));
-            if (!warp_wait(smem_u32(&bars->xchg[sub][s]), (j >> 1) & 1, a.err)) {
-                ok = false;
-                break;
-            }
-            float mx = mpart;
-#pragma unroll
-            for (int q = 0; q < WPS; ++q)
-                if (q != half) mx = fmaxf(mx, bars->red_max[s][q][row]);
+            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             const float m_tile = mx * sl2;
-            const bool grow = m_tile > m_run + RESCALE_LOG2 || (j == 0);
+            const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
             const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
-            if (grow && j > 0 && m_run > -INFINITY) {
-                // O holds the sum over earlier tiles: wait for PV of tile j-1, then rescale this half.
-                if (!warp_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, a.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            if (grow && c > 0 && m_run > -INFINITY) {
+                // O holds the sum over earlier tiles; the PV that last wrote it completed
+                // before this S (its QK^T was issued after that PV).
                 const float corr = fast_exp2(m_run - m_new);
                 l_run *= corr;
 #pragma unroll
-                for (int c = 0; c < HC / 32; ++c) {
+                for (int q = 0; q < D / 32; ++q) {
                     float o[32];
-                    const uint32_t oa = lane_addr + COL_O + half * HC + c * 32;
-                    tmem_ld32(oa, o);
+                    tmem_ld32(o_addr + q * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= corr;
-                    tmem_st32(oa, o);
+                    tmem_st32(o_addr + q * 32, o);
                 }
                 tmem_wait_st();
             }
             m_run = m_new;
             const float mu = m_run == -INFINITY ? 0.f : m_run;
-            // P in registers first: the exponentials overlap the previous tile's PV.
-            // (packed float32x2 FMA for the arguments and packed adds for the sums:
-            // the softmax warps are issue-bound, so fewer instructions matter)
-            uint32_t pk[HC / 2];
+            // P = exp2(x * scale - max), packed to bf16 pairs: the P of half hf goes to
+            // columns 32 hf .. 32 hf + 31 of S_X, which hold S values already read (half 0
+            // of S, read just before); packed float32x2 arithmetic, since the softmax
+            // warps issue most of the kernel's instructions.
             float2 l4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
             const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
 #pragma unroll
-            for (int e = 0; e < HC / 2; ++e) {
-                const float2 arg = __ffma2_rn(make_float2(x[2 * e], x[2 * e + 1]), sl2v, negmu);
-                const float p0 = fast_exp2(arg.x);
-                const float p1 = fast_exp2(arg.y);
-                l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
-                pk[e] = pack_bf16(p0, p1);
+            for (int hf = 0; hf < 2; ++hf) {
+                load_half(hf);
+#pragma unroll
+                for (int q = 0; q < HC / 32; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c2 = q * 32 + 2 * e;
+                        const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
+                        const float p0 = fast_exp2(arg.x);
+                        const float p1 = fast_exp2(arg.y);
+                        l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16u(s_addr + hf * (HC / 2) + q * 16, pk);
+                }
             }
             l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
             l_run += l4[0].x + l4[0].y;
-            // P buffer s was last read by the PV of tile j-2.
-            if (j >= 2 && !warp_wait(smem_u32(&bars->pv_done[s]), ((j >> 1) - 1) & 1, a.err)) {
-                ok = false;
-                break;
-            }
-            if constexpr (HC / 2 == 32) {
-                tmem_st32u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
-            } else {
-                tmem_st16u(lane_addr + (s ? COL_P1 : COL_P0) + half * (HC / 2), pk);
-            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[s]));
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X]));
         }
-        bars->red_sum[half][row] = l_run;
-        mbar_arrive(smem_u32(&bars->fin[sub]));
-        if (!warp_wait(smem_u32(&bars->fin[sub]), 0, a.err)) ok = false;
-        if (ok && n > 0) {
-            if (!warp_wait(smem_u32(&bars->pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, a.err)) {
+        if (ok && c > 0) {
+            if (!warp_wait(smem_u32(&bars->o_done), 0, a.err)) {
                 ok = false;
             } else {
                 tc_fence_after();
-                float lsum = 0.f;
+                const float inv = 1.0f / l_run;
+                float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D;
 #pragma unroll
-                for (int q = 0; q < WPS; ++q) lsum += bars->red_sum[q][row];
-                const float inv = 1.0f / lsum;
-                float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D + half * HC;
-#pragma unroll
-                for (int c = 0; c < HC / 32; ++c) {
+                for (int q = 0; q < D / 32; ++q) {
                     float o[32];
-                    tmem_ld32(lane_addr + COL_O + half * HC + c * 32, o);
+                    tmem_ld32(o_addr + q * 32, o);
                     tmem_wait_ld();
                     if (i < rows_b) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
-                            *(float4*)(orow + c * 32 + e) =
+                            *(float4*)(orow + q * 32 + e) =
                                 make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
                     }
                 }
