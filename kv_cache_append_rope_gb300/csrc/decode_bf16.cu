@@ -281,7 +281,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % STAGES;
-            if (!mbar_wait_bounded(smem_u32(&full[s]), (i / STAGES) & 1)) {
+            // one verdict for the warp: the MMAs below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (i / STAGES) & 1))) {
                 *s_err = 1;
                 atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
                 break;

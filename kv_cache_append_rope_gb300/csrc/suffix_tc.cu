@@ -360,10 +360,13 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
             const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
-            if (grow && c > 0 && m_run > -INFINITY) {
-                // O holds the sum over earlier tiles; the PV that last wrote it completed
-                // before this S (its QK^T was issued after that PV).
-                const float corr = fast_exp2(m_run - m_new);
+            // O holds the sum over earlier tiles; the PV that last wrote it completed before
+            // this S (its QK^T was issued after that PV).  tcgen05.ld/st are warp-collective
+            // (.sync.aligned), so the whole warp rescales when any of its rows must, the
+            // other rows by 1.
+            const bool rescale = grow && c > 0 && m_run > -INFINITY;
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float corr = rescale ? fast_exp2(m_run - m_new) : 1.0f;
                 l_run *= corr;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
