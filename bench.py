@@ -50,9 +50,9 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # Summaries: profiles/decode_bf16_mha_small_full.md,
 # profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
 TRAFFIC = {
-    "mha_decode": ("ratio", (503473920.0 + 4291840.0) / 499236864.0),
-    "mqa_decode": ("ratio", (217863936.0 + 3975680.0) / 217403392.0),
-    "suffix": ("per_sequence", 375377408.0 + 170292480.0),
+    "mha_decode": ("ratio", (503476224.0 + 4633856.0) / 499236864.0),
+    "mqa_decode": ("ratio", (217849856.0 + 3716864.0) / 217403392.0),
+    "suffix": ("per_sequence", 375263488.0 + 169530112.0),
 }
 
 
