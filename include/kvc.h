@@ -245,7 +245,8 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
 /*
  * [Ch37] "Keep layer, logical length, and capacity separate" / "Reset or reject
  * without corrupting retained state": every layer's length and next position
- * become 0.  Storage, positions, capacity and allocation are unchanged.
+ * become 0.  Storage, positions, capacity and allocation are unchanged.  A
+ * device error recorded by an earlier call is cleared.
  */
 kvc_status kvc_reset(kvc_handle* h, void* stream);
 
@@ -325,6 +326,7 @@ kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** v
  * (a bounded wait that gave up, an out-of-range slot) and that the device
  * lengths and next positions equal the host mirrors.  KVC_ERR_DEVICE on any
  * difference (message names it), KVC_ERR_CUDA if the synchronisation fails.
+ * A reported error word is cleared (while it is set, kernels stop early).
  */
 kvc_status kvc_check(kvc_handle* h, void* stream);
 

@@ -1060,6 +1060,7 @@ kvc_status kvc_reset(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemsetAsync(h->len_d, 0, n * sizeof(int32_t), s));
     KVC_CUDA(h, cudaMemsetAsync(h->next_d, 0, n * sizeof(int32_t), s));
     KVC_CUDA(h, cudaMemsetAsync(h->lane_ticket, 0, (size_t)h->B() * h->Hkv() * sizeof(unsigned), s));
+    KVC_CUDA(h, cudaMemsetAsync(h->err_d, 0, sizeof(uint32_t), s));
     for (int b = 0; b < h->B(); ++b) release_blocks(h, b, 0);
     kvc_status st = upload_table(h, s);
     if (st != KVC_OK) return st;
@@ -1225,6 +1226,8 @@ kvc_status kvc_check(kvc_handle* h, void* stream) {
     KVC_CUDA(h, cudaMemcpy(len.data(), h->len_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
     KVC_CUDA(h, cudaMemcpy(next.data(), h->next_d, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
     KVC_CUDA(h, cudaMemcpy(&err, h->err_d, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    // reported once: kernels stop early while the word is set, so it is cleared here
+    if (err) KVC_CUDA(h, cudaMemset(h->err_d, 0, sizeof(uint32_t)));
     if (err)
         return fail(h, KVC_ERR_DEVICE,
                     "device error word 0x%x (1: slot out of range, 2: bounded wait timed out, 4: tensor memory, "

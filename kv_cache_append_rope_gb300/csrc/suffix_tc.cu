@@ -226,10 +226,11 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 }
                 issued = j + 1;
             }
-            // Our own copies must have landed before the CTA's shared memory is released.
-            if (is_k) mbar_wait_bounded(qb, 0, a.err);
+            // Our own copies must have landed before the CTA's shared memory is released
+            // (bounded in time only: an error raised elsewhere must not cut this short).
+            if (is_k) mbar_wait_bounded(qb, 0);
             for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
-                mbar_wait_bounded(smem_u32(&full[t % NS]), (t / NS) & 1, a.err);
+                mbar_wait_bounded(smem_u32(&full[t % NS]), (t / NS) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
