@@ -48,6 +48,8 @@
 // allocator warp frees the tensor memory.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "kvc_internal.h"
 #include "ptx.cuh"
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         const uint32_t o_addr = lane_addr + COL_O + X * 128;
         const float sl2 = a.scale_log2;
         const int tile_slot0 = cut + qt * BM;        // slot of the tile's first row
+        auto kbase_of = [](int jj) { return jj * BN; };
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int c = 0;
@@ -325,95 +328,103 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            // The row is read in two 64-column halves, twice (maximum, then exponentials),
-            // which keeps a thread's registers within the 168 that 10 warps leave it.
-            constexpr int HC = BN / 2;
-            const int kbase = jj * BN;
             // causal mask (keys after the row's slot) on diagonal tiles; with a window also
-            // the keys before slot - window + 1 on the first tiles
-            const bool past_window = a.window > 0 && kbase < tile_slot0 + BM - a.window;
-            const bool masked = kbase + BN - 1 > tile_slot0 || past_window;
-            const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
-            float x[HC];
-            auto load_half = [&](int hf) {
+            // the keys before slot - window + 1 on the first tiles.  The tile is processed
+            // by one of two copies of the code, with and without the mask, so that the
+            // unmasked tiles (nearly all) carry no masking instructions.
+            const bool masked =
+                kbase_of(jj) + BN - 1 > tile_slot0 || (a.window > 0 && kbase_of(jj) < tile_slot0 + BM - a.window);
+            auto tile = [&](auto mask_c) {
+                // The row is read in two 64-column halves, twice (maximum, then exponentials),
+                // which keeps a thread's registers within the 168 that 10 warps leave it.
+                constexpr int HC = BN / 2;
+                const int kbase = jj * BN;
+                float x[HC];
+                auto load_half = [&](int hf, auto mask_c) {
 #pragma unroll
-                for (int q = 0; q < HC / 32; ++q) tmem_ld32(s_addr + hf * HC + q * 32, x + q * 32);
-                tmem_wait_ld();
-                if (masked) {
-                    const int kb = kbase + hf * HC;
-#pragma unroll
-                    for (int e = 0; e < HC; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
-                }
-            };
-            // row maximum (8 independent chains of 3-input maxima)
-            float m8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                load_half(hf);
-#pragma unroll
-                for (int e = 0; e + 16 <= HC; e += 16)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
-            }
-            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            const float m_tile = mx * sl2;
-            const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
-            const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
-            // O holds the sum over earlier tiles; the PV that last wrote it completed before
-            // this S (its QK^T was issued after that PV).  tcgen05.ld/st are warp-collective
-            // (.sync.aligned), so the whole warp rescales when any of its rows must, the
-            // other rows by 1.
-            const bool rescale = grow && c > 0 && m_run > -INFINITY;
-            if (__any_sync(0xffffffffu, rescale)) {
-                const float corr = rescale ? fast_exp2(m_run - m_new) : 1.0f;
-                l_run *= corr;
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    float o[32];
-                    tmem_ld32(o_addr + q * 32, o);
+                    for (int q = 0; q < HC / 32; ++q) tmem_ld32(s_addr + hf * HC + q * 32, x + q * 32);
                     tmem_wait_ld();
+                    if constexpr (decltype(mask_c)::value) {
+                        const int kb = kbase + hf * HC;
+                        const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= corr;
-                    tmem_st32(o_addr + q * 32, o);
-                }
-                tmem_wait_st();
-            }
-            m_run = m_new;
-            const float mu = m_run == -INFINITY ? 0.f : m_run;
-            // P = exp2(x * scale - max), packed to bf16 pairs: the P of half hf goes to
-            // columns 32 hf .. 32 hf + 31 of S_X, which hold S values already read (half 0
-            // of S, read just before); packed float32x2 arithmetic, since the softmax
-            // warps issue most of the kernel's instructions.
-            float2 l4[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
-            const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                load_half(hf);
-#pragma unroll
-                for (int q = 0; q < HC / 32; ++q) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c2 = q * 32 + 2 * e;
-                        const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
-                        const float p0 = fast_exp2(arg.x);
-                        const float p1 = fast_exp2(arg.y);
-                        l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
-                        pk[e] = pack_bf16(p0, p1);
+                        for (int e = 0; e < HC; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
                     }
-                    tmem_st16u(s_addr + hf * (HC / 2) + q * 16, pk);
+                };
+                // row maximum (8 independent chains of 3-input maxima)
+                float m8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    load_half(hf, mask_c);
+#pragma unroll
+                    for (int e = 0; e + 16 <= HC; e += 16)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
                 }
-            }
-            l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
-            l_run += l4[0].x + l4[0].y;
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X]));
+                const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                const float m_tile = mx * sl2;
+                const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
+                const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
+                // O holds the sum over earlier tiles; the PV that last wrote it completed before
+                // this S (its QK^T was issued after that PV).  tcgen05.ld/st are warp-collective
+                // (.sync.aligned), so the whole warp rescales when any of its rows must, the
+                // other rows by 1.
+                const bool rescale = grow && c > 0 && m_run > -INFINITY;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float corr = rescale ? fast_exp2(m_run - m_new) : 1.0f;
+                    l_run *= corr;
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        float o[32];
+                        tmem_ld32(o_addr + q * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= corr;
+                        tmem_st32(o_addr + q * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                m_run = m_new;
+                const float mu = m_run == -INFINITY ? 0.f : m_run;
+                // P = exp2(x * scale - max), packed to bf16 pairs: the P of half hf goes to
+                // columns 32 hf .. 32 hf + 31 of S_X, which hold S values already read (half 0
+                // of S, read just before); packed float32x2 arithmetic, since the softmax
+                // warps issue most of the kernel's instructions.
+                float2 l4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
+                const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    load_half(hf, mask_c);
+#pragma unroll
+                    for (int q = 0; q < HC / 32; ++q) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c2 = q * 32 + 2 * e;
+                            const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
+                            const float p0 = fast_exp2(arg.x);
+                            const float p1 = fast_exp2(arg.y);
+                            l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
+                            pk[e] = pack_bf16(p0, p1);
+                        }
+                        tmem_st16u(s_addr + hf * (HC / 2) + q * 16, pk);
+                    }
+                }
+                l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+                l_run += l4[0].x + l4[0].y;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X]));
+            };
+            if (masked)
+                tile(std::true_type{});
+            else
+                tile(std::false_type{});
         }
         if (ok && c > 0) {
             if (!warp_wait(smem_u32(&bars->o_done), 0, a.err)) {
