@@ -50,9 +50,9 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # Summaries: profiles/decode_bf16_mha_small_full.md,
 # profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
 TRAFFIC = {
-    "mha_decode": ("ratio", (503476224.0 + 4633856.0) / 499236864.0),
-    "mqa_decode": ("ratio", (217849856.0 + 3716864.0) / 217403392.0),
-    "suffix": ("per_sequence", 375263488.0 + 169530112.0),
+    "mha_decode": ("ratio", (503521280.0 + 4513280.0) / 499236864.0),
+    "mqa_decode": ("ratio", (217871616.0 + 3592448.0) / 217403392.0),
+    "suffix": ("per_sequence", 376881152.0 + 176183040.0),
 }
 
 
