@@ -126,6 +126,17 @@ __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
 __device__ __forceinline__ void tmem_relinquish() {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+// Register reallocation between warpgroups (all four warps of a warpgroup execute
+// it).  The counts of all warpgroups must add up to the block's launch allocation:
+// an increase waits until released registers are available.
+template <uint32_t N> __device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N> __device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }

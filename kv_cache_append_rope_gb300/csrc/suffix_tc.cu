@@ -22,7 +22,7 @@
 // cut + i) attends key slots 0 .. cut + i; key tiles are 128 slots, the
 // diagonal ones masked element-wise.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 both Q
 //             tiles once and K tiles into a 2-stage ring, lane 1 V tiles into
 //             a 2-stage ring.
@@ -36,7 +36,8 @@
 //             bf16, overwrites the first 64 columns of S_X once the softmax has
 //             read S_X, and the next S_X = Q_X K^T is issued after the PV that
 //             reads P_X (the MMAs of one thread execute in order).
-//   warps 2-5 softmax of tile A, warps 6-9 of tile B: one thread per query row
+//   warps 2-3 idle (they complete warpgroup 0, whose registers go to the softmax).
+//   warps 4-7 softmax of tile A, warps 8-11 of tile B: one thread per query row
 //             (= TMEM lane of its sub-partition) owning the whole 128-column row
 //             -- no exchange between warps: tcgen05.ld of S, causal (and
 //             window) mask, running max in log2 units, O rescaled through TMEM
@@ -68,7 +69,13 @@ constexpr int OFF_V = OFF_K + KST * TILE;
 constexpr int OFF_BAR = OFF_V + VST * TILE;
 constexpr int SMEM_BYTES = OFF_BAR + 4096 + 1024;
 constexpr int NSW = 4 * QT;                // softmax warps: one per TMEM sub-partition per query tile
-constexpr int THREADS = (2 + NSW) * 32;
+constexpr int THREADS = (4 + NSW) * 32;    // warpgroup 0: producer, MMA issuer, 2 idle; 1-2: softmax
+// Registers: three warps per SM sub-partition cap a thread at 168 at launch; warpgroup 0
+// then gives registers back so that the softmax warpgroups can hold a whole 128-column
+// row of S.  The split must add up to the launch allocation exactly (checked on the host
+// against the built kernel's register count before the first launch).
+constexpr int kLaunchRegs = 168, kRegsLow = 120, kRegsHigh = 192;
+static_assert(128 * kRegsLow + 2 * 128 * kRegsHigh == THREADS * kLaunchRegs, "register split");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256; // S_X at 128 X, O_X at 256 + 128 X
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -175,7 +182,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-
+    if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // lane 0 streams both Q tiles and the K ring, lane 1 the V ring, so that the
@@ -303,11 +311,13 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             tc_commit(smem_u32(&bars->o_done));
             mbar_wait_bounded(smem_u32(&bars->o_done), 0);  // no abort: the MMAs always finish
         }
+    }
     } else {
+        setmaxnreg_inc<kRegsHigh>();
         // ------------------------------------------------------------ softmax warps
-        // Warps 2-5 take query tile A, 6-9 tile B; warp w reads TMEM lanes
+        // Warps 4-7 take query tile A, 8-11 tile B; warp w reads TMEM lanes
         // 32 * (w % 4) .. + 31, one query row per thread.
-        const int X = (warp - 2) >> 2;
+        const int X = (warp - 4) >> 2;
         const int sub = warp & 3;
         const int row = sub * 32 + lane;             // query row inside the tile = TMEM lane
         const int qt = QT * qp + X;
@@ -335,34 +345,30 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             const bool masked =
                 kbase_of(jj) + BN - 1 > tile_slot0 || (a.window > 0 && kbase_of(jj) < tile_slot0 + BM - a.window);
             auto tile = [&](auto mask_c) {
-                // The row is read in two 64-column halves, twice (maximum, then exponentials),
-                // which keeps a thread's registers within the 168 that 10 warps leave it.
-                constexpr int HC = BN / 2;
-                const int kbase = jj * BN;
-                float x[HC];
-                auto load_half = [&](int hf, auto mask_c) {
+                // The whole 128-column row is read with one wait, then reduced to its
+                // maximum, then turned into exponentials in place.
+                float x[BN];
 #pragma unroll
-                    for (int q = 0; q < HC / 32; ++q) tmem_ld32(s_addr + hf * HC + q * 32, x + q * 32);
-                    tmem_wait_ld();
-                    if constexpr (decltype(mask_c)::value) {
-                        const int kb = kbase + hf * HC;
-                        const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
+                for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+                tmem_wait_ld();
+                if constexpr (decltype(mask_c)::value) {
+                    const int kb = jj * BN;
+                    const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
 #pragma unroll
-                        for (int e = 0; e < HC; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
-                    }
-                };
+                    for (int e = 0; e < BN; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
+                }
                 // row maximum (8 independent chains of 3-input maxima)
                 float m8[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+                for (int q = 0; q < 8; ++q) m8[q] = fmax3(x[q], x[8 + q], x[16 + q]);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf, mask_c);
+                for (int e = 24; e + 16 <= BN; e += 16)
 #pragma unroll
-                    for (int e = 0; e + 16 <= HC; e += 16)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
-                }
+                    for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
+                m8[0] = fmax3(m8[0], x[120], x[121]);
+                m8[1] = fmax3(m8[1], x[122], x[123]);
+                m8[2] = fmax3(m8[2], x[124], x[125]);
+                m8[3] = fmax3(m8[3], x[126], x[127]);
                 const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 const float m_tile = mx * sl2;
                 const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float corr = rescale ? fast_exp2(m_run - m_new) : 1.0f;
                     l_run *= corr;
-#pragma unroll
+#pragma unroll 1
                     for (int q = 0; q < D / 32; ++q) {
                         float o[32];
                         tmem_ld32(o_addr + q * 32, o);
@@ -388,31 +394,26 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 }
                 m_run = m_new;
                 const float mu = m_run == -INFINITY ? 0.f : m_run;
-                // P = exp2(x * scale - max), packed to bf16 pairs: the P of half hf goes to
-                // columns 32 hf .. 32 hf + 31 of S_X, which hold S values already read (half 0
-                // of S, read just before); packed float32x2 arithmetic, since the softmax
-                // warps issue most of the kernel's instructions.
+                // P = exp2(x * scale - max), packed to bf16 pairs into columns 0 .. 63 of S_X
+                // (all of S is in registers already); packed float32x2 arithmetic, since the
+                // softmax warps issue most of the kernel's instructions.
                 float2 l4[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
                 const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf, mask_c);
+                for (int q = 0; q < BN / 32; ++q) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int q = 0; q < HC / 32; ++q) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int c2 = q * 32 + 2 * e;
-                            const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
-                            const float p0 = fast_exp2(arg.x);
-                            const float p1 = fast_exp2(arg.y);
-                            l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
-                            pk[e] = pack_bf16(p0, p1);
-                        }
-                        tmem_st16u(s_addr + hf * (HC / 2) + q * 16, pk);
+                    for (int e = 0; e < 16; ++e) {
+                        const int c2 = q * 32 + 2 * e;
+                        const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
+                        const float p0 = fast_exp2(arg.x);
+                        const float p1 = fast_exp2(arg.y);
+                        l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
+                        pk[e] = pack_bf16(p0, p1);
                     }
+                    tmem_st16u(s_addr + q * 16, pk);
                 }
                 l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
                 l_run += l4[0].x + l4[0].y;
@@ -463,7 +464,12 @@ int suffix_tc_grid(int sms) { return sms; }
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(suffix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        // the register split assumes the launch allocation it was computed for
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, suffix_tc_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(suffix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr = true;
     }
