@@ -252,14 +252,19 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             tc_fence_after();
             auto active = [&](int X, int jj) { return jj >= jlo[X] && jj < jhi[X]; };
             // S_X = Q_X K^T from K stage ks
+            // Descriptors are built once: the start address sits in the low 14 bits (in
+            // 16-byte units, and every shared address here is below 256 KB), so the
+            // descriptor of base + off is the base's descriptor + off / 16.
+            const uint64_t dq = smem_desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+            const uint64_t dk = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+            const uint64_t dv = smem_desc_sw128(smem_u32(smem + OFF_V), HALF, 1024);
             auto issue_qk = [&](int X, int ks) {
-                const uint32_t q_s = smem_u32(smem + OFF_Q + X * TILE);
-                const uint32_t k_s = smem_u32(smem + OFF_K + ks * TILE);
+                const uint64_t qd = dq + (uint64_t)((X * TILE) >> 4);
+                const uint64_t kd = dk + (uint64_t)((ks * TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-                    tc_mma_ss(tmem + COL_S + X * 128, smem_desc_sw128(q_s + off, 16, 1024),
-                              smem_desc_sw128(k_s + off, 16, 1024), idesc_qk, kk > 0);
+                    const uint32_t off = ((kk >> 2) * HALF + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(tmem + COL_S + X * 128, qd + off, kd + off, idesc_qk, kk > 0);
                 }
                 tc_commit(smem_u32(&bars->s_full[X]));
             };
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                     break;
                 }
                 tc_fence_after();
-                const uint32_t v_s = smem_u32(smem + OFF_V + vs * TILE);
+                const uint64_t vd = dv + (uint64_t)((vs * TILE) >> 4);
                 for (int X = 0; ok && X < QT; ++X) {
                     if (active(X, jj)) {
                         if (!mbar_wait_bounded(smem_u32(&bars->p_full[X]), pv_count[X] & 1, a.err)) {
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                             // A = P_X from tensor memory (16 keys = 8 columns per step),
                             // B = V (rows = keys, contiguous head dims: MN-major)
                             tc_mma_ts(tmem + COL_O + X * 128, tmem + COL_S + X * 128 + kk * 8,
-                                      smem_desc_sw128(v_s + kk * 16 * 128, HALF, 1024), idesc_pv,
+                                      vd + (uint64_t)(kk * 16 * 128 >> 4), idesc_pv,
                                       (pv_count[X] > 0 || kk > 0));
                         }
                         pv_count[X] += 1;
