@@ -438,18 +438,32 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             } else {
                 tc_fence_after();
                 const float inv = 1.0f / l_run;
-                float* orow = a.out + (((int64_t)b * a.Hq + h) * a.S + i) * D;
+                // O rows leave through shared memory (the Q tiles, unused once every MMA has
+                // completed): each thread writes 32 columns of its row, the warp then stores
+                // 4 rows x 128 bytes per instruction -- whole lines instead of 32 scattered
+                // 16-byte pieces.  16-byte slots are XOR-swizzled by row (mod 8), so both
+                // sides take the minimum of 4 shared-memory wavefronts per instruction.
+                float4* stage = reinterpret_cast<float4*>(smem + OFF_Q) + (warp - 4) * 256;
+                const int row0 = qt * BM + sub * 32;             // query row of lane 0
+                float* obase = a.out + (((int64_t)b * a.Hq + h) * a.S) * D;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     float o[32];
                     tmem_ld32(o_addr + q * 32, o);
                     tmem_wait_ld();
-                    if (i < rows_b) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *(float4*)(orow + q * 32 + e) =
-                                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+                    for (int e = 0; e < 8; ++e)
+                        stage[lane * 8 + (e ^ (lane & 7))] =
+                            make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = 4 * k + (lane >> 3), cc = lane & 7;
+                        const float4 val = stage[rr * 8 + (cc ^ (rr & 7))];
+                        if (row0 + rr < rows_b)
+                            *reinterpret_cast<float4*>(obase + (int64_t)(row0 + rr) * D + q * 32 + cc * 4) = val;
                     }
+                    __syncwarp();
                 }
             }
         }
