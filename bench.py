@@ -52,7 +52,7 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 TRAFFIC = {
     "mha_decode": ("ratio", (503521280.0 + 4513280.0) / 499236864.0),
     "mqa_decode": ("ratio", (217871616.0 + 3592448.0) / 217403392.0),
-    "suffix": ("per_sequence", 376881152.0 + 176183040.0),
+    "suffix": ("per_sequence", 375401472.0 + 174217472.0),
 }
 
 
