@@ -19,7 +19,9 @@ Every step reads far more than the 129 MB L2 (2.2 GB of K/V per MHA decode
 step), so no L2 flush is inserted.  `value` is device-timed with inputs
 resident in HBM; `e2e` repeats the measurement through the same C-ABI calls
 with the per-step inputs copied from pinned host memory and the outputs
-copied back inside the timed region.  `roofline` times the dominant kernel
+copied back inside the timed region (suffix: kvc_prefill_suffix_host, which
+takes the pinned host buffers and overlaps each stage of sequences' copies
+with another stage's work).  `roofline` times the dominant kernel
 with CUDA events recorded by the library around each launch on its stream,
 in a second pass over the same number of steps (so that the event records do
 not weigh on `value`).
@@ -71,6 +73,8 @@ def parse():
     p.add_argument("--graph", action="store_true",
                    help="decode workloads: lengths kept on the device, each bench step's decode calls "
                         "captured once in a CUDA graph and replayed")
+    p.add_argument("--host-chunk", type=int, default=0,
+                   help="suffix e2e: sequences per stage of the host-buffer call; 0 = the library's choice")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=0,
@@ -362,6 +366,7 @@ class SuffixBench:
         self.out = torch.empty((B, H, self.S, D), dtype=torch.float32, device=device)
         self.seqlen = [self.T - cu for cu in self.cuts]
         self.flops = float(sum(H * 4 * D * (s * cu + s * (s + 1) / 2) for s, cu in zip(self.seqlen, self.cuts)))
+        self.host_chunk = 0
         torch.cuda.synchronize(device)
 
     def step(self):
@@ -373,26 +378,21 @@ class SuffixBench:
     def e2e_setup(self):
         self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
         self.hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        self.dq, self.dk, self.dv = (torch.empty_like(x) for x in (self.q, self.k, self.v))
-        self.copy_stream = torch.cuda.Stream(self.device)
-        self.h2d = self.hq.nbytes + self.hk.nbytes + self.hv.nbytes
-        self.d2h = self.hout.nbytes
+        # the host-buffer call copies rows 0 .. seqlen[b]-1 of every head, in and out
+        c = self.cfg
+        rows = sum(self.seqlen)
+        self.h2d = rows * (c["Hq"] + 2 * c["Hq"]) * c["D"] * 2
+        self.d2h = rows * c["Hq"] * c["D"] * 4
 
     def e2e_step(self):
-        """Upload q/k/v (three streams of copies in parallel with the cut search on the
-        host), run the step, read the output back."""
+        """The cut search on the host, truncate, then kvc_prefill_suffix_host on pinned host
+        buffers: each stage of sequences is uploaded, attended and read back while the next
+        stage's rows are on their way in."""
         from kv_cache_append_rope_gb300 import kvc
-        compute, copy = torch.cuda.current_stream(self.device), self.copy_stream
-        copy.wait_stream(compute)
-        with torch.cuda.stream(copy):
-            self.dq.copy_(self.hq, non_blocking=True)
-        self.dk.copy_(self.hk, non_blocking=True)
-        self.dv.copy_(self.hv, non_blocking=True)
         cuts = [kvc.lcp(self.cached[b], self.query[b]) for b in range(self.cfg["B"])]
         self.cache.truncate(cuts)
-        compute.wait_stream(copy)
-        self.cache.prefill_suffix(0, self.dq, self.dk, self.dv, seqlen=self.seqlen, out=self.out)
-        self.hout.copy_(self.out, non_blocking=True)
+        self.cache.prefill_suffix_host(0, self.hq, self.hk, self.hv, seqlen=self.seqlen, out=self.hout,
+                                       chunk_sequences=self.host_chunk, sync=False)
 
     def dominant(self):
         return "suffix" if self.cache.kernel_stats("suffix")[1] else "generic_attend"
@@ -478,6 +478,8 @@ def run_ours(args, name, world, rank, local):
     torch.cuda.set_device(device)
     hbm, tflops, peak_kind = peaks()
     bench = make_bench(name, device, args.batch, args.graph, args.block_rows)
+    if hasattr(bench, "host_chunk"):
+        bench.host_chunk = args.host_chunk
     cache = bench.cache
     if args.split_rows:
         cache.set_option(L.OPT_DECODE_SPLIT_ROWS, args.split_rows)

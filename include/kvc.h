@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 3
+#define KVC_ABI_VERSION 4
 
 typedef enum kvc_status {
     KVC_OK = 0,
@@ -241,6 +241,32 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
                               const kvc_tensor* k, const kvc_tensor* v,
                               const int32_t* start_pos, const int32_t* seqlen,
                               const kvc_tensor* out, void* stream);
+
+/*
+ * kvc_prefill_suffix with q, k, v and out in HOST memory (page-locked memory
+ * lets the copies overlap the work; pageable memory works, without overlap).
+ * Same arguments, layouts, results and errors as kvc_prefill_suffix, plus:
+ *   chunk_sequences: sequences per pipeline stage (0 -> ceil(B / 8)).
+ * Every check of the whole call (shapes, dtypes, capacity, positions, storage
+ * blocks; in checked mode the finiteness of k and v, scanned on the host) runs
+ * before any copy or launch; an error leaves the state unchanged.  The call
+ * then copies rows 0 .. seqlen[b]-1 of each head of each sequence into device
+ * staging owned by the handle, stage by stage, on an internal upload stream;
+ * runs each stage's append and attention on `stream` as soon as its rows have
+ * landed (the other sequences take 0 rows); and copies each stage's output rows
+ * back on an internal download stream, so that the copies of one stage overlap
+ * the work of another.  The call returns once everything is enqueued; `stream`
+ * completes after the last output row is in host memory, and the host buffers
+ * must stay valid and unchanged until then.  The results equal those of
+ * kvc_prefill_suffix on the same inputs bit for bit.  Rows >= seqlen[b] of out
+ * are left untouched.  KVC_ERR_CONFIG if a pointer is device memory;
+ * KVC_ERR_ALLOC if the staging (the size of q, k, v and out) cannot be allocated.
+ */
+kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tensor* q,
+                                   const kvc_tensor* k, const kvc_tensor* v,
+                                   const int32_t* start_pos, const int32_t* seqlen,
+                                   const kvc_tensor* out, int32_t chunk_sequences,
+                                   void* stream);
 
 /*
  * [Ch37] "Keep layer, logical length, and capacity separate" / "Reset or reject

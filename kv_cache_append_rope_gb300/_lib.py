@@ -30,7 +30,7 @@ KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "gen
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
-           "kvc_destroy", "kvc_append_attend", "kvc_prepare_attend", "kvc_commit", "kvc_prefill_suffix", "kvc_reset", "kvc_truncate",
+           "kvc_destroy", "kvc_append_attend", "kvc_prepare_attend", "kvc_commit", "kvc_prefill_suffix", "kvc_prefill_suffix_host", "kvc_reset", "kvc_truncate",
            "kvc_lcp", "kvc_lcp_window", "kvc_share_prefix", "kvc_block_table", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
            "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
 
@@ -82,6 +82,8 @@ def _load():
                                               ctypes.POINTER(kvc_ticket), _P]),
         "kvc_commit": (ctypes.c_int, [_P, ctypes.POINTER(kvc_ticket), ctypes.c_int32, _P]),
         "kvc_prefill_suffix": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _TP, _I32P, _I32P, _TP, _P]),
+        "kvc_prefill_suffix_host": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _TP, _I32P, _I32P, _TP,
+                                                    ctypes.c_int32, _P]),
         "kvc_reset": (ctypes.c_int, [_P, _P]),
         "kvc_truncate": (ctypes.c_int, [_P, _I32P, _P]),
         "kvc_lcp": (ctypes.c_int, [_I32P, ctypes.c_int64, _I32P, ctypes.c_int64, _I32P]),

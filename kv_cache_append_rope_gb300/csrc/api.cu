@@ -219,6 +219,13 @@ void free_all(kvc_handle* h) {
     cudaFree(h->lane_ticket);
     cudaFree(h->step_ticket);
     cudaFree(h->table_d);
+    cudaFree(h->io_buf);
+    for (auto e : h->io_ev) cudaEventDestroy(e);
+    h->io_ev.clear();
+    if (h->io_entry) cudaEventDestroy(h->io_entry);
+    if (h->io_last) cudaEventDestroy(h->io_last);
+    if (h->io_h2d) cudaStreamDestroy(h->io_h2d);
+    if (h->io_d2h) cudaStreamDestroy(h->io_d2h);
     h->ring.destroy();
     for (auto& t : h->timers) {
         for (auto e : t.start) cudaEventDestroy(e);
@@ -248,9 +255,13 @@ void ArgRing::destroy() {
         if (host[i]) cudaFreeHost(host[i]);
         if (dev[i]) cudaFree(dev[i]);
         if (done[i]) cudaEventDestroy(done[i]);
-        host[i] = dev[i] = nullptr;
+        host[i] = dev[i] = mapped[i] = nullptr;
         done[i] = nullptr;
     }
+    for (void* p : retired_host) cudaFreeHost(p);
+    for (void* p : retired_dev) cudaFree(p);
+    retired_host.clear();
+    retired_dev.clear();
 }
 
 cudaError_t ArgRing::acquire(size_t bytes, void** host_ptr) {
@@ -261,12 +272,16 @@ cudaError_t ArgRing::acquire(size_t bytes, void** host_ptr) {
         pending[s] = false;
     }
     if (cap[s] < bytes) {
-        size_t c = std::max<size_t>(bytes, 4096);
-        if (host[s]) cudaFreeHost(host[s]);
-        if (dev[s]) cudaFree(dev[s]);
-        host[s] = dev[s] = nullptr;
+        // grow geometrically; the replaced buffers are retired, not freed (their last
+        // copy has completed, but freeing would synchronise the device)
+        size_t c = std::max<size_t>(std::max<size_t>(bytes, 2 * cap[s]), 65536);
+        if (host[s]) retired_host.push_back(host[s]);
+        if (dev[s]) retired_dev.push_back(dev[s]);
+        host[s] = dev[s] = mapped[s] = nullptr;
         cap[s] = 0;
-        cudaError_t e = cudaHostAlloc(&host[s], c, cudaHostAllocDefault);
+        cudaError_t e = cudaHostAlloc(&host[s], c, cudaHostAllocMapped);
+        if (e != cudaSuccess) return e;
+        e = cudaHostGetDevicePointer(&mapped[s], host[s], 0);
         if (e != cudaSuccess) return e;
         e = cudaMalloc(&dev[s], c);
         if (e != cudaSuccess) return e;
@@ -279,7 +294,12 @@ cudaError_t ArgRing::acquire(size_t bytes, void** host_ptr) {
 
 cudaError_t ArgRing::upload(size_t bytes, cudaStream_t stream, void** dev_ptr) {
     *dev_ptr = dev[cur];
-    return cudaMemcpyAsync(dev[cur], host[cur], bytes, cudaMemcpyHostToDevice, stream);
+    return copy(dev[cur], bytes, stream);
+}
+
+cudaError_t ArgRing::copy(void* dst, size_t bytes, cudaStream_t stream) {
+    if (by_kernel) return launch_copy_args(mapped[cur], dst, bytes, stream);
+    return cudaMemcpyAsync(dst, host[cur], bytes, cudaMemcpyHostToDevice, stream);
 }
 
 cudaError_t ArgRing::release(cudaStream_t stream) {
@@ -544,7 +564,7 @@ static kvc_status upload_table(kvc_handle* h, cudaStream_t s) {
     void* hp;
     KVC_CUDA(h, h->ring.acquire(bytes, &hp));
     memcpy(hp, h->table_h.data(), bytes);
-    KVC_CUDA(h, cudaMemcpyAsync(h->table_d, hp, bytes, cudaMemcpyHostToDevice, s));
+    KVC_CUDA(h, h->ring.copy(h->table_d, bytes, s));
     KVC_CUDA(h, h->ring.release(s));
     h->table_dirty = false;
     return KVC_OK;
@@ -553,8 +573,9 @@ static kvc_status upload_table(kvc_handle* h, cudaStream_t s) {
 // Gives every sequence b blocks for rows [from[b], to[b]) -- a block that is shared
 // with another sequence is first copied (copy-on-write) -- then uploads the table.
 // All or nothing: KVC_ERR_FULL, with no change, when the pool is short.
-static kvc_status ensure_blocks(kvc_handle* h, const int32_t* from, const int32_t* to, cudaStream_t s) {
-    if (!h->paged()) return KVC_OK;
+// Blocks that growing each sequence b from from[b] to to[b] rows takes from the pool: one
+// per missing block and one per shared block written into (copied first).
+static int64_t blocks_needed(kvc_handle* h, const int32_t* from, const int32_t* to) {
     const int B = h->B(), P = h->cfg.block_rows, nb = h->nblk;
     int64_t need = 0;
     for (int b = 0; b < B; ++b)
@@ -562,6 +583,13 @@ static kvc_status ensure_blocks(kvc_handle* h, const int32_t* from, const int32_
             const int blk = h->table_h[(size_t)b * nb + j];
             need += blk < 0 || h->refcnt[blk] > 1;
         }
+    return need;
+}
+
+static kvc_status ensure_blocks(kvc_handle* h, const int32_t* from, const int32_t* to, cudaStream_t s) {
+    if (!h->paged()) return KVC_OK;
+    const int B = h->B(), P = h->cfg.block_rows, nb = h->nblk;
+    const int64_t need = blocks_needed(h, from, to);
     if (need > (int64_t)h->free_blocks.size())
         return fail(h, KVC_ERR_FULL, "the block pool has %zu free blocks; the call needs %lld", h->free_blocks.size(),
                     (long long)need);
@@ -840,69 +868,13 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     return KVC_OK;
 }
 
-}  // namespace
-}  // namespace kvc
 
-extern "C" {
+// kvc_prefill_suffix with device tensors; `check_finite` false skips the checked-mode
+// scan (the host-buffer entry point scans its host inputs once for the whole call).
+kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k, const kvc_tensor* v,
+                        const int32_t* start_pos, const int32_t* seqlen, const kvc_tensor* out, void* stream,
+                        bool check_finite) {
 
-kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
-                             const kvc_tensor* v, const kvc_tensor* out, void* stream) {
-    return append_attend_impl(h, layer, q, k, v, out, true, stream);
-}
-
-kvc_status kvc_prepare_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
-                              const kvc_tensor* v, const kvc_tensor* out, kvc_ticket* ticket, void* stream) {
-    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
-    if (!ticket) return fail(h, KVC_ERR_NULL, "ticket pointer is NULL");
-    kvc_status st = append_attend_impl(h, layer, q, k, v, out, false, stream);
-    if (st != KVC_OK) return st;
-    ticket->handle = h;
-    ticket->layer = layer;
-    ticket->reserved = 0;
-    ticket->version = h->layer_version[layer];
-    return KVC_OK;
-}
-
-kvc_status kvc_commit(kvc_handle* h, const kvc_ticket* tickets, int32_t n, void* stream) {
-    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
-    if (n < 0) return fail(h, KVC_ERR_TICKET, "ticket count %d is negative", n);
-    if (n > 0 && !tickets) return fail(h, KVC_ERR_NULL, "ticket array is NULL");
-    const int L = h->cfg.layers, B = h->B();
-    std::vector<char> seen(L, 0);
-    for (int i = 0; i < n; ++i) {
-        const kvc_ticket& t = tickets[i];
-        if (t.handle != h) return fail(h, KVC_ERR_TICKET, "ticket %d was prepared by another cache", i);
-        if (t.layer < 0 || t.layer >= L) return fail(h, KVC_ERR_TICKET, "ticket %d names layer %d", i, t.layer);
-        if (seen[t.layer]) return fail(h, KVC_ERR_TICKET, "tickets repeat layer %d", t.layer);
-        seen[t.layer] = 1;
-        if (t.version != h->layer_version[t.layer])
-            return fail(h, KVC_ERR_TICKET, "ticket %d of layer %d is stale: the layer changed after it was prepared",
-                        i, t.layer);
-    }
-    if (n == 0) return KVC_OK;
-    cudaStream_t s = (cudaStream_t)stream;
-    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
-    for (int i0 = 0; i0 < n; i0 += kCommitMaxLayers) {
-        CommitLayers cl{};
-        cl.n = std::min(n - i0, kCommitMaxLayers);
-        for (int i = 0; i < cl.n; ++i) cl.layer[i] = tickets[i0 + i].layer;
-        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_commit_layers(h->len_d, h->next_d, cl, B, s); }));
-    }
-    for (int i = 0; i < n; ++i) {
-        const int l = tickets[i].layer;
-        h->layer_version[l] += 1;
-        for (int b = 0; b < B; ++b) {
-            h->len_h[(size_t)l * B + b] += 1;
-            h->next_h[(size_t)l * B + b] += 1;
-        }
-    }
-    return KVC_OK;
-}
-
-kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
-                              const kvc_tensor* v, const int32_t* start_pos, const int32_t* seqlen,
-                              const kvc_tensor* out, void* stream) {
-    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
     kvc_status st;
     if ((st = check_layer(h, layer)) != KVC_OK) return st;
     const int B = h->B(), Hq = h->Hq(), Hkv = h->Hkv(), D = h->D(), C = h->C();
@@ -938,7 +910,7 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     }
     cudaStream_t s = (cudaStream_t)stream;
     KVC_CUDA(h, cudaSetDevice(h->cfg.device));
-    if (h->cfg.checked) {
+    if (h->cfg.checked && check_finite) {
         const int64_t nk = (int64_t)B * Hkv * S * D;
         if ((st = check_nonfinite(h, k, v, nk, nk, s)) != KVC_OK) return st;
     }
@@ -1049,6 +1021,298 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         nexth[b] = st_h[b] + sl_h[b];
     }
     h->layer_version[layer] += 1;
+    return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_append_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                             const kvc_tensor* v, const kvc_tensor* out, void* stream) {
+    return append_attend_impl(h, layer, q, k, v, out, true, stream);
+}
+
+kvc_status kvc_prepare_attend(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                              const kvc_tensor* v, const kvc_tensor* out, kvc_ticket* ticket, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (!ticket) return fail(h, KVC_ERR_NULL, "ticket pointer is NULL");
+    kvc_status st = append_attend_impl(h, layer, q, k, v, out, false, stream);
+    if (st != KVC_OK) return st;
+    ticket->handle = h;
+    ticket->layer = layer;
+    ticket->reserved = 0;
+    ticket->version = h->layer_version[layer];
+    return KVC_OK;
+}
+
+kvc_status kvc_commit(kvc_handle* h, const kvc_ticket* tickets, int32_t n, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    if (n < 0) return fail(h, KVC_ERR_TICKET, "ticket count %d is negative", n);
+    if (n > 0 && !tickets) return fail(h, KVC_ERR_NULL, "ticket array is NULL");
+    const int L = h->cfg.layers, B = h->B();
+    std::vector<char> seen(L, 0);
+    for (int i = 0; i < n; ++i) {
+        const kvc_ticket& t = tickets[i];
+        if (t.handle != h) return fail(h, KVC_ERR_TICKET, "ticket %d was prepared by another cache", i);
+        if (t.layer < 0 || t.layer >= L) return fail(h, KVC_ERR_TICKET, "ticket %d names layer %d", i, t.layer);
+        if (seen[t.layer]) return fail(h, KVC_ERR_TICKET, "tickets repeat layer %d", t.layer);
+        seen[t.layer] = 1;
+        if (t.version != h->layer_version[t.layer])
+            return fail(h, KVC_ERR_TICKET, "ticket %d of layer %d is stale: the layer changed after it was prepared",
+                        i, t.layer);
+    }
+    if (n == 0) return KVC_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    for (int i0 = 0; i0 < n; i0 += kCommitMaxLayers) {
+        CommitLayers cl{};
+        cl.n = std::min(n - i0, kCommitMaxLayers);
+        for (int i = 0; i < cl.n; ++i) cl.layer[i] = tickets[i0 + i].layer;
+        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_commit_layers(h->len_d, h->next_d, cl, B, s); }));
+    }
+    for (int i = 0; i < n; ++i) {
+        const int l = tickets[i].layer;
+        h->layer_version[l] += 1;
+        for (int b = 0; b < B; ++b) {
+            h->len_h[(size_t)l * B + b] += 1;
+            h->next_h[(size_t)l * B + b] += 1;
+        }
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                              const kvc_tensor* v, const int32_t* start_pos, const int32_t* seqlen,
+                              const kvc_tensor* out, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    return kvc::prefill_impl(h, layer, q, k, v, start_pos, seqlen, out, stream, true);
+}
+
+// ---------------------------------------------------------------- host-buffer prefill
+
+namespace {
+
+// Shape, dtype and alignment of a [B, H, S?, d] tensor in HOST memory (pinned or pageable).
+kvc_status check_host_tensor(kvc_handle* h, const kvc_tensor* t, const char* name, kvc_status shape_err, int dtype,
+                             int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+    if (!t || !t->data) return fail(h, KVC_ERR_NULL, "%s tensor or its data pointer is NULL", name);
+    if (t->dtype != dtype)
+        return fail(h, KVC_ERR_DTYPE, "%s has dtype %s, the cache expects %s", name, dtype_name(t->dtype),
+                    dtype_name(dtype));
+    const int64_t want[4] = {d0, d1, d2, d3};
+    bool ok = t->ndim == 4;
+    for (int i = 0; ok && i < 4; ++i) ok = want[i] < 0 ? t->shape[i] > 0 : t->shape[i] == want[i];
+    if (!ok) {
+        int64_t shown[4];
+        for (int i = 0; i < 4; ++i) shown[i] = want[i] < 0 ? -1 : want[i];
+        return fail(h, shape_err, "%s must have shape %s, got %s", name, shape_str(shown, 4).c_str(),
+                    shape_str(t->shape, t->ndim < 0 ? 0 : (t->ndim > 4 ? 4 : t->ndim)).c_str());
+    }
+    if (((uintptr_t)t->data & 15u) != 0)
+        return fail(h, KVC_ERR_CONFIG, "%s data pointer is not 16-byte aligned", name);
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, t->data) != cudaSuccess) {
+        cudaGetLastError();   // older drivers: an unregistered host pointer
+        return KVC_OK;
+    }
+    if (attr.type == cudaMemoryTypeDevice)
+        return fail(h, KVC_ERR_CONFIG, "%s data is device memory; the host-buffer call takes host memory", name);
+    return KVC_OK;
+}
+
+// First non-finite element of `n` host elements of the storage dtype, or -1.
+int64_t first_nonfinite_host(const void* p, int64_t n, int dtype) {
+    if (dtype == KVC_BF16) {
+        const uint16_t* u = (const uint16_t*)p;
+        for (int64_t i = 0; i < n; ++i)
+            if ((u[i] & 0x7f80u) == 0x7f80u) return i;
+    } else if (dtype == KVC_F32) {
+        const uint32_t* u = (const uint32_t*)p;
+        for (int64_t i = 0; i < n; ++i)
+            if ((u[i] & 0x7f800000u) == 0x7f800000u) return i;
+    } else {
+        const uint64_t* u = (const uint64_t*)p;
+        for (int64_t i = 0; i < n; ++i)
+            if ((u[i] & 0x7ff0000000000000ull) == 0x7ff0000000000000ull) return i;
+    }
+    return -1;
+}
+
+// Rows 0 .. n-1 of every head of sequences [b0, b1) of a [B, H, S, d] tensor: one strided
+// copy per sequence (H runs of n rows, S rows apart).
+cudaError_t copy_rows(char* dst, const char* src, int b0, int b1, const int32_t* n, int H, int S, size_t row_bytes,
+                      cudaMemcpyKind kind, cudaStream_t st) {
+    const size_t pitch = (size_t)S * row_bytes;
+    for (int b = b0; b < b1; ++b) {
+        if (n[b] == 0) continue;
+        const size_t off = (size_t)b * H * pitch;
+        cudaError_t e = cudaMemcpy2DAsync(dst + off, pitch, src + off, pitch, (size_t)n[b] * row_bytes, (size_t)H,
+                                          kind, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tensor* q, const kvc_tensor* k,
+                                   const kvc_tensor* v, const int32_t* start_pos, const int32_t* seqlen,
+                                   const kvc_tensor* out, int32_t chunk_sequences, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    kvc_status st;
+    if ((st = check_layer(h, layer)) != KVC_OK) return st;
+    if (chunk_sequences < 0) return fail(h, KVC_ERR_CONFIG, "chunk_sequences is %d, must be >= 0", chunk_sequences);
+    const int B = h->B(), Hq = h->Hq(), Hkv = h->Hkv(), D = h->D(), C = h->C();
+    const int dt = h->cfg.dtype;
+    const bool need_q = out != nullptr || q != nullptr;
+    if (need_q && (st = check_host_tensor(h, q, "query", KVC_ERR_QUERY_SHAPE, dt, B, Hq, -1, D)) != KVC_OK) return st;
+    if (!need_q && (st = check_host_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, -1, D)) != KVC_OK) return st;
+    const int64_t S64 = need_q ? q->shape[2] : k->shape[2];
+    if (S64 > INT32_MAX) return fail(h, KVC_ERR_QUERY_SHAPE, "a chunk of %lld rows is too long", (long long)S64);
+    const int S = (int)S64;
+    if ((st = check_host_tensor(h, k, "key", KVC_ERR_KEY_SHAPE, dt, B, Hkv, S, D)) != KVC_OK) return st;
+    if ((st = check_host_tensor(h, v, "value", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, S, D)) != KVC_OK) return st;
+    if (out && (st = check_host_tensor(h, out, "output", KVC_ERR_OUTPUT_SHAPE, out_dtype(dt), B, Hq, S, D)) != KVC_OK)
+        return st;
+    if ((st = refresh_mirrors(h)) != KVC_OK) return st;
+    // The whole call is checked before any copy or launch, as kvc_prefill_suffix checks it.
+    const int32_t* lenh = &h->len_h[(size_t)layer * B];
+    const int32_t* nexth = &h->next_h[(size_t)layer * B];
+    std::vector<int32_t> sl(B), sp(B);
+    for (int b = 0; b < B; ++b) {
+        const int n = seqlen ? seqlen[b] : S;
+        if (n < 0 || n > S)
+            return fail(h, KVC_ERR_QUERY_SHAPE, "sequence %d declares %d rows, the chunk holds %d", b, n, S);
+        const int p = start_pos ? start_pos[b] : nexth[b];
+        if (lenh[b] + (int64_t)n > C)
+            return fail(h, KVC_ERR_FULL, "sequence %d of layer %d holds %d rows; %d more exceed the capacity %d", b,
+                        layer, lenh[b], n, C);
+        if (p < 0 || (int64_t)p + n > (h->rope ? (int64_t)h->max_positions : (int64_t)INT32_MAX))
+            return fail(h, KVC_ERR_POSITION, "sequence %d: positions %d .. %lld leave the %d-position table", b, p,
+                        (long long)p + n - 1, h->max_positions);
+        sl[b] = n;
+        sp[b] = p;
+    }
+    if (h->paged()) {
+        // counted for the whole call as one kvc_prefill_suffix counts it (an upper bound on
+        // what the chunks take one after another), so no chunk can run out of blocks
+        std::vector<int32_t> to(B);
+        for (int b = 0; b < B; ++b) to[b] = lenh[b] + sl[b];
+        const int64_t need = blocks_needed(h, lenh, to.data());
+        if (need > (int64_t)h->free_blocks.size())
+            return fail(h, KVC_ERR_FULL, "the block pool has %zu free blocks; the call needs %lld",
+                        h->free_blocks.size(), (long long)need);
+    }
+    const size_t esz = h->elem_size, osz = out_dtype(dt) == KVC_F64 ? 8 : 4;
+    const size_t row_bytes = (size_t)D * esz;
+    if (h->cfg.checked) {
+        const int64_t nkv = (int64_t)B * Hkv * S * D;
+        for (int which = 0; which < 2; ++which) {
+            const int64_t idx = first_nonfinite_host(which ? v->data : k->data, nkv, dt);
+            if (idx >= 0)
+                return fail(h, which ? KVC_ERR_NONFINITE_VALUE : KVC_ERR_NONFINITE_KEY,
+                            "%s element at flat index %lld is not finite; nothing was appended",
+                            which ? "value" : "key", (long long)idx);
+        }
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    // Device staging: q, k, v and the output, each laid out like the caller's buffer.
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t qb = need_q ? al((size_t)B * Hq * S * row_bytes) : 0;
+    const size_t kb = al((size_t)B * Hkv * S * row_bytes);
+    const size_t ob = out ? al((size_t)B * Hq * S * D * osz) : 0;
+    const size_t total = qb + 2 * kb + ob;
+    if (total > h->io_bytes) {
+        if (h->io_h2d) KVC_CUDA(h, cudaStreamSynchronize(h->io_h2d));
+        if (h->io_d2h) KVC_CUDA(h, cudaStreamSynchronize(h->io_d2h));
+        KVC_CUDA(h, cudaStreamSynchronize(s));
+        cudaFree(h->io_buf);
+        h->io_buf = nullptr;
+        h->io_bytes = 0;
+        if (cudaMalloc(&h->io_buf, total) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, KVC_ERR_ALLOC, "cannot allocate %zu bytes of staging for host buffers", total);
+        }
+        h->io_bytes = total;
+    }
+    if (!h->io_h2d) {
+        KVC_CUDA(h, cudaStreamCreateWithFlags(&h->io_h2d, cudaStreamNonBlocking));
+        KVC_CUDA(h, cudaStreamCreateWithFlags(&h->io_d2h, cudaStreamNonBlocking));
+        KVC_CUDA(h, cudaEventCreateWithFlags(&h->io_entry, cudaEventDisableTiming));
+        KVC_CUDA(h, cudaEventCreateWithFlags(&h->io_last, cudaEventDisableTiming));
+        KVC_CUDA(h, cudaEventRecord(h->io_last, h->io_d2h));
+    }
+    const int cs = chunk_sequences > 0 ? std::min(chunk_sequences, B) : std::max(1, (B + 7) / 8);
+    const int nchunks = (B + cs - 1) / cs;
+    while ((int)h->io_ev.size() < 2 * nchunks) {
+        cudaEvent_t e;
+        KVC_CUDA(h, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        h->io_ev.push_back(e);
+    }
+    char* dq = (char*)h->io_buf;
+    char* dk = dq + qb;
+    char* dv = dk + kb;
+    char* dout = dv + kb;
+    // The staging is rewritten only after the caller's earlier work and the previous
+    // call's output copies are done.
+    KVC_CUDA(h, cudaEventRecord(h->io_entry, s));
+    KVC_CUDA(h, cudaStreamWaitEvent(h->io_h2d, h->io_entry, 0));
+    KVC_CUDA(h, cudaStreamWaitEvent(h->io_h2d, h->io_last, 0));
+    // 1. every chunk's inputs, in chunk order, on the upload stream
+    for (int c = 0; c < nchunks; ++c) {
+        const int b0 = c * cs, b1 = std::min(B, b0 + cs);
+        if (need_q)
+            KVC_CUDA(h, copy_rows(dq, (const char*)q->data, b0, b1, sl.data(), Hq, S, row_bytes,
+                                  cudaMemcpyHostToDevice, h->io_h2d));
+        KVC_CUDA(h, copy_rows(dk, (const char*)k->data, b0, b1, sl.data(), Hkv, S, row_bytes, cudaMemcpyHostToDevice,
+                              h->io_h2d));
+        KVC_CUDA(h, copy_rows(dv, (const char*)v->data, b0, b1, sl.data(), Hkv, S, row_bytes, cudaMemcpyHostToDevice,
+                              h->io_h2d));
+        KVC_CUDA(h, cudaEventRecord(h->io_ev[2 * c], h->io_h2d));
+    }
+    // 2. each chunk's append and attention on the caller's stream once its inputs have
+    //    landed (the other sequences take 0 rows), then its output rows on the download stream
+    kvc_tensor tq{}, tk{}, tv{}, to{};
+    if (need_q) { tq = *q; tq.data = dq; }
+    tk = *k; tk.data = dk;
+    tv = *v; tv.data = dv;
+    if (out) { to = *out; to.data = dout; }
+    std::vector<int32_t> sl_c(B), sp_c(B);
+    for (int c = 0; c < nchunks; ++c) {
+        const int b0 = c * cs, b1 = std::min(B, b0 + cs);
+        int rows = 0;
+        for (int b = 0; b < B; ++b) {
+            const bool in = b >= b0 && b < b1;
+            sl_c[b] = in ? sl[b] : 0;
+            sp_c[b] = in ? sp[b] : h->next_h[(size_t)layer * B + b];
+            rows += sl_c[b];
+        }
+        if (rows == 0) continue;
+        KVC_CUDA(h, cudaStreamWaitEvent(s, h->io_ev[2 * c], 0));
+        // the stage's small argument arrays must not wait behind the bulk uploads on the
+        // copy engine: the SMs read them from the mapped ring slot instead
+        h->ring.by_kernel = true;
+        st = kvc::prefill_impl(h, layer, need_q ? &tq : nullptr, &tk, &tv, sp_c.data(), sl_c.data(),
+                               out ? &to : nullptr, s, false);
+        h->ring.by_kernel = false;
+        if (st != KVC_OK) return st;
+        if (out) {
+            KVC_CUDA(h, cudaEventRecord(h->io_ev[2 * c + 1], s));
+            KVC_CUDA(h, cudaStreamWaitEvent(h->io_d2h, h->io_ev[2 * c + 1], 0));
+            KVC_CUDA(h, copy_rows((char*)out->data, dout, b0, b1, sl.data(), Hq, S, (size_t)D * osz,
+                                  cudaMemcpyDeviceToHost, h->io_d2h));
+        }
+    }
+    // io_last follows every launch and output copy of this call (the next call's uploads
+    // wait for it before they overwrite the staging); the caller's stream waits for it too,
+    // so that its completion means the output rows are in host memory
+    KVC_CUDA(h, cudaEventRecord(h->io_entry, s));
+    KVC_CUDA(h, cudaStreamWaitEvent(h->io_d2h, h->io_entry, 0));
+    KVC_CUDA(h, cudaEventRecord(h->io_last, h->io_d2h));
+    KVC_CUDA(h, cudaStreamWaitEvent(s, h->io_last, 0));
     return KVC_OK;
 }
 

@@ -35,14 +35,19 @@ __host__ __device__ inline int64_t kv_row(const KvLayout& L, int b, int h, int s
 // positions, chunk lengths, cuts, work lists).  Each slot is reused only after
 // the event recorded behind its consumers has completed.
 struct ArgRing {
-    static constexpr int kSlots = 8;
+    // enough slots that a caller enqueuing a few steps ahead rarely waits for one
+    static constexpr int kSlots = 32;
     void* host[kSlots] = {};
+    void* mapped[kSlots] = {};   // device view of host[] (page-locked memory is mapped)
     void* dev[kSlots] = {};
     size_t cap[kSlots] = {};
     cudaEvent_t done[kSlots] = {};
     bool pending[kSlots] = {};
     int next = 0;
     int cur = -1;
+    // buffers replaced by larger ones; freed by destroy(), since freeing device memory
+    // would wait for the whole device in the middle of a pipeline
+    std::vector<void*> retired_host, retired_dev;
 
     cudaError_t init();
     void destroy();
@@ -50,6 +55,11 @@ struct ArgRing {
     cudaError_t acquire(size_t bytes, void** host_ptr);
     // Enqueues the copy of the acquired slot; *dev_ptr is its device copy.
     cudaError_t upload(size_t bytes, cudaStream_t stream, void** dev_ptr);
+    // Enqueues the copy of the acquired slot's first `bytes` to device memory `dst`.
+    cudaError_t copy(void* dst, size_t bytes, cudaStream_t stream);
+    // true: copies run as a small kernel reading the mapped slot (set while bulk copies
+    // occupy the host-to-device copy engine), else as copy-engine transfers
+    bool by_kernel = false;
     // Records the slot's release behind the work enqueued so far on `stream`.
     cudaError_t release(cudaStream_t stream);
 };
@@ -81,6 +91,14 @@ struct Handle {
     void* qrot_chunk = nullptr;    // [B][H_q][S][d_h] rotated queries of a chunk
     size_t qrot_chunk_bytes = 0;
     int* work_counter = nullptr;   // dynamic tile scheduler counter
+    // host-buffer prefill (kvc_prefill_suffix_host): device staging of the inputs and
+    // the output, the two copy streams and their events
+    void* io_buf = nullptr;
+    size_t io_bytes = 0;
+    cudaStream_t io_h2d = nullptr, io_d2h = nullptr;
+    std::vector<cudaEvent_t> io_ev;   // per chunk: inputs landed, results ready
+    cudaEvent_t io_entry = nullptr;   // the caller's stream at entry
+    cudaEvent_t io_last = nullptr;    // the last output copy of the previous call
     unsigned* lane_ticket = nullptr;  // [B*H_kv] split counters of the fused decode step
     unsigned* step_ticket = nullptr;  // [L] CTA counters of device-length decode steps
 
@@ -161,6 +179,7 @@ struct AppendLaunch {
     KvLayout kv;             // where stored rows live
 };
 cudaError_t launch_rope_append(int dtype, const AppendLaunch& a, cudaStream_t s);
+cudaError_t launch_copy_args(const void* src_mapped, void* dst, size_t bytes, cudaStream_t s);
 
 struct GenericAttendLaunch {
     const void* qrot;        // [B,H_q,S,d] float or double

@@ -10,6 +10,8 @@
 // nonfinite: [Ch37] listing "Own a fixed layer-bound cache, append one checked
 //           row, and reset logical length" rejects non-finite keys and values
 //           before they are stored; this finds the first such flat index.
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "kvc_internal.h"
 
@@ -103,6 +105,27 @@ cudaError_t launch_copy_blocks(char* K, char* V, size_t layer_bytes, int layers,
                                const int2* pairs, int npairs, cudaStream_t s) {
     if (npairs <= 0) return cudaSuccess;
     copy_blocks_kernel<<<(unsigned)npairs * 2 * layers, 256, 0, s>>>(K, V, layer_bytes, block_bytes, pairs, layers);
+    return cudaGetLastError();
+}
+
+// Small argument arrays read by the SMs straight from mapped page-locked host memory:
+// unlike a copy-engine transfer, this does not queue behind bulk host-to-device copies
+// that other streams have in flight.
+__global__ void copy_args_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t bytes) {
+    const size_t words = bytes / 16;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride)
+        reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    for (size_t i = words * 16 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < bytes; i += stride)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_copy_args(const void* src_mapped, void* dst, size_t bytes, cudaStream_t s) {
+    if (bytes == 0) return cudaSuccess;
+    if (((uintptr_t)src_mapped | (uintptr_t)dst) & 15u) return cudaErrorMisalignedAddress;
+    const size_t words = (bytes + 15) / 16;
+    const unsigned blocks = (unsigned)std::min<size_t>(64, (words + 255) / 256);
+    copy_args_kernel<<<blocks, 256, 0, s>>>((const uint8_t*)src_mapped, (uint8_t*)dst, bytes);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,25 @@ def tensor_desc(t):
     return d
 
 
+def host_tensor_desc(t):
+    """kvc_tensor descriptor of a contiguous CPU tensor (pinned for overlapped copies)."""
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("the host-buffer call takes CPU tensors")
+    if not t.is_contiguous():
+        raise ValueError("libkvc takes contiguous tensors")
+    if t.dtype not in TORCH_DTYPE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("rank must be at most 4")
+    d = L.kvc_tensor()
+    d.data = t.data_ptr()
+    d.dtype = TORCH_DTYPE[t.dtype]
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = s
+    return d
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -143,6 +162,27 @@ class KVCache:
         sl = L.int_array(seqlen) if seqlen is not None else None
         self._check(L.lib.kvc_prefill_suffix(self._h, layer, _ref(dq), ctypes.byref(dk),
                                              ctypes.byref(dv), sp, sl, _ref(do), _stream(stream)))
+        return out
+
+    def prefill_suffix_host(self, layer, q, k, v, start_pos=None, seqlen=None, out=True, chunk_sequences=0,
+                            stream=None, sync=True):
+        """kvc_prefill_suffix_host: q, k, v (and out) are CPU tensors, ideally pinned.  ``out``: a
+        CPU tensor, True (allocate a pinned one) or None/False (append only).  With ``sync`` the
+        stream is synchronised before returning, else ``out`` is valid once the stream completes."""
+        if out is True:
+            out = torch.empty(q.shape, dtype=self.out_dtype).pin_memory() if q is not None else None
+        elif out is False:
+            out = None
+        dq = host_tensor_desc(q) if q is not None else None
+        dk, dv = host_tensor_desc(k), host_tensor_desc(v)
+        do = host_tensor_desc(out) if out is not None else None
+        sp = L.int_array(start_pos) if start_pos is not None else None
+        sl = L.int_array(seqlen) if seqlen is not None else None
+        st = _stream(stream)
+        self._check(L.lib.kvc_prefill_suffix_host(self._h, layer, _ref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                                  sp, sl, _ref(do), int(chunk_sequences), st))
+        if sync:
+            (stream or torch.cuda.current_stream()).synchronize()
         return out
 
     def reset(self, stream=None):

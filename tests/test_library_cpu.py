@@ -24,7 +24,7 @@ def test_every_declared_symbol_is_exported(kvc_lib):
     for n in names:
         assert hasattr(kvc_lib.lib, n), n
     assert set(names) == set(kvc_lib.EXPORTS)
-    assert kvc_lib.lib.kvc_abi_version() == 3
+    assert kvc_lib.lib.kvc_abi_version() == 4
 
 
 def test_status_strings(kvc_lib):
@@ -76,6 +76,8 @@ def test_null_arguments(kvc_lib):
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_prepare_attend(None, 0, None, None, None, None, None, None)] == "KVC_ERR_NULL"
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_commit(None, None, 0, None)] == "KVC_ERR_NULL"
     assert kvc_lib.STATUS[kvc_lib.lib.kvc_sync_lengths(None)] == "KVC_ERR_NULL"
+    assert kvc_lib.STATUS[kvc_lib.lib.kvc_prefill_suffix_host(None, 0, None, None, None, None, None, None, 0,
+                                                             None)] == "KVC_ERR_NULL"
     kvc_lib.lib.kvc_destroy(None)
 
 
