@@ -78,34 +78,34 @@ __device__ __forceinline__ void rope_one(const AppendLaunch& a, int kind, int b,
             QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
             *reinterpret_cast<Pack<QO, P>*>(dst) = oq;
         }
-        return;
-    }
-    double xr[2 * P];
-#pragma unroll
-    for (int e = 0; e < P; ++e) {
-        const double x = S::to_f64(in.v[2 * e]);
-        const double y = S::to_f64(in.v[2 * e + 1]);
-        if (a.rope) {
-            const double2 cs = a.rope[t0 + e];
-            rope_pair_f64(x, y, cs.x, cs.y, xr[2 * e], xr[2 * e + 1]);
-        } else {
-            xr[2 * e] = x;
-            xr[2 * e + 1] = y;
-        }
-    }
-    if (kind == 1) {
-        Pack<T, P> o;
-#pragma unroll
-        for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<T>(xr[e]);
-        T* dst = (T*)a.K + kv_row(a.kv, b, h, slot) * a.d + 2 * P * c;
-        *reinterpret_cast<Pack<T, P>*>(dst) = o;
-        if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
     } else {
-        Pack<QO, P> o;
+        double xr[2 * P];
 #pragma unroll
-        for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<QO>(xr[e]);
-        QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
-        *reinterpret_cast<Pack<QO, P>*>(dst) = o;
+        for (int e = 0; e < P; ++e) {
+            const double x = S::to_f64(in.v[2 * e]);
+            const double y = S::to_f64(in.v[2 * e + 1]);
+            if (a.rope) {
+                const double2 cs = a.rope[t0 + e];
+                rope_pair_f64(x, y, cs.x, cs.y, xr[2 * e], xr[2 * e + 1]);
+            } else {
+                xr[2 * e] = x;
+                xr[2 * e + 1] = y;
+            }
+        }
+        if (kind == 1) {
+            Pack<T, P> o;
+#pragma unroll
+            for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<T>(xr[e]);
+            T* dst = (T*)a.K + kv_row(a.kv, b, h, slot) * a.d + 2 * P * c;
+            *reinterpret_cast<Pack<T, P>*>(dst) = o;
+            if (h == 0 && c == 0) a.positions[(int64_t)b * a.C + slot] = pos;
+        } else {
+            Pack<QO, P> o;
+#pragma unroll
+            for (int e = 0; e < 2 * P; ++e) o.v[e] = from_f64_rn<QO>(xr[e]);
+            QO* dst = (QO*)a.qrot + (((int64_t)b * a.Hq + h) * a.S + i) * a.d + 2 * P * c;
+            *reinterpret_cast<Pack<QO, P>*>(dst) = o;
+        }
     }
 }
 
