@@ -638,6 +638,17 @@ static void release_blocks(kvc_handle* h, int b, int keep) {
     }
 }
 
+// True while `s` records a CUDA graph (or when that cannot be told): decode launches are
+// then made without the programmatic-dependent-launch attribute.
+static bool stream_capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
 static kvc_status ensure_partials(kvc_handle* h, size_t splits) {
     if (h->part_splits >= splits) return KVC_OK;
     cudaDeviceSynchronize();
@@ -814,6 +825,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
         dl.merge_in_kernel = Hq / Hkv <= 16;
         dl.no_commit = !commit;
+        dl.pdl = !dev_len && !stream_capturing(s);
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         for (int b = 0; b < B && !dev_len; ++b) {
@@ -844,6 +856,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.out_bf16 = out_bf16;
         dl.window = W;
         dl.kv = h->layout();
+        dl.pdl = !stream_capturing(s);
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));

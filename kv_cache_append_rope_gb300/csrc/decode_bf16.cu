@@ -96,6 +96,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
     volatile int* s_err = (volatile int*)(empty + STAGES);   // s_err[1]: last-CTA flag
+    // Everything below may read what the previous kernel of the stream wrote (the
+    // previous step's row, lengths, split scratch): wait for it; and let the next
+    // step's CTAs take the slots this grid leaves as it drains.
+    grid_dependency_wait();
+    launch_dependents();
 
     // Fused step: the old length and position come from the host mirrors, so no
     // kernel of the step reads the length this kernel commits.
@@ -460,6 +465,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 }
 
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
+    grid_dependency_wait();
+    launch_dependents();
     const int qh = blockIdx.x;
     const int b = qh / a.Hq;
     int t, rows = a.split_rows;
@@ -486,6 +493,22 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     store_out(a, (int64_t)qh * D + threadIdx.x, O / L);
 }
 
+// Launch attributes: programmatic stream serialization when a.pdl is set.
+struct PdlConfig {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg{};
+    PdlConfig(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+    }
+};
+
 template <int MT, int MODE>
 cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<Cfg<MT>::STAGES>();
@@ -497,15 +520,15 @@ cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
         attr_set = true;
     }
     dim3 grid(a.max_splits, a.B * a.Hkv);
-    decode_bf16_kernel<MT, MODE><<<grid, THREADS, SMEM, s>>>(*a.tmK, *a.tmV, a);
-    return cudaGetLastError();
+    PdlConfig pc(grid, dim3(THREADS), SMEM, s, a.pdl != 0 && MODE != 2);
+    return cudaLaunchKernelEx(&pc.cfg, decode_bf16_kernel<MT, MODE>, *a.tmK, *a.tmV, a);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s) {
-    decode_combine_kernel<<<a.B * a.Hq, 128, 0, s>>>(a);
-    return cudaGetLastError();
+    PdlConfig pc(dim3(a.B * a.Hq), dim3(128), 0, s, a.pdl != 0);
+    return cudaLaunchKernelEx(&pc.cfg, decode_combine_kernel, a);
 }
 
 int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg<2>::MINB; }

@@ -224,6 +224,7 @@ struct DecodeLaunch {
     // (rows per split from its own length), and the grid's last CTA to read
     // the lengths commits them.
     int dev_len;
+    int pdl;                             // 1: launched as a programmatic dependent of the previous kernel
     unsigned* step_ticket;               // zero between launches
     int max_positions;
     int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
