@@ -52,8 +52,8 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # Summaries: profiles/decode_bf16_mha_small_full.md,
 # profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
 TRAFFIC = {
-    "mha_decode": ("ratio", (503521280.0 + 4513280.0) / 499236864.0),
-    "mqa_decode": ("ratio", (217871616.0 + 3592448.0) / 217403392.0),
+    "mha_decode": ("ratio", (503467264.0 + 4079104.0) / 499236864.0),
+    "mqa_decode": ("ratio", (217853184.0 + 3945984.0) / 217403392.0),
     "suffix": ("per_sequence", 375401472.0 + 174217472.0),
 }
 

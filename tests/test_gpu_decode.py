@@ -178,3 +178,51 @@ def test_fused_and_separate_decode_steps_agree(Hkv, split_rows):
         np.testing.assert_array_equal(x, y)
     assert caches[0].get_lengths(0) == caches[1].get_lengths(0)
     assert np.abs(outs[0] - outs[1]).max() < 5e-3
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 32), (32, 1)])
+def test_steps_fed_from_a_copy_stream_match_resident_inputs(Hq, Hkv):
+    """Decode steps whose inputs arrive on another stream (pinned host -> device copies,
+    double-buffered, ordered by events) give the results of steps on resident inputs:
+    a decode launch must never run ahead of the event wait that precedes it."""
+    need_gpu()
+    B, D, steps = 64, 128, 12
+    L0 = np.random.default_rng(5).integers(1, 400, size=B).tolist()
+    T = max(L0) + steps
+    qd, kd, vd = (device_tensor(W.normal_np((B, H, T, D), 80 + i), "bf16") for i, H in enumerate((Hq, Hkv, Hkv)))
+    idx = lambda i: torch.tensor([l + i for l in L0], device="cuda")
+    rows = lambda x, i: x[torch.arange(B, device="cuda"), :, idx(i)][:, :, None, :].contiguous()
+    caches = []
+    for _ in range(2):
+        c = KVCache(B, Hq, 512, D, heads_kv=Hkv, rope_base=BASE)
+        c.prefill_suffix(0, None, kd[:, :, :max(L0)].contiguous(), vd[:, :, :max(L0)].contiguous(),
+                         seqlen=L0, out=False)
+        caches.append(c)
+    # resident inputs
+    want = [caches[0].append_attend(0, rows(qd, i), rows(kd, i), rows(vd, i)) for i in range(steps)]
+    # the same steps fed through a copy stream from pinned host memory, two device buffers
+    host = [[rows(x, i).cpu().pin_memory() for x in (qd, kd, vd)] for i in range(steps)]
+    dev = [[torch.empty_like(t, device="cuda") for t in host[0]] for _ in range(2)]
+    outs = torch.empty((steps,) + tuple(want[0].shape), dtype=torch.float32, device="cuda")
+    compute, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    copy.wait_stream(compute)
+    for i in range(steps):
+        s = i % 2
+        with torch.cuda.stream(copy):
+            if i >= 2:
+                copy.wait_event(consumed[s])
+            for d, h in zip(dev[s], host[i]):
+                d.copy_(h, non_blocking=True)
+            uploaded[s].record(copy)
+        compute.wait_event(uploaded[s])
+        caches[1].append_attend(0, *dev[s], out=outs[i], stream=compute)
+        consumed[s].record(compute)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        assert torch.equal(outs[i], want[i]), i
+    for x, y in zip(storage_np(caches[0]), storage_np(caches[1])):
+        np.testing.assert_array_equal(x, y)
+    for c in caches:
+        c.check()
