@@ -397,7 +397,7 @@ typedef enum kvc_option {
                                       issues no loads, so the consumers' bounded waits give up (about 1 s)
                                       and the step reports a device error through kvc_check; the step's
                                       outputs are undefined and the cache should then be reset */
-    KVC_OPT_DEVICE_LENGTHS = 7     /* 1 = decode steps read the lengths and next positions from device memory
+    KVC_OPT_DEVICE_LENGTHS = 7,    /* 1 = decode steps read the lengths and next positions from device memory
                                       instead of the host mirrors, so that the launches of a step do not
                                       depend on them and can be captured in a CUDA graph and replayed:
                                       kvc_append_attend then enqueues one launch (two with more than 16
@@ -414,6 +414,12 @@ typedef enum kvc_option {
                                       device and read the lengths back.  Paged storage cannot use it
                                       (blocks are taken on the host as rows are appended):
                                       KVC_ERR_CONFIG. */
+    KVC_OPT_DECODE_PDL = 8         /* 1 (default) = bf16 d_h = 128 decode and merge kernels are launched as
+                                      programmatic dependents of the previous kernel in the stream (each
+                                      CTA waits for it before touching global memory), so that a step's
+                                      CTAs take the slots the previous step frees as it drains; 0 = plain
+                                      launches.  Never used while the stream captures a graph or with
+                                      KVC_OPT_DEVICE_LENGTHS. */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

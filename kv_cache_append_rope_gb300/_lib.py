@@ -25,6 +25,7 @@ DTYPES = {"bf16": 0, "f32": 1, "f64": 2}
 OPT_DECODE_SPLIT_ROWS, OPT_FORCE_GENERIC, OPT_SUFFIX_KERNEL, OPT_TIMING, OPT_DECODE_FUSED = 1, 2, 3, 4, 5
 OPT_TEST_STALL = 6
 OPT_DEVICE_LENGTHS = 7
+OPT_DECODE_PDL = 8
 KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "generic_attend": 4,
            "bookkeeping": 5}
 

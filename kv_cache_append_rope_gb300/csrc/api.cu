@@ -825,7 +825,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.rope_f = h->rope_f; dl.rope = h->rope; dl.lane_ticket = h->lane_ticket;
         dl.merge_in_kernel = Hq / Hkv <= 16;
         dl.no_commit = !commit;
-        dl.pdl = !dev_len && !stream_capturing(s);
+        dl.pdl = h->opt_decode_pdl && !dev_len && !stream_capturing(s);
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         for (int b = 0; b < B && !dev_len; ++b) {
@@ -856,7 +856,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         dl.out_bf16 = out_bf16;
         dl.window = W;
         dl.kv = h->layout();
-        dl.pdl = !stream_capturing(s);
+        dl.pdl = h->opt_decode_pdl && !stream_capturing(s);
         dl.test_stall = (int)h->opt_test_stall;
         h->opt_test_stall = 0;
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
@@ -1547,6 +1547,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_TEST_STALL:
             h->opt_test_stall = value != 0;
+            return KVC_OK;
+        case KVC_OPT_DECODE_PDL:
+            h->opt_decode_pdl = value != 0;
             return KVC_OK;
         case KVC_OPT_DEVICE_LENGTHS: {
             if (value && h->paged())

@@ -135,6 +135,7 @@ struct Handle {
     int64_t opt_decode_fused = 1;
     int64_t opt_test_stall = 0;
     int64_t opt_device_lengths = 0;
+    int64_t opt_decode_pdl = 1;
     std::vector<uint64_t> layer_version;  // [L] bumped by every change of a layer's state or staged slot
     bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 

@@ -226,3 +226,32 @@ def test_steps_fed_from_a_copy_stream_match_resident_inputs(Hq, Hkv):
         np.testing.assert_array_equal(x, y)
     for c in caches:
         c.check()
+
+
+@pytest.mark.parametrize("Hkv", [32, 1])
+def test_dependent_launch_option_changes_no_result(Hkv):
+    """KVC_OPT_DECODE_PDL only changes how consecutive decode launches overlap: outputs,
+    stored rows and lengths are identical with it on and off."""
+    need_gpu()
+    B, Hq, D, steps = 16, 32, 128, 6
+    L0 = np.random.default_rng(9).integers(1, 700, size=B).tolist()
+    T = max(L0) + steps
+    qd, kd, vd = (device_tensor(W.normal_np((B, H, T, D), 95 + i), "bf16") for i, H in enumerate((Hq, Hkv, Hkv)))
+    idx = lambda i: torch.tensor([l + i for l in L0], device="cuda")
+    rows = lambda x, i: x[torch.arange(B, device="cuda"), :, idx(i)][:, :, None, :].contiguous()
+    outs = []
+    caches = []
+    for pdl in (1, 0):
+        c = KVCache(B, Hq, 1024, D, heads_kv=Hkv, rope_base=BASE)
+        c.set_option(L.OPT_DECODE_PDL, pdl)
+        c.prefill_suffix(0, None, kd[:, :, :max(L0)].contiguous(), vd[:, :, :max(L0)].contiguous(),
+                         seqlen=L0, out=False)
+        outs.append([c.append_attend(0, rows(qd, i), rows(kd, i), rows(vd, i)) for i in range(steps)])
+        caches.append(c)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    assert caches[0].get_lengths(0) == caches[1].get_lengths(0)
+    for x, y in zip(storage_np(caches[0]), storage_np(caches[1])):
+        np.testing.assert_array_equal(x, y)
+    for c in caches:
+        c.check()
