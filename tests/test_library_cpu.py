@@ -127,3 +127,30 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     with pytest.raises(ImportError):
         L._load()
     importlib.reload(L)
+
+
+def test_host_buffer_descriptors():
+    """The binding of kvc_prefill_suffix_host describes CPU tensors as they are (pointer,
+    dtype, rank, shape) and refuses what the call cannot take."""
+    import torch
+
+    from kv_cache_append_rope_gb300 import _lib as L
+    from kv_cache_append_rope_gb300.kvc import host_tensor_desc
+    t = torch.zeros((2, 4, 5, 128), dtype=torch.bfloat16)
+    d = host_tensor_desc(t)
+    assert d.data == t.data_ptr() and d.ndim == 4 and list(d.shape) == [2, 4, 5, 128]
+    assert d.dtype == L.DTYPES["bf16"]
+    with pytest.raises(ValueError):
+        host_tensor_desc(t.transpose(1, 2))                      # not contiguous
+    with pytest.raises(ValueError):
+        host_tensor_desc(torch.zeros((2, 4), dtype=torch.int8))  # no such storage dtype
+    with pytest.raises(ValueError):
+        host_tensor_desc(torch.zeros((1, 1, 1, 1, 2)))           # rank 5
+    with pytest.raises(ValueError):
+        host_tensor_desc(np.zeros((2, 4)))                       # not a tensor
+
+
+def test_host_buffer_call_rejects_a_null_handle_and_bad_stage_size(kvc_lib):
+    # no handle: rejected before anything else (no GPU needed)
+    st = kvc_lib.lib.kvc_prefill_suffix_host(None, 0, None, None, None, None, None, None, -1, None)
+    assert kvc_lib.STATUS[st] == "KVC_ERR_NULL"
