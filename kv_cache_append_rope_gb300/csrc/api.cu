@@ -934,11 +934,44 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
     }
     // Attention kernel: the tensor-core tile kernel for bf16 with d_h = 128, else the generic one.
     const bool tc_ok = dt == KVC_BF16 && D == 128 && h->have_tmaps;
-    if (out && h->opt_suffix_kernel == 2 && !tc_ok)
+    if (out && h->opt_suffix_kernel >= 2 && !tc_ok)
         return fail(h, KVC_ERR_CONFIG, "the tensor-core suffix kernel needs bf16 storage and d_h = 128");
     const bool use_tc = out && tc_ok && !h->opt_force_generic && h->opt_suffix_kernel != 1;
+    const bool use_tc2 = use_tc && h->opt_suffix_kernel == 3 && !h->paged();
     std::vector<int4> work;
-    if (use_tc) {
+    if (use_tc2) {
+        // one item per (sequence, query head, four 128-row query tiles): a pair of CTAs
+        const int W = h->cfg.window;
+        auto range = [&](int b, int qt, int& lo, int& hi) {
+            if (qt * 128 >= sl_h[b]) { lo = hi = 0; return; }
+            const int q_end = std::min(qt * 128 + 128, sl_h[b]);
+            lo = W > 0 ? std::max(0, lenh[b] + qt * 128 - W + 1) / 128 : 0;
+            hi = (lenh[b] + q_end + 127) / 128;
+        };
+        for (int b = 0; b < B; ++b)
+            for (int hq = 0; hq < Hq; ++hq)
+                for (int qd = 0; qd * 512 < sl_h[b]; ++qd) {
+                    int wgt = 0;
+                    for (int X = 0; X < 2; ++X) {
+                        int l0, h0, l1, h1;
+                        range(b, 4 * qd + 2 * X, l0, h0);
+                        range(b, 4 * qd + 2 * X + 1, l1, h1);
+                        if (h0 > 0) wgt += 2 * (std::max(h0, h1) - l0);
+                    }
+                    work.push_back(make_int4(b, hq, qd, wgt));
+                }
+        std::vector<int64_t> gw((size_t)B * Hq, 0);
+        for (const int4& t : work) gw[(size_t)t.x * Hq + t.y] += t.w;
+        std::stable_sort(work.begin(), work.end(), [&](const int4& x, const int4& y) {
+            const int64_t wx = gw[(size_t)x.x * Hq + x.y], wy = gw[(size_t)y.x * Hq + y.y];
+            if (wx != wy) return wx > wy;
+            if (x.x != y.x) return x.x < y.x;
+            if (x.y != y.y) return x.y < y.y;
+            return x.w > y.w;
+        });
+        if ((uint64_t)B * Hq * S > (uint64_t)INT32_MAX)
+            return fail(h, KVC_ERR_ELEMENT_OVERFLOW, "B * H_q * S must fit in 31 bits for the tile kernel");
+    } else if (use_tc) {
         // one item per (sequence, query head, pair of 128-row query tiles); its weight is
         // the number of (query tile, key tile) products, key tiles from the window start
         // (tile 0 without a window) to the tile of the query tile's last row
@@ -1004,7 +1037,19 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
     ap.kv = h->layout();
     // Without an output the query heads are skipped (Hq = 0 in the launch).
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
-    if (out && use_tc && !work.empty()) {
+    if (out && use_tc2 && !work.empty()) {
+        SuffixLaunch2 sl{};
+        if (!encode_rows_map(&sl.tmQ, h->qrot_chunk, (uint64_t)B * Hq * S, 128))
+            return fail(h, KVC_ERR_CUDA, "cannot encode the query tensor map");
+        sl.tmK64 = h->tmap_k[layer];
+        sl.tmV128 = h->tmap_v128[layer];
+        sl.slot0 = h->len_layer(layer); sl.seqlen = seqlen_d;
+        sl.work = work_d; sl.n_work = (int)work.size();
+        sl.out = (float*)out->data; sl.err = h->err_d;
+        sl.B = B; sl.Hq = Hq; sl.Hkv = Hkv; sl.S = S; sl.C = C; sl.window = h->cfg.window;
+        sl.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+        KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc2(sl, (int)work.size(), s); }));
+    } else if (out && use_tc && !work.empty()) {
         SuffixLaunch sl{};
         if (!encode_rows_map(&sl.tmQ, h->qrot_chunk, (uint64_t)B * Hq * S, 128))
             return fail(h, KVC_ERR_CUDA, "cannot encode the query tensor map");
@@ -1536,7 +1581,7 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             h->opt_force_generic = value != 0;
             return KVC_OK;
         case KVC_OPT_SUFFIX_KERNEL:
-            if (value < 0 || value > 2) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1 or 2");
+            if (value < 0 || value > 3) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1, 2 or 3");
             h->opt_suffix_kernel = value;
             return KVC_OK;
         case KVC_OPT_TIMING:

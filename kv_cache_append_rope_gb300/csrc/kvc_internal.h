@@ -268,6 +268,23 @@ struct SuffixLaunch {
     float scale_log2;            // log2(e) / sqrt(d_h)
 };
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);
+
+// Pair-of-SMs tile kernel (cta_group::2): a cluster of two CTAs per work item.
+struct SuffixLaunch2 {
+    CUtensorMap tmQ;      // rotated queries [B*Hq*S, 128] bf16, 128-row x 64-col boxes
+    CUtensorMap tmK64;    // one layer's keys [B*Hkv*C, 128], 64-row x 64-col boxes
+    CUtensorMap tmV128;   // one layer's values, 128-row x 64-col boxes
+    const int32_t* slot0;
+    const int32_t* seqlen;
+    const int4* work;     // (b, h, quad of query tiles, weight)
+    int n_work;
+    float* out;
+    uint32_t* err;
+    int B, Hq, Hkv, S, C, window;
+    float scale_log2;
+};
+
+cudaError_t launch_suffix_tc2(const SuffixLaunch2& a, int items, cudaStream_t s);
 int suffix_tc_grid(int sms);
 
 }  // namespace kvc

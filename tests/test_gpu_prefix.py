@@ -32,6 +32,9 @@ def make_inputs(B, Hq, Hkv, T, D, dtype, seed):
     ("bf16", 128, 4, 4, 0, 300, [150, 0, 257]),      # tensor-core tile kernel (automatic)
     ("bf16", 128, 8, 2, 2, 300, [150, 0, 257]),      # tile kernel, grouped heads
     ("bf16", 128, 2, 1, 2, 1500, [1200, 37, 640]),   # tile kernel, many key tiles per query tile
+    ("bf16", 128, 4, 4, 3, 300, [150, 0, 257]),      # pair-of-SMs tile kernel
+    ("bf16", 128, 8, 2, 3, 300, [150, 0, 257]),
+    ("bf16", 128, 2, 1, 3, 1500, [1200, 37, 640]),
 ])
 def test_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, T, cuts):
     need_gpu()
