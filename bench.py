@@ -337,6 +337,22 @@ class DecodeBench:
                 break
         return t_total, done_bytes, f"{n} (b, kv-head) lanes x {self.steps} decode steps (all {G} query heads each)"
 
+    def one_thread_sample(self):
+        """The oracle call of one lane of median old length, for a one-thread timing:
+        (kind, arrays, bytes, description)."""
+        c = self.cfg
+        G = c["Hq"] // c["Hkv"]
+        b = int(np.argsort(self.L0)[len(self.L0) // 2])
+        L0 = int(self.L0[b])
+        k = np.concatenate([self.k_prefix[b, 0, :L0].double().cpu().numpy(),
+                            self.k[:, b, 0, 0].double().cpu().numpy()])[None]
+        v = np.concatenate([self.v_prefix[b, 0, :L0].double().cpu().numpy(),
+                            self.v[:, b, 0, 0].double().cpu().numpy()])[None]
+        q = self.q[:, b, 0:G, 0].double().cpu().numpy()
+        work = float(((L0 + 1 + np.arange(self.steps)) * c["D"] * 2 * 2).sum())
+        return ("decode", {"q": q, "k": k, "v": v, "L0": np.int64(L0)}, work,
+                f"one (b, kv-head) lane, old length {L0}, x {self.steps} decode steps (all {G} query heads)")
+
 
 # ----------------------------------------------------------------- suffix workload
 
@@ -428,6 +444,19 @@ class SuffixBench:
         flops = float(sum(4 * self.cfg["D"] * (cut + r + 1) for r in rows))
         return dt, flops, f"{rows.size} suffix rows of one (b, h) lane against the full masked prefix"
 
+    def one_thread_sample(self):
+        """256 suffix rows of the same lane, for a one-thread timing: (kind, arrays, flops, description)."""
+        b, h = int(np.argmax(self.cuts)), 0
+        cut = self.cuts[b]
+        S = self.seqlen[b]
+        rows = np.arange(0, S, max(1, S // 256))[:256]
+        k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(), self.k[b, h, :S].double().cpu().numpy()])
+        v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(), self.v[b, h, :S].double().cpu().numpy()])
+        q = self.q[b, h:h + 1, :S].double().cpu().numpy()
+        flops = float(sum(4 * self.cfg["D"] * (cut + r + 1) for r in rows))
+        arrays = {"q": q, "k": k[None], "v": v[None], "T": np.int64(self.T), "cut": np.int64(cut), "rows": rows}
+        return "suffix", arrays, flops, f"{rows.size} suffix rows of one (b, h) lane against the full masked prefix"
+
 
 # ----------------------------------------------------------------- driver
 
@@ -470,6 +499,34 @@ def cpu_threads():
         if os.environ.get(var, "").isdigit():
             return int(os.environ[var])
     return os.cpu_count()
+
+
+# One oracle call per kind, as run in a fresh interpreter (arrays come from an .npz file).
+_ONE_CORE_CALLS = {
+    "decode": "A.decode_steps_reference(z['q'], z['k'], z['v'], int(z['L0']), 10000.0, 'bf16')",
+    "suffix": "A.suffix_reference(z['q'], z['k'], z['v'], np.arange(int(z['T'])), int(z['cut']), 10000.0, "
+              "'bf16', rows=z['rows'])",
+}
+
+
+def oracle_seconds_one_thread(kind, arrays, timeout_s=120):
+    """Seconds the oracle takes for one call of `kind` on `arrays` in a fresh interpreter
+    limited to one BLAS/OpenMP thread (so the oracle runs on one core)."""
+    import subprocess
+    import sys
+    import tempfile
+    root = os.path.dirname(os.path.abspath(__file__))
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "sample.npz")
+        np.savez(path, **arrays)
+        code = ("import sys, time\nimport numpy as np\n"
+                f"sys.path.insert(0, {root!r})\nfrom oracle import attention as A\n"
+                f"z = np.load({path!r})\nt0 = time.perf_counter()\n{_ONE_CORE_CALLS[kind]}\n"
+                "print(time.perf_counter() - t0)\n")
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=timeout_s, check=True)
+        return float(r.stdout.strip().splitlines()[-1])
 
 
 def run_ours(args, name, world, rank, local):
@@ -561,6 +618,14 @@ def run_ours(args, name, world, rank, local):
         secs, work, sample = bench.oracle_sample()
         cpu = {"value": round(work / (1e9 if unit == "GB/s" else 1e12) / secs, 6), "unit": unit,
                "cores": cpu_threads(), "kind": "oracle", "sample": sample, "seconds": round(secs, 2)}
+        # the same oracle on one core (a fresh interpreter with one BLAS/OpenMP thread)
+        try:
+            kind, arrays, work1, sample1 = bench.one_thread_sample()
+            secs1 = oracle_seconds_one_thread(kind, arrays)
+            cpu["one_core"] = {"value": round(work1 / (1e9 if unit == "GB/s" else 1e12) / secs1, 6),
+                               "unit": unit, "cores": 1, "sample": sample1, "seconds": round(secs1, 2)}
+        except Exception as e:   # reported, never fatal: the line stands without it
+            cpu["one_core"] = {"unavailable": f"{type(e).__name__}: {str(e)[:120]}"}
 
     cache.check()
     line = {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
