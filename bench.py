@@ -49,8 +49,6 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # scaled to a full launch: decode traffic grows with the K/V bytes streamed
 # (ratio to the algorithmic bytes), the tile kernel's with the number of
 # sequences (each sequence's K/V comes from DRAM about once, then from L2).
-# Summaries: profiles/decode_bf16_mha_small_full.md,
-# profiles/decode_bf16_mqa_small_full.md, profiles/suffix_tc_b1_full.md.
 TRAFFIC = {
     "mha_decode": ("ratio", (503467264.0 + 4079104.0) / 499236864.0),
     "mqa_decode": ("ratio", (217853184.0 + 3945984.0) / 217403392.0),

@@ -17,7 +17,7 @@ Definitions followed (cited by page title and section / listing title):
   "哪些东西必须一起裁剪": after truncation to ``cut`` the suffix is computed
   against the retained prefix, continuing at position ``cut``.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * The cache holds rows in its storage dtype, so attention reads the rounded
   rotated key and rounded value; the query is rotated in float64 and not

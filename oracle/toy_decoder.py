@@ -4,7 +4,8 @@
 16, vocabulary 32, float64, sinusoidal absolute positions, tanh residual, no
 training, no FFN, no LayerNorm.  The architecture itself belongs to an earlier
 article of that series and is not printed, so this module takes the plainest
-reading (listed in DESIGN.md):
+reading; the page publishes no weights either, so this architecture is parity
+unpinned (only its internal invariants are checked):
 
 * h = E[id] + PE(position), PE the sinusoid of "Attention Is All You Need":
   PE[p, 2i] = sin(p / 10000**(2i/d)), PE[p, 2i+1] = cos(p / 10000**(2i/d));

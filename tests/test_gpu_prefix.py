@@ -12,7 +12,7 @@ from kv_cache_append_rope_gb300 import workloads as W
 from kv_cache_append_rope_gb300.kvc import KVCache, KVCError
 from oracle import attention as A
 from oracle import prefix as P
-from oracle.toy_decoder import ToyDecoder
+from oracle.toy_decoder import ToyDecoder, sinusoidal_positions
 
 pytestmark = pytest.mark.gpu
 BASE = 10000.0
@@ -138,14 +138,8 @@ def test_stale_next_position_negative_control():
 # ---- the prefix-reuse page's 2-layer decoder, attention through libkvc -------------
 
 def _pe_torch(positions, d):
-    """Additive sinusoidal positions, written for the GPU harness (torch, f64)."""
-    pos = torch.as_tensor(positions, dtype=torch.float64, device="cuda")[:, None]
-    i = torch.arange(0, d, 2, dtype=torch.float64, device="cuda")[None, :]
-    ang = pos / torch.pow(torch.tensor(10000.0, dtype=torch.float64, device="cuda"), i / d)
-    pe = torch.zeros(pos.shape[0], d, dtype=torch.float64, device="cuda")
-    pe[:, 0::2] = torch.sin(ang)
-    pe[:, 1::2] = torch.cos(ang)
-    return pe
+    """The oracle's additive sinusoid (pinned by tests/test_oracle_sinusoid.py), on the GPU."""
+    return torch.from_numpy(sinusoidal_positions(positions, d)).to("cuda")
 
 
 class GpuToyDecoder:
