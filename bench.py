@@ -1,9 +1,14 @@
 #!/usr/bin/env python
 """Throughput of cached incremental attention on GB300 through libkvc's C ABI.
 
+The default run prints one JSON line: the headline workload (mha_decode) and,
+under "workloads", the three other configurations measured the same way
+(gqa_decode, mqa_decode, suffix), each with its own value, roofline, CPU
+baseline, end-to-end number and clocks.
+
 Workloads (seeded, synthetic; sizes as the pages' workloads are stated):
 
-* mha_decode (default, headline): B = 32, H = 32, d_h = 128, bf16, C = 8192,
+* mha_decode (headline): B = 32, H = 32, d_h = 128, bf16, C = 8192,
   old lengths uniform in [1, 8128], 64 decode steps.  One bench step =
   kvc_truncate back to the old lengths + 64 kvc_append_attend calls.  Metric:
   K/V bytes the attention must read (every retained row of every lane at every
@@ -24,8 +29,13 @@ takes the pinned host buffers and overlaps each stage of sequences' copies
 with another stage's work).  `roofline` times the dominant kernel
 with CUDA events recorded by the library around each launch on its stream,
 in a second pass over the same number of steps (so that the event records do
-not weigh on `value`).
-`cpu_baseline` times the float64 oracle on a bounded sample on the host.
+not weigh on `value`); per-launch events break the overlap of consecutive
+dependent launches, so `roofline.step_frac` also divides the same algorithmic
+work by the whole step's time (`ms_per_step`).
+`cpu_baseline` times the float64 oracle on a bounded sample, one oracle process
+per host core side by side (`cores`), plus `one_core` (one process alone).
+`--impl reference` times that oracle as the reference arm; it builds the same
+seeded inputs with torch and never loads libkvc.
 """
 import argparse
 import json
@@ -62,8 +72,10 @@ def parse():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="mha_decode",
-                   choices=["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix", "all"])
+    p.add_argument("--workload", default="default",
+                   choices=["default", "mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix", "all"],
+                   help="default: one line, mha_decode with gqa_decode, mqa_decode and suffix under "
+                        "'workloads'; all: one line per workload")
     p.add_argument("--block-rows", type=int, default=0,
                    help="paged storage with blocks of this many rows (a multiple of 64); 0 = contiguous")
     p.add_argument("--split-rows", type=int, default=0,
@@ -80,7 +92,15 @@ def parse():
     return p.parse_args()
 
 
+# GB300 datasheet figures (dense): HBM3e bandwidth and bf16 tensor throughput
+NOMINAL_HBM_GBS, NOMINAL_BF16_TFLOPS = 7900.0, 2250.0
+# sub-workloads of the default line
+SUB_WORKLOADS = ("gqa_decode", "mqa_decode", "suffix")
+
+
 def peaks():
+    """Roofline denominators: the measured copy rate (read + write GB/s of a device copy)
+    and the measured cuBLAS bf16 burst rate, else the fallback figures."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
@@ -164,28 +184,35 @@ def gpu_index(local_rank):
 # ----------------------------------------------------------------- decode workloads
 
 class DecodeBench:
-    def __init__(self, name, device, batch=0, graph=False, block_rows=0):
+    """A decode workload.  ``with_cache`` False (the reference arm) draws the same seeded
+    inputs and builds no libkvc cache (the library is never loaded)."""
+
+    def __init__(self, name, device, batch=0, graph=False, block_rows=0, with_cache=True):
         from kv_cache_append_rope_gb300 import workloads as W
-        from kv_cache_append_rope_gb300.kvc import KVCache
         cfg = dict(W.CONFIGS[name])
         if batch:
             cfg["B"] = batch
-        self.name, self.cfg, self.device = name, cfg, device
+        self.name, self.cfg, self.device, self.block_rows = name, cfg, device, block_rows
         B, Hq, Hkv, D, C, steps = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["C"], cfg["steps"]
         self.L0 = W.old_lengths(cfg["seed"], B, cfg["lo"], cfg["hi"], C, steps)
-        self.cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype="bf16", rope_base=10000.0,
-                             device=device.index or 0, block_rows=block_rows)
+        self.cache = None
+        if with_cache:
+            from kv_cache_append_rope_gb300.kvc import KVCache
+            self.cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype="bf16", rope_base=10000.0,
+                                 device=device.index or 0, block_rows=block_rows)
         S = int(self.L0.max())
         seed = cfg["seed"] * 1000
         # unrotated prefix rows (kept for the oracle sample), appended without attending
         self.k_prefix = W.normal((B, Hkv, S, D), seed + 1, device=device)
         self.v_prefix = W.normal((B, Hkv, S, D), seed + 2, device=device)
-        self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, seqlen=self.L0.tolist(), out=False)
+        if with_cache:
+            self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, seqlen=self.L0.tolist(), out=False)
         self.q = W.normal((steps, B, Hq, 1, D), seed + 3, device=device)
         self.k = W.normal((steps, B, Hkv, 1, D), seed + 4, device=device)
         self.v = W.normal((steps, B, Hkv, 1, D), seed + 5, device=device)
-        self.out = torch.empty((steps, B, Hq, 1, D), dtype=torch.float32, device=device)
-        torch.cuda.synchronize(device)
+        self.out = torch.empty((steps, B, Hq, 1, D), dtype=torch.float32, device=device) if with_cache else None
+        if device.type == "cuda":
+            torch.cuda.synchronize(device)
         # algorithmic K/V bytes read by attention over the 64 steps: every lane reads t rows of K and V
         t = self.L0[None, :] + 1 + np.arange(steps)[:, None]          # [steps, B]
         self.kv_bytes_per_call = (t.sum(axis=1) * Hkv * D * 2 * 2).astype(np.float64)
@@ -194,7 +221,7 @@ class DecodeBench:
         self.io_bytes = float(steps * B * (Hq * D * 2 + 2 * Hkv * D * 2 + 2 * Hkv * D * 2 + Hq * D * 4))
         self.steps = steps
         self.graph, self.graph_launches, self.replays = None, 0, 0
-        if graph:
+        if graph and with_cache:
             self.capture()
 
     def step(self):
@@ -307,81 +334,72 @@ class DecodeBench:
                  f"{self.kv_bytes / 1e9:.2f} GB; L2 not flushed between bench steps"),
                 "launch": f"CUDA graph of the {self.steps} decode calls, lengths on the device" if self.graph is not None
                 else "one kvc_append_attend call per decode step",
-                "storage": (f"paged, {self.cache.config.block_rows}-row blocks" if self.cache.config.block_rows
-                            else "contiguous")}
+                "storage": (f"paged, {self.block_rows}-row blocks" if self.block_rows else "contiguous")}
 
-    def oracle_sample(self, budget_s=15.0):
-        """Oracle decode of sampled lanes (all steps); returns (seconds, bytes, description)."""
-        from oracle import attention as A
-        c = self.cfg
-        B, G = c["B"], c["Hq"] // c["Hkv"]
-        order = np.argsort(self.L0)
-        lanes = [int(order[0]), int(order[-1])] + [int(b) for b in order[1:-1][::max(1, B // 6)]]
-        done_bytes, t_total, n = 0.0, 0.0, 0
-        for b in lanes:
-            L0 = int(self.L0[b])
-            hk = 0
-            k = np.concatenate([self.k_prefix[b, hk, :L0].double().cpu().numpy(),
-                                self.k[:, b, hk, 0].double().cpu().numpy()])[None]
-            v = np.concatenate([self.v_prefix[b, hk, :L0].double().cpu().numpy(),
-                                self.v[:, b, hk, 0].double().cpu().numpy()])[None]
-            q = self.q[:, b, hk * G:(hk + 1) * G, 0].double().cpu().numpy()
-            t0 = time.perf_counter()
-            A.decode_steps_reference(q, k, v, L0, 10000.0, "bf16")
-            t_total += time.perf_counter() - t0
-            done_bytes += float(((L0 + 1 + np.arange(self.steps)) * c["D"] * 2 * 2).sum())
-            n += 1
-            if t_total > budget_s:
-                break
-        return t_total, done_bytes, f"{n} (b, kv-head) lanes x {self.steps} decode steps (all {G} query heads each)"
-
-    def one_thread_sample(self):
-        """The oracle call of one lane of median old length, for a one-thread timing:
-        (kind, arrays, bytes, description)."""
+    def cpu_tasks(self, n, steps=None):
+        """``n`` oracle tasks (one (sequence, key/value head) lane each, lanes of old length
+        nearest the median, the first ``steps`` decode steps -- all by default) for the host
+        cores: (tasks, attention bytes of each, description)."""
         c = self.cfg
         G = c["Hq"] // c["Hkv"]
-        b = int(np.argsort(self.L0)[len(self.L0) // 2])
-        L0 = int(self.L0[b])
-        k = np.concatenate([self.k_prefix[b, 0, :L0].double().cpu().numpy(),
-                            self.k[:, b, 0, 0].double().cpu().numpy()])[None]
-        v = np.concatenate([self.v_prefix[b, 0, :L0].double().cpu().numpy(),
-                            self.v[:, b, 0, 0].double().cpu().numpy()])[None]
-        q = self.q[:, b, 0:G, 0].double().cpu().numpy()
-        work = float(((L0 + 1 + np.arange(self.steps)) * c["D"] * 2 * 2).sum())
-        return ("decode", {"q": q, "k": k, "v": v, "L0": np.int64(L0)}, work,
-                f"one (b, kv-head) lane, old length {L0}, x {self.steps} decode steps (all {G} query heads)")
+        steps = min(self.steps, steps or self.steps)
+        order = np.argsort(np.abs(self.L0 - np.median(self.L0)), kind="stable")
+        tasks, work = [], []
+        for i in range(n):
+            b = int(order[i % len(order)])
+            hk = (i // len(order)) % c["Hkv"]
+            L0 = int(self.L0[b])
+            k = np.concatenate([self.k_prefix[b, hk, :L0].double().cpu().numpy(),
+                                self.k[:steps, b, hk, 0].double().cpu().numpy()])[None]
+            v = np.concatenate([self.v_prefix[b, hk, :L0].double().cpu().numpy(),
+                                self.v[:steps, b, hk, 0].double().cpu().numpy()])[None]
+            q = self.q[:steps, b, hk * G:(hk + 1) * G, 0].double().cpu().numpy()
+            tasks.append({"kind": "decode", "q": q, "k": k, "v": v, "L0": np.int64(L0)})
+            work.append(float(((L0 + 1 + np.arange(steps)) * c["D"] * 2 * 2).sum()))
+        desc = (f"(b, kv-head) lanes of old length near the median ({int(np.median(self.L0))}) x {steps} "
+                f"decode steps (all {G} query heads each)")
+        return tasks, work, desc
 
 
 # ----------------------------------------------------------------- suffix workload
 
 class SuffixBench:
-    def __init__(self, device, batch=0, block_rows=0):
+    """The suffix-chunk workload.  ``with_cache`` False (the reference arm) draws the same
+    seeded inputs, takes the cuts from the oracle and never loads libkvc."""
+
+    def __init__(self, device, batch=0, block_rows=0, with_cache=True):
         from kv_cache_append_rope_gb300 import workloads as W
-        from kv_cache_append_rope_gb300.kvc import KVCache
         c = dict(W.CONFIGS["suffix"])
         if batch:
             c["B"] = batch
-        self.cfg, self.device = c, device
+        self.cfg, self.device, self.name, self.block_rows = c, device, "suffix", block_rows
         B, H, D = c["B"], c["Hq"], c["D"]
         self.T = c["prefix"] + c["appended"]
         self.cached, self.query, self.edit = W.edited_histories(c["seed"], B, c["prefix"], c["appended"], c["vocab"])
-        self.cache = KVCache(B, H, self.T, D, dtype="bf16", rope_base=10000.0, device=device.index or 0,
-                             block_rows=block_rows)
+        self.cache = None
         seed = c["seed"] * 1000
         self.k_prefix = W.normal((B, H, c["prefix"], D), seed + 1, device=device)
         self.v_prefix = W.normal((B, H, c["prefix"], D), seed + 2, device=device)
-        self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, out=False)
-        from kv_cache_append_rope_gb300 import kvc
-        self.cuts = [kvc.lcp(self.cached[b].tolist(), self.query[b].tolist()) for b in range(B)]
+        if with_cache:
+            from kv_cache_append_rope_gb300 import kvc
+            from kv_cache_append_rope_gb300.kvc import KVCache
+            self.cache = KVCache(B, H, self.T, D, dtype="bf16", rope_base=10000.0, device=device.index or 0,
+                                 block_rows=block_rows)
+            self.cache.prefill_suffix(0, None, self.k_prefix, self.v_prefix, out=False)
+            self.cuts = [kvc.lcp(self.cached[b].tolist(), self.query[b].tolist()) for b in range(B)]
+        else:
+            from oracle import prefix as P
+            self.cuts = [P.lcp_cut(self.cached[b].tolist(), self.query[b].tolist()) for b in range(B)]
         self.S = self.T - min(self.cuts)
         self.q = W.normal((B, H, self.S, D), seed + 3, device=device)
         self.k = W.normal((B, H, self.S, D), seed + 4, device=device)
         self.v = W.normal((B, H, self.S, D), seed + 5, device=device)
-        self.out = torch.empty((B, H, self.S, D), dtype=torch.float32, device=device)
+        self.out = torch.empty((B, H, self.S, D), dtype=torch.float32, device=device) if with_cache else None
         self.seqlen = [self.T - cu for cu in self.cuts]
         self.flops = float(sum(H * 4 * D * (s * cu + s * (s + 1) / 2) for s, cu in zip(self.seqlen, self.cuts)))
         self.host_chunk = 0
-        torch.cuda.synchronize(device)
+        if device.type == "cuda":
+            torch.cuda.synchronize(device)
 
     def step(self):
         from kv_cache_append_rope_gb300 import kvc
@@ -424,44 +442,37 @@ class SuffixBench:
                 "flops_per_step": self.flops,
                 "l2": "inputs larger than L2: the K/V prefix alone is "
                       f"{self.k_prefix.nbytes * 2 / 1e9:.1f} GB",
-                "storage": (f"paged, {self.cache.config.block_rows}-row blocks" if self.cache.config.block_rows
-                            else "contiguous")}
+                "storage": (f"paged, {self.block_rows}-row blocks" if self.block_rows else "contiguous")}
 
-    def oracle_sample(self, budget_s=15.0):
-        from oracle import attention as A
-        b, h = int(np.argmax(self.cuts)), 0
-        cut = self.cuts[b]
-        S = self.seqlen[b]
-        rows = np.arange(0, S, max(1, S // 1536))[:1536]
-        k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(), self.k[b, h, :S].double().cpu().numpy()])
-        v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(), self.v[b, h, :S].double().cpu().numpy()])
-        q = self.q[b, h:h + 1, :S].double().cpu().numpy()
-        t0 = time.perf_counter()
-        A.suffix_reference(q, k[None], v[None], np.arange(self.T), cut, 10000.0, "bf16", rows=rows)
-        dt = time.perf_counter() - t0
-        flops = float(sum(4 * self.cfg["D"] * (cut + r + 1) for r in rows))
-        return dt, flops, f"{rows.size} suffix rows of one (b, h) lane against the full masked prefix"
-
-    def one_thread_sample(self):
-        """256 suffix rows of the same lane, for a one-thread timing: (kind, arrays, flops, description)."""
-        b, h = int(np.argmax(self.cuts)), 0
-        cut = self.cuts[b]
-        S = self.seqlen[b]
-        rows = np.arange(0, S, max(1, S // 256))[:256]
-        k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(), self.k[b, h, :S].double().cpu().numpy()])
-        v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(), self.v[b, h, :S].double().cpu().numpy()])
-        q = self.q[b, h:h + 1, :S].double().cpu().numpy()
-        flops = float(sum(4 * self.cfg["D"] * (cut + r + 1) for r in rows))
-        arrays = {"q": q, "k": k[None], "v": v[None], "T": np.int64(self.T), "cut": np.int64(cut), "rows": rows}
-        return "suffix", arrays, flops, f"{rows.size} suffix rows of one (b, h) lane against the full masked prefix"
+    def cpu_tasks(self, n, rows=384):
+        """``n`` oracle tasks for the host cores, each ``rows`` suffix rows (spread over the
+        suffix) of one (sequence, head) lane against its full masked prefix:
+        (tasks, flops of each, description)."""
+        c = self.cfg
+        B, H = c["B"], c["Hq"]
+        tasks, work = [], []
+        for i in range(n):
+            b, h = i % B, (i // B) % H
+            cut, S = self.cuts[b], self.seqlen[b]
+            sel = np.linspace(0, S - 1, min(rows, S)).astype(np.int64)
+            k = np.concatenate([self.k_prefix[b, h, :cut].double().cpu().numpy(),
+                                self.k[b, h, :S].double().cpu().numpy()])
+            v = np.concatenate([self.v_prefix[b, h, :cut].double().cpu().numpy(),
+                                self.v[b, h, :S].double().cpu().numpy()])
+            q = self.q[b, h:h + 1, :S].double().cpu().numpy()
+            tasks.append({"kind": "suffix", "q": q, "k": k[None], "v": v[None], "T": np.int64(self.T),
+                          "cut": np.int64(cut), "rows": sel})
+            work.append(float(sum(4 * c["D"] * (cut + int(r) + 1) for r in sel)))
+        desc = f"{rows} suffix rows per (b, h) lane, spread over the suffix, against the full masked prefix"
+        return tasks, work, desc
 
 
 # ----------------------------------------------------------------- driver
 
-def make_bench(name, device, batch=0, graph=False, block_rows=0):
+def make_bench(name, device, batch=0, graph=False, block_rows=0, with_cache=True):
     if name == "suffix":
-        return SuffixBench(device, batch, block_rows)
-    return DecodeBench(name, device, batch, graph, block_rows)
+        return SuffixBench(device, batch, block_rows, with_cache)
+    return DecodeBench(name, device, batch, graph, block_rows, with_cache)
 
 
 def dist_setup(args):
@@ -492,42 +503,38 @@ def barrier(world):
         dist.barrier()
 
 
-def cpu_threads():
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
-        if os.environ.get(var, "").isdigit():
-            return int(os.environ[var])
-    return os.cpu_count()
+# Oracle task sizes: the CPU baseline (one task per host core, each a few seconds of
+# float64 work) and the reference arm (smaller tasks, one batch per bench step).
+CPU_TASK = {"mha_decode": dict(steps=64), "mha_decode_short": dict(steps=64), "gqa_decode": dict(steps=32),
+            "mqa_decode": dict(steps=8), "suffix": dict(rows=384)}
+REF_TASK = {"mha_decode": dict(steps=16), "mha_decode_short": dict(steps=64), "gqa_decode": dict(steps=8),
+            "mqa_decode": dict(steps=2), "suffix": dict(rows=96)}
 
 
-# One oracle call per kind, as run in a fresh interpreter (arrays come from an .npz file).
-_ONE_CORE_CALLS = {
-    "decode": "A.decode_steps_reference(z['q'], z['k'], z['v'], int(z['L0']), 10000.0, 'bf16')",
-    "suffix": "A.suffix_reference(z['q'], z['k'], z['v'], np.arange(int(z['T'])), int(z['cut']), 10000.0, "
-              "'bf16', rows=z['rows'])",
-}
+def start_workers(n=None):
+    """One one-thread oracle process per host core (exec'd interpreters, started before
+    this process touches the GPU)."""
+    from oracle.timing import Workers
+    return Workers(n or os.cpu_count() or 1)
 
 
-def oracle_seconds_one_thread(kind, arrays, timeout_s=120):
-    """Seconds the oracle takes for one call of `kind` on `arrays` in a fresh interpreter
-    limited to one BLAS/OpenMP thread (so the oracle runs on one core)."""
-    import subprocess
-    import sys
-    import tempfile
-    root = os.path.dirname(os.path.abspath(__file__))
-    with tempfile.TemporaryDirectory() as d:
-        path = os.path.join(d, "sample.npz")
-        np.savez(path, **arrays)
-        code = ("import sys, time\nimport numpy as np\n"
-                f"sys.path.insert(0, {root!r})\nfrom oracle import attention as A\n"
-                f"z = np.load({path!r})\nt0 = time.perf_counter()\n{_ONE_CORE_CALLS[kind]}\n"
-                "print(time.perf_counter() - t0)\n")
-        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                           timeout=timeout_s, check=True)
-        return float(r.stdout.strip().splitlines()[-1])
+def cpu_baseline(bench, workers, unit):
+    """The oracle on the host cores: one task per core side by side (value = their work /
+    the slowest one's time), and one task alone (`one_core`)."""
+    scale = 1e9 if unit == "GB/s" else 1e12
+    tasks, work, desc = bench.cpu_tasks(workers.n, **CPU_TASK[bench.name])
+    secs = workers.run(tasks)
+    wall = max(secs)
+    line = {"value": round(sum(work) / scale / wall, 6), "unit": unit, "cores": workers.n, "kind": "oracle",
+            "sample": f"{workers.n} {desc}, one oracle process per core side by side",
+            "seconds": round(wall, 2), "cpu_seconds": round(sum(secs), 2)}
+    one = workers.run(tasks[:1])[0]
+    line["one_core"] = {"value": round(work[0] / scale / one, 6), "unit": unit, "cores": 1,
+                        "sample": f"1 {desc}, alone", "seconds": round(one, 2)}
+    return line
 
 
-def run_ours(args, name, world, rank, local):
+def run_ours(args, name, world, rank, local, workers=None):
     from kv_cache_append_rope_gb300 import _lib as L
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
@@ -574,8 +581,10 @@ def run_ours(args, name, world, rank, local):
     value = units * world / (ms / 1e3)
     per_step_ms = ms / args.steps
 
-    # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / event-timed duration
+    # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / event-timed
+    # duration; and the same work per bench step / the whole step's time (no per-launch events)
     alg = bench.dominant_algorithmic(dom_launches)
+    alg_step = alg / args.steps
     traffic = None
     kind = TRAFFIC.get(bench.config()["workload"])
     if kind and kind[0] == "ratio":
@@ -584,16 +593,27 @@ def run_ours(args, name, world, rank, local):
         traffic = round(kind[1] * bench.cfg["B"])
     if unit == "GB/s":
         achieved = alg / 1e9 / (dom_ms / 1e3)
+        achieved_step = alg_step / 1e9 / (per_step_ms / 1e3)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": "decode_bf16_kernel",
-                "peak_source": f"{peak_kind} hbm_gbs", "kernel_ms_per_launch": round(dom_ms / dom_launches, 5),
-                "algorithmic_bytes_per_launch": round(alg / dom_launches)}
+                "peak_source": f"{peak_kind} hbm_gbs (a device copy's read + write rate, not a datasheet peak)",
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
+                "kernel_ms_per_launch": round(dom_ms / dom_launches, 5),
+                "algorithmic_bytes_per_launch": round(alg / dom_launches),
+                "step_achieved": round(achieved_step, 1), "step_frac": round(achieved_step / hbm, 4)}
     else:
         achieved = alg / 1e12 / (dom_ms / 1e3)
+        achieved_step = alg_step / 1e12 / (per_step_ms / 1e3)
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tflops, "unit": "TFLOP/s",
                 "frac": round(achieved / tflops, 4), "traffic": traffic, "kernel": dom,
-                "peak_source": f"{peak_kind} bf16_tflops (burst)", "kernel_ms_per_launch": round(dom_ms / dom_launches, 3),
-                "algorithmic_flops_per_launch": round(alg / dom_launches)}
+                "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4), "nominal_peak": NOMINAL_BF16_TFLOPS,
+                "kernel_ms_per_launch": round(dom_ms / dom_launches, 3),
+                "algorithmic_flops_per_launch": round(alg / dom_launches),
+                "step_achieved": round(achieved_step, 1), "step_frac": round(achieved_step / tflops, 4)}
+    roof["launch_modes"] = ("achieved/frac: per-launch CUDA events (a second pass; the events serialise "
+                            "dependent launches); step_achieved/step_frac: the same algorithmic work per "
+                            "bench step / ms_per_step of the event-free pass")
 
     e2e = None
     if not args.no_e2e:
@@ -612,18 +632,8 @@ def run_ours(args, name, world, rank, local):
                "d2h_bytes_per_step": int(bench.d2h)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, work, sample = bench.oracle_sample()
-        cpu = {"value": round(work / (1e9 if unit == "GB/s" else 1e12) / secs, 6), "unit": unit,
-               "cores": cpu_threads(), "kind": "oracle", "sample": sample, "seconds": round(secs, 2)}
-        # the same oracle on one core (a fresh interpreter with one BLAS/OpenMP thread)
-        try:
-            kind, arrays, work1, sample1 = bench.one_thread_sample()
-            secs1 = oracle_seconds_one_thread(kind, arrays)
-            cpu["one_core"] = {"value": round(work1 / (1e9 if unit == "GB/s" else 1e12) / secs1, 6),
-                               "unit": unit, "cores": 1, "sample": sample1, "seconds": round(secs1, 2)}
-        except Exception as e:   # reported, never fatal: the line stands without it
-            cpu["one_core"] = {"unavailable": f"{type(e).__name__}: {str(e)[:120]}"}
+    if rank == 0 and world == 1 and workers is not None:
+        cpu = cpu_baseline(bench, workers, unit)
 
     cache.check()
     line = {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -637,52 +647,94 @@ def run_ours(args, name, world, rank, local):
     else:
         line["tensor_peak_frac"] = round(value / world / tflops, 4)
         line["steps_per_s"] = round(args.steps / (ms / 1e3), 3)
+    release(bench)
     return line
 
 
-def run_reference(args, name):
-    """The oracle as the reference arm: each step a bounded sample of the same workload."""
+def release(bench):
+    """Frees a workload's device memory before the next one is built."""
+    import gc
+    if getattr(bench, "cache", None) is not None:
+        bench.cache.destroy()
+    bench.__dict__.clear()
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def run_reference(args, name, workers):
+    """The oracle as the reference arm: each bench step one batch of oracle tasks, one per
+    host core side by side, on the same seeded inputs (built with torch; libkvc is not
+    loaded)."""
     device = torch.device("cuda", 0) if torch.cuda.is_available() else None
     if device is None:
         return {"impl": "reference", "unavailable": "the workload inputs are generated on a CUDA device"}
-    bench = make_bench(name, device)
-    budget = 20.0 / max(1, args.steps + args.warmup)
-    for _ in range(args.warmup):
-        bench.oracle_sample(budget)
-    secs, work, sample = 0.0, 0.0, ""
-    for _ in range(args.steps):
-        s, w, sample = bench.oracle_sample(budget)
-        secs += s
-        work += w
-    units, unit = bench.units(1)
+    bench = make_bench(name, device, with_cache=False)
+    _, unit = bench.units(1)
     scale = 1e9 if unit == "GB/s" else 1e12
-    value = work / scale / secs
-    cpu = {"value": round(value, 6), "unit": unit, "cores": cpu_threads(), "kind": "oracle", "sample": sample}
+    tasks, work, desc = bench.cpu_tasks(workers.n, **REF_TASK[name])
+    config = bench.config()
+    release(bench)
+    for _ in range(args.warmup):
+        workers.run(tasks)
+    secs = 0.0
+    for _ in range(args.steps):
+        secs += max(workers.run(tasks))
+    value = sum(work) * args.steps / scale / secs
+    sample = f"{workers.n} {desc}, one oracle process per core side by side, per step"
+    cpu = {"value": round(value, 6), "unit": unit, "cores": workers.n, "kind": "oracle", "sample": sample}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": bench.config(), "cpu_baseline": cpu,
+            "config": config, "cpu_baseline": cpu,
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+SUB_KEYS = ("value", "unit", "ms_per_step", "roofline", "cpu_baseline", "e2e", "clocks", "config", "gpu_launches",
+            "hbm_peak_frac", "decode_steps_per_s", "tensor_peak_frac", "steps_per_s")
 
 
 def main():
     args = parse()
-    if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:
+    rank_env = int(os.environ.get("RANK", "0"))
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference" and rank_env != 0:
         return                                   # the oracle arm runs on rank 0 only
-    world, rank, local = dist_setup(args) if args.impl == "ours" else (1, 0, 0)
-    names = (["mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix"] if args.workload == "all"
-             else [args.workload])
-    for name in names:
-        if args.impl == "reference":
+    # the oracle processes start before this process touches the GPU
+    workers = None
+    if rank_env == 0 and (args.impl == "reference" or (world_env == 1 and not args.no_cpu_baseline)):
+        workers = start_workers()
+    try:
+        world, rank, local = dist_setup(args) if args.impl == "ours" else (1, 0, 0)
+        if args.workload == "default":
+            groups = [("mha_decode", SUB_WORKLOADS)]
+        elif args.workload == "all":
+            groups = [(n, ()) for n in ("mha_decode", "mha_decode_short", "gqa_decode", "mqa_decode", "suffix")]
+        else:
+            groups = [(args.workload, ())]
+        for head, subs in groups:
+            if args.impl == "reference":
+                line = run_reference(args, head, workers)
+                if subs:
+                    line["workloads"] = {}
+                    for n in subs:
+                        sub = run_reference(args, n, workers)
+                        line["workloads"][n] = {k: sub[k] for k in SUB_KEYS if k in sub}
+                print(json.dumps(line), flush=True)
+                continue
+            line = run_ours(args, head, world, rank, local, workers)
+            if subs:
+                line["workloads"] = {}
+                for n in subs:
+                    sub = run_ours(args, n, world, rank, local, workers)
+                    line["workloads"][n] = {k: sub[k] for k in SUB_KEYS if k in sub}
             if rank == 0:
-                print(json.dumps(run_reference(args, name)), flush=True)
-            continue
-        line = run_ours(args, name, world, rank, local)
-        if rank == 0:
-            print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+                print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    finally:
+        if workers is not None:
+            workers.close()
 
 
 if __name__ == "__main__":

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 4
+#define KVC_ABI_VERSION 5
 
 typedef enum kvc_status {
     KVC_OK = 0,
@@ -313,6 +313,33 @@ kvc_status kvc_lcp_window(const int32_t* cached, int64_t n, const int32_t* query
 kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
                            int32_t* next_positions);
 
+/* The host mirror of one layer's logical lengths, [B] host ([Ch37] listing "Own a
+ * fixed layer-bound cache, append one checked row, and reset logical length":
+ * len()).  The same as kvc_get_lengths without the next positions; after
+ * device-length decode steps call kvc_sync_lengths first.  KVC_ERR_NULL for a
+ * NULL handle or array, KVC_ERR_LAYER for a layer out of range. */
+kvc_status kvc_get_len(const kvc_handle* h, int32_t layer, int32_t* len_B);
+
+/*
+ * Logical snapshot of one layer ([Ch37] listing "Own a fixed layer-bound cache,
+ * append one checked row, and reset logical length": keys() and values() copy
+ * out the retained rows [B, H, len, d_h], never the unused capacity).
+ *   keys, values  [B, H_kv, R, d_h] DEVICE tensors of the storage dtype,
+ *                 1 <= R <= C, caller-owned; either may be NULL (not both)
+ *   positions     [B, R] int32 DEVICE pointer, or NULL
+ * Row r of sequence b receives stored row r (the rotated key, the value, the
+ * recorded position) when r < length[b], gathered through the block table for
+ * paged storage; rows r >= length[b] receive zeros and position -1.  The
+ * lengths are the device lengths at the point of `stream` where the copy runs,
+ * so the snapshot follows every earlier call on that stream (device-length
+ * steps included).  Enqueued on `stream`; the storage is only read.  Errors (no
+ * work enqueued): KVC_ERR_NULL, KVC_ERR_LAYER, KVC_ERR_DTYPE, KVC_ERR_KEY_SHAPE /
+ * KVC_ERR_VALUE_SHAPE (shape, or R outside [1, C]), KVC_ERR_CONFIG (a pointer
+ * that is not device memory of the handle's GPU, or misaligned).
+ */
+kvc_status kvc_read_rows(kvc_handle* h, int32_t layer, const kvc_tensor* keys, const kvc_tensor* values,
+                         int32_t* positions, void* stream);
+
 /* Waits for all work on the handle's device, then copies every layer's device
  * lengths and next positions into the host mirrors.  No other effect. */
 kvc_status kvc_sync_lengths(kvc_handle* h);
@@ -349,7 +376,9 @@ kvc_status kvc_storage(const kvc_handle* h, int32_t layer, void** keys, void** v
 
 /*
  * Synchronises `stream`, then checks the device side: the kernels' error word
- * (a bounded wait that gave up, an out-of-range slot) and that the device
+ * (bits: 1 an append slot or position out of range, 2 a bounded wait that gave
+ * up, 4 tensor memory, 8 a rejected device-length step, 16 a device-checked cut
+ * beyond a length, 32 a debug-build bounds check that skipped an access) and that the device
  * lengths and next positions equal the host mirrors.  KVC_ERR_DEVICE on any
  * difference (message names it), KVC_ERR_CUDA if the synchronisation fails.
  * A reported error word is cleared (while it is set, kernels stop early).
@@ -384,6 +413,18 @@ kvc_status kvc_decode_attend_noalloc(const void* keys, const void* values, const
                                      const int32_t* lengths, float* out, int32_t batch, int32_t heads_q,
                                      int32_t heads_kv, int32_t capacity, void* stream);
 
+/*
+ * Device-side status of kvc_decode_attend_noalloc on the current device (no
+ * page counterpart, like that call).  Synchronises `stream`, reads the error
+ * word in the static array and clears it: KVC_ERR_DEVICE when some call since
+ * the last check had a bounded wait give up (its `out` is then undefined),
+ * KVC_OK otherwise (also before any call on this device), KVC_ERR_CUDA if the
+ * synchronisation or the read fails.  Allocates nothing.  A wait that gives up
+ * cannot be seen from the call that launched it (the call returns before the
+ * kernel runs), so callers check after the steps whose outputs they consume.
+ */
+kvc_status kvc_noalloc_check(void* stream);
+
 /* Tuning / test options (kvc_set_option). */
 typedef enum kvc_option {
     KVC_OPT_DECODE_SPLIT_ROWS = 1, /* key rows per decode split (multiple of 64); 0 = automatic */
@@ -397,7 +438,9 @@ typedef enum kvc_option {
     KVC_OPT_TEST_STALL = 6,        /* test only, applies to the next bf16 d_h = 128 decode step: its producer
                                       issues no loads, so the consumers' bounded waits give up (about 1 s)
                                       and the step reports a device error through kvc_check; the step's
-                                      outputs are undefined and the cache should then be reset */
+                                      outputs are undefined and the cache should then be reset.  With a
+                                      NULL handle it applies to the next kvc_decode_attend_noalloc call
+                                      instead (reported by kvc_noalloc_check) */
     KVC_OPT_DEVICE_LENGTHS = 7,    /* 1 = decode steps read the lengths and next positions from device memory
                                       instead of the host mirrors, so that the launches of a step do not
                                       depend on them and can be captured in a CUDA graph and replayed:
@@ -415,12 +458,26 @@ typedef enum kvc_option {
                                       device and read the lengths back.  Paged storage cannot use it
                                       (blocks are taken on the host as rows are appended):
                                       KVC_ERR_CONFIG. */
-    KVC_OPT_DECODE_PDL = 8         /* 1 (default) = bf16 d_h = 128 decode and merge kernels are launched as
+    KVC_OPT_DECODE_PDL = 8,        /* 1 (default) = bf16 d_h = 128 decode and merge kernels are launched as
                                       programmatic dependents of the previous kernel in the stream (each
                                       CTA waits for it before touching global memory), so that a step's
                                       CTAs take the slots the previous step frees as it drains; 0 = plain
                                       launches.  Never used while the stream captures a graph or with
                                       KVC_OPT_DEVICE_LENGTHS. */
+    KVC_OPT_TEST_POISON = 9,       /* test only: value 1 synchronises the device and fills every stored row
+                                      that no sequence holds -- slots at or past a sequence's length
+                                      (paged: past the held rows of a block, and every free block) -- in
+                                      every layer with a large finite poison: keys 0, values 1e4 (9984 in
+                                      bf16), so that a kernel reading a row it must not moves its output
+                                      by about 1e4 / t.  Lengths and held rows are unchanged; a prepared,
+                                      uncommitted step's staged row is overwritten.  0 does nothing. */
+    KVC_OPT_TEST_PLANT_LENGTH = 10 /* test only, debug builds (libkvc_debug.so, compiled with KVC_DEBUG)
+                                      only, else KVC_ERR_CONFIG: synchronises the device and writes `value`
+                                      into the DEVICE length and next position of layer 0, sequence 0,
+                                      leaving the host mirror alone -- a state the host checks never
+                                      produce -- so that the debug build's device bounds checks can be
+                                      seen to record KVC_ERR_DEVICE bit 32 and skip the access.  Reset
+                                      the cache afterwards. */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

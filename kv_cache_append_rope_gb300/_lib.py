@@ -9,7 +9,10 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libkvc.so")
+# KVC_LIB=debug loads the build whose kernels check every length and slot index
+# against the capacity (bit 32 of the device error word; see include/kvc.h)
+VARIANT = "debug" if os.environ.get("KVC_LIB", "") == "debug" else "release"
+LIB_PATH = os.path.join(PKG, "libkvc_debug.so" if VARIANT == "debug" else "libkvc.so")
 
 STATUS = {
     0: "KVC_OK", 1: "KVC_ERR_NULL", 2: "KVC_ERR_ZERO_BATCH", 3: "KVC_ERR_ZERO_CAPACITY",
@@ -26,14 +29,17 @@ OPT_DECODE_SPLIT_ROWS, OPT_FORCE_GENERIC, OPT_SUFFIX_KERNEL, OPT_TIMING, OPT_DEC
 OPT_TEST_STALL = 6
 OPT_DEVICE_LENGTHS = 7
 OPT_DECODE_PDL = 8
+OPT_TEST_POISON = 9
+OPT_TEST_PLANT_LENGTH = 10
 KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "generic_attend": 4,
            "bookkeeping": 5}
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_abi_version", "kvc_status_string", "kvc_last_error", "kvc_create", "kvc_create_ex",
            "kvc_destroy", "kvc_append_attend", "kvc_prepare_attend", "kvc_commit", "kvc_prefill_suffix", "kvc_prefill_suffix_host", "kvc_reset", "kvc_truncate",
-           "kvc_lcp", "kvc_lcp_window", "kvc_share_prefix", "kvc_block_table", "kvc_get_lengths", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
-           "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc")
+           "kvc_lcp", "kvc_lcp_window", "kvc_share_prefix", "kvc_block_table", "kvc_get_lengths", "kvc_get_len",
+           "kvc_read_rows", "kvc_sync_lengths", "kvc_get_config", "kvc_storage", "kvc_check", "kvc_set_option",
+           "kvc_kernel_stats", "kvc_reset_stats", "kvc_decode_attend_noalloc", "kvc_noalloc_check")
 
 
 class KVCError(RuntimeError):
@@ -92,6 +98,8 @@ def _load():
         "kvc_share_prefix": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P]),
         "kvc_block_table": (ctypes.c_int, [_P, _I32P, _I32P]),
         "kvc_get_lengths": (ctypes.c_int, [_P, ctypes.c_int32, _I32P, _I32P]),
+        "kvc_get_len": (ctypes.c_int, [_P, ctypes.c_int32, _I32P]),
+        "kvc_read_rows": (ctypes.c_int, [_P, ctypes.c_int32, _TP, _TP, _P, _P]),
         "kvc_sync_lengths": (ctypes.c_int, [_P]),
         "kvc_get_config": (ctypes.c_int, [_P, ctypes.POINTER(kvc_config)]),
         "kvc_storage": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_P), ctypes.POINTER(_P),
@@ -103,6 +111,7 @@ def _load():
         "kvc_reset_stats": (ctypes.c_int, [_P]),
         "kvc_decode_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _I32P, _P, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_int32, ctypes.c_int32, _P]),
+        "kvc_noalloc_check": (ctypes.c_int, [_P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

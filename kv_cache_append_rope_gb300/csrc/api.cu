@@ -866,13 +866,14 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         GenericAttendLaunch g{};
         g.qrot = h->qrot; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = nullptr; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D; g.window = W; g.kv = h->layout();
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = 1; g.C = C; g.d = D; g.window = W; g.kv = h->layout(); g.err = h->err_d;
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     h->layer_version[layer] += 1;
     if (!commit) return KVC_OK;
     KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
-        return launch_commit(h->len_layer(layer), h->next_layer(layer), h->next_layer(layer), nullptr, 1, B, s);
+        return launch_commit(h->len_layer(layer), h->next_layer(layer), h->next_layer(layer), nullptr, 1, B, C,
+                             h->err_d, s);
     }));
     for (int b = 0; b < B; ++b) {
         lenh[b] += 1;
@@ -1067,11 +1068,11 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
         GenericAttendLaunch g{};
         g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
         g.slot0 = h->len_layer(layer); g.seqlen = seqlen_d; g.out = out->data;
-        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D; g.window = h->cfg.window; g.kv = h->layout();
+        g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.S = S; g.C = C; g.d = D; g.window = h->cfg.window; g.kv = h->layout(); g.err = h->err_d;
         KVC_CUDA(h, timed(h, KVC_KERNEL_GENERIC_ATTEND, s, [&] { return launch_attend_generic(dt, g, s); }));
     }
     KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
-        return launch_commit(h->len_layer(layer), h->next_layer(layer), start_d, seqlen_d, S, B, s);
+        return launch_commit(h->len_layer(layer), h->next_layer(layer), start_d, seqlen_d, S, B, C, h->err_d, s);
     }));
     KVC_CUDA(h, h->ring.release(s));
     for (int b = 0; b < B; ++b) {
@@ -1128,7 +1129,7 @@ kvc_status kvc_commit(kvc_handle* h, const kvc_ticket* tickets, int32_t n, void*
         CommitLayers cl{};
         cl.n = std::min(n - i0, kCommitMaxLayers);
         for (int i = 0; i < cl.n; ++i) cl.layer[i] = tickets[i0 + i].layer;
-        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_commit_layers(h->len_d, h->next_d, cl, B, s); }));
+        KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] { return launch_commit_layers(h->len_d, h->next_d, cl, B, h->C(), h->err_d, s); }));
     }
     for (int i = 0; i < n; ++i) {
         const int l = tickets[i].layer;
@@ -1470,6 +1471,47 @@ kvc_status kvc_get_lengths(const kvc_handle* h, int32_t layer, int32_t* lengths,
     return KVC_OK;
 }
 
+kvc_status kvc_get_len(const kvc_handle* h, int32_t layer, int32_t* len_B) {
+    if (!len_B) return KVC_ERR_NULL;
+    return kvc_get_lengths(h, layer, len_B, nullptr);
+}
+
+kvc_status kvc_read_rows(kvc_handle* h, int32_t layer, const kvc_tensor* keys, const kvc_tensor* values,
+                         int32_t* positions, void* stream) {
+    if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
+    kvc_status st;
+    if ((st = check_layer(h, layer)) != KVC_OK) return st;
+    if (!keys && !values) return fail(h, KVC_ERR_NULL, "keys and values are both NULL");
+    const int B = h->B(), Hkv = h->Hkv(), D = h->D(), dt = h->cfg.dtype;
+    const kvc_tensor* first = keys ? keys : values;
+    if (first->ndim != 4 || first->shape[2] < 1 || first->shape[2] > h->C())
+        return fail(h, KVC_ERR_KEY_SHAPE, "the snapshot must have shape [%d, %d, R, %d] with 1 <= R <= %d", B, Hkv, D,
+                    h->C());
+    const int R = (int)first->shape[2];
+    if (keys && (st = check_tensor(h, keys, "keys", KVC_ERR_KEY_SHAPE, dt, B, Hkv, R, D)) != KVC_OK) return st;
+    if (values && (st = check_tensor(h, values, "values", KVC_ERR_VALUE_SHAPE, dt, B, Hkv, R, D)) != KVC_OK)
+        return st;
+    if (positions) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, positions) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, KVC_ERR_CONFIG, "positions pointer is not a CUDA allocation");
+        }
+        if ((attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) ||
+            attr.device != h->cfg.device)
+            return fail(h, KVC_ERR_CONFIG, "positions must be device memory of GPU %d", h->cfg.device);
+        if ((uintptr_t)positions & 3u) return fail(h, KVC_ERR_CONFIG, "positions pointer is not 4-byte aligned");
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    KVC_CUDA(h, timed(h, KVC_KERNEL_BOOKKEEPING, s, [&] {
+        return launch_read_rows(h->K_layer(layer), h->V_layer(layer), h->pos_layer(layer), h->len_layer(layer),
+                                h->layout(), keys ? keys->data : nullptr, values ? values->data : nullptr,
+                                positions, B, Hkv, R, (int)(D * h->elem_size), s);
+    }));
+    return KVC_OK;
+}
+
 kvc_status kvc_share_prefix(kvc_handle* h, int32_t dst, int32_t src, int32_t rows, void* stream) {
     if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
     if (!h->paged()) return fail(h, KVC_ERR_CONFIG, "sharing a prefix needs paged storage (block_rows > 0)");
@@ -1554,7 +1596,8 @@ kvc_status kvc_check(kvc_handle* h, void* stream) {
         return fail(h, KVC_ERR_DEVICE,
                     "device error word 0x%x (1: slot out of range, 2: bounded wait timed out, 4: tensor memory, "
                     "8: cache full or position beyond the table in a device-length step, "
-                    "16: cut beyond a length in a device-checked truncate)",
+                    "16: cut beyond a length in a device-checked truncate, "
+                    "32: debug-build bounds check skipped an access)",
                     err);
     if (h->mirrors_stale || h->opt_device_lengths) {
         h->len_h = len;
@@ -1568,9 +1611,72 @@ kvc_status kvc_check(kvc_handle* h, void* stream) {
     return KVC_OK;
 }
 
+// KVC_OPT_TEST_POISON: every storage row that no sequence holds -- slot >= length in
+// contiguous storage; past the held rows of a block, or the whole of a free block, in
+// paged storage -- gets keys 0 and values 1e4 (in the storage dtype), in every layer.
+static kvc_status poison_unheld_rows(kvc_handle* h) {
+    kvc_status st = refresh_mirrors(h);
+    if (st != KVC_OK) return st;
+    const int L = h->cfg.layers, B = h->B(), Hkv = h->Hkv();
+    const int groups = h->paged() ? h->nblocks : B;
+    const int R = h->paged() ? h->cfg.block_rows : h->C();
+    std::vector<int32_t> live((size_t)L * groups, 0);
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b) {
+            const int n = h->len_h[(size_t)l * B + b];
+            if (!h->paged()) {
+                live[(size_t)l * groups + b] = n;
+                continue;
+            }
+            for (int j = 0; j < h->nblk; ++j) {
+                const int blk = h->table_h[(size_t)b * h->nblk + j];
+                if (blk < 0) continue;
+                const int held = std::max(0, std::min(R, n - j * R));
+                int32_t& x = live[(size_t)l * groups + blk];
+                x = std::max(x, held);
+            }
+        }
+    unsigned long long vbits = 0;
+    if (h->cfg.dtype == KVC_F64) { const double v = 1e4; memcpy(&vbits, &v, 8); }
+    else if (h->cfg.dtype == KVC_F32) { const float v = 1e4f; uint32_t u; memcpy(&u, &v, 4); vbits = u; }
+    else vbits = 0x461c;   // 1e4 rounded to bf16 (9984)
+    int32_t* live_d = nullptr;
+    KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+    KVC_CUDA(h, cudaDeviceSynchronize());
+    KVC_CUDA(h, cudaMalloc((void**)&live_d, live.size() * sizeof(int32_t)));
+    cudaError_t e = cudaMemcpy(live_d, live.data(), live.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = launch_poison(h->K, h->V, h->layer_elems * h->elem_size, live_d, L, groups, Hkv, R, h->D(),
+                          (int)h->elem_size, vbits, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    cudaFree(live_d);
+    if (e != cudaSuccess) return cuda_fail(h, e, "poisoning unheld rows");
+    return KVC_OK;
+}
+
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
+    if (!h && option == KVC_OPT_TEST_STALL) {
+        // no handle: the next kvc_decode_attend_noalloc call stalls (test only)
+        if (value) noalloc_arm_test_stall();
+        return KVC_OK;
+    }
     if (!h) return fail(nullptr, KVC_ERR_NULL, "handle is NULL");
     switch (option) {
+        case KVC_OPT_TEST_POISON:
+            return value ? poison_unheld_rows(h) : KVC_OK;
+        case KVC_OPT_TEST_PLANT_LENGTH: {
+#ifdef KVC_DEBUG
+            if (value < INT32_MIN || value > INT32_MAX) return fail(h, KVC_ERR_CONFIG, "planted length out of range");
+            const int32_t v = (int32_t)value;
+            KVC_CUDA(h, cudaSetDevice(h->cfg.device));
+            KVC_CUDA(h, cudaDeviceSynchronize());
+            KVC_CUDA(h, cudaMemcpy(h->len_d, &v, sizeof(v), cudaMemcpyHostToDevice));
+            KVC_CUDA(h, cudaMemcpy(h->next_d, &v, sizeof(v), cudaMemcpyHostToDevice));
+            return KVC_OK;
+#else
+            return fail(h, KVC_ERR_CONFIG, "planting a device length needs the debug build (libkvc_debug.so)");
+#endif
+        }
         case KVC_OPT_DECODE_SPLIT_ROWS:
             if (value < 0 || value % 64 || value > (int64_t)1 << 30)
                 return fail(h, KVC_ERR_CONFIG, "decode split rows must be 0 or a positive multiple of 64, got %lld",

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(GenericAttendLaunch
     const int rows = a.seqlen ? a.seqlen[b] : a.S;
     if (i >= rows) return;
     const int t = a.slot0[b] + i + 1;
+    if (!debug_check(t >= 1 && t <= a.C, lane == 0 ? a.err : nullptr)) return;
     const int g = h / (a.Hq / a.Hkv);
     const A* q = (const A*)a.qrot + row * a.d;
     const A scale = (A)1 / sqrt((A)a.d);

@@ -143,6 +143,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     } else {
         old_len = FUSED ? a.old_len[b] : a.len[b];
         pos = FUSED ? a.pos[b] : 0;
+        // debug builds: the new row's slot (and so every key row read) lies inside the lane
+        if (!debug_check(old_len >= 0 && old_len < a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
         if (FUSED && split == 0 && hkv == 0 && threadIdx.x == 0 && !a.no_commit) {
             a.len_out[b] = old_len + 1;
             a.next_out[b] = pos + 1;
@@ -183,7 +185,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             // key (bit-exact bf16 rounding), store the value and the position, then
             // order these generic-proxy writes before this warp's TMA reads of them.
             const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
-            const int64_t dst = kv_row(a.kv, b, hkv, old_len) * D + lane * 4;
+            const bool slot_ok = debug_check(kv_slot_ok(a.kv, b, old_len), lane == 0 ? a.err : nullptr);
+            const int64_t dst = slot_ok ? kv_row(a.kv, b, hkv, old_len) * D + lane * 4 : 0;
             const uint2 kraw = *(const uint2*)(a.k_in + src);
             const uint2 vraw = *(const uint2*)(a.v_in + src);
             const __nv_bfloat16* kin = (const __nv_bfloat16*)&kraw;
@@ -201,9 +204,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     kout[2 * e + 1] = kin[2 * e + 1];
                 }
             }
-            *(uint2*)(a.K + dst) = *(const uint2*)kout;
-            *(uint2*)(a.V + dst) = vraw;
-            if (hkv == 0 && lane == 0) a.positions[(int64_t)b * a.C + old_len] = pos;
+            if (slot_ok) {
+                *(uint2*)(a.K + dst) = *(const uint2*)kout;
+                *(uint2*)(a.V + dst) = vraw;
+                if (hkv == 0 && lane == 0) a.positions[(int64_t)b * a.C + old_len] = pos;
+            }
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
         }
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     } else {
         t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
     }
+    if (!debug_check(t >= 1 && t <= a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
     const int ns = (key_span(t, a.window) + rows - 1) / rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
@@ -512,13 +518,11 @@ struct PdlConfig {
 template <int MT, int MODE>
 cudaError_t launch_mt(const DecodeLaunch& a, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<Cfg<MT>::STAGES>();
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_bf16_kernel<MT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run([] {
+        return cudaFuncSetAttribute(decode_bf16_kernel<MT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    });
+    if (e != cudaSuccess) return e;
     dim3 grid(a.max_splits, a.B * a.Hkv);
     PdlConfig pc(grid, dim3(THREADS), SMEM, s, a.pdl != 0 && MODE != 2);
     return cudaLaunchKernelEx(&pc.cfg, decode_bf16_kernel<MT, MODE>, *a.tmK, *a.tmV, a);

@@ -18,11 +18,15 @@
 // the array and it keeps the last call's contents: calls that overlap on the
 // GPU (different streams, or different host threads without ordering) race
 // on it.  Within one call every partial is written before it is read, and the
-// lengths and the error word are rewritten by the call itself.
+// lengths are rewritten by the call itself.  The error word is not: a bounded
+// wait that gave up in any call sets a bit there, and the bit stays until
+// kvc_noalloc_check reads it back and clears it, so a failed step is reported
+// even when later calls ran in between.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -42,17 +46,34 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes]
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<int> g_test_stall{0};   // test only: the next call's producer issues no loads
+
+// The array's device address on the current device (resolved on the first use
+// there), or null if the lookup fails.  *fresh is set when this call resolved it.
+void* scratch_on(int dev, bool* fresh = nullptr) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (fresh) *fresh = false;
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = p;
+        if (fresh) *fresh = true;
+    }
+    return g_scratch_ptr[dev];
+}
 
 struct LengthsParam {
     int32_t len_minus_one[256];
 };
 
 // Writes the old lengths (t - 1, the decode kernel's convention) of up to 256
-// sequences into the scratch and clears the error word.
-__global__ void noalloc_prologue(int32_t* lens_dst, uint32_t* err, LengthsParam p, int offset, int n) {
+// sequences into the scratch.
+__global__ void noalloc_prologue(int32_t* lens_dst, LengthsParam p, int offset, int n) {
     const int i = threadIdx.x;
     if (i < n) lens_dst[offset + i] = p.len_minus_one[i];
-    if (offset == 0 && i == 0) *err = 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -81,6 +102,9 @@ bool encode(CUtensorMap* map, const void* base, uint64_t rows) {
 }
 
 }  // namespace
+
+void noalloc_arm_test_stall() { g_test_stall.store(1); }
+
 }  // namespace kvc
 
 using namespace kvc;
@@ -106,20 +130,13 @@ extern "C" kvc_status kvc_decode_attend_noalloc(const void* keys, const void* va
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
 
-    void* base;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_ptr[dev]) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
-                cudaGetLastError();
-                return KVC_ERR_CUDA;
-            }
-            g_scratch_ptr[dev] = p;
-        }
-        base = g_scratch_ptr[dev];
-    }
+    bool fresh = false;
+    void* base = scratch_on(dev, &fresh);
+    if (!base) return KVC_ERR_CUDA;
     uint32_t* err = (uint32_t*)base;
+    // the error word starts at zero on every device (it is cleared again only by
+    // kvc_noalloc_check); everything else in the array is written before it is read
+    if (fresh && cudaMemsetAsync(err, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
     int32_t* lens = (int32_t*)((uint8_t*)base + 256);
     uint8_t* parts = (uint8_t*)base + kHeaderBytes;
 
@@ -146,7 +163,7 @@ extern "C" kvc_status kvc_decode_attend_noalloc(const void* keys, const void* va
         LengthsParam p;
         const int n = batch - off < 256 ? batch - off : 256;
         for (int i = 0; i < n; ++i) p.len_minus_one[i] = lengths[off + i] - 1;
-        noalloc_prologue<<<1, 256, 0, s>>>(lens, err, p, off, n);
+        noalloc_prologue<<<1, 256, 0, s>>>(lens, p, off, n);
         if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
     }
     DecodeLaunch dl{};
@@ -166,7 +183,28 @@ extern "C" kvc_status kvc_decode_attend_noalloc(const void* keys, const void* va
     dl.C = capacity;
     dl.split_rows = (int)r;
     dl.max_splits = max_splits;
+    dl.test_stall = g_test_stall.exchange(0);
     if (launch_decode_bf16(dl, s) != cudaSuccess) return KVC_ERR_CUDA;
     if (max_splits > 1 && launch_decode_combine(dl, s) != cudaSuccess) return KVC_ERR_CUDA;
     return KVC_OK;
+}
+
+extern "C" kvc_status kvc_noalloc_check(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_scratch_ptr[dev]) return KVC_OK;   // no call has run on this device
+    }
+    uint32_t* err = (uint32_t*)scratch_on(dev);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    if (!word) return KVC_OK;
+    if (cudaMemsetAsync(err, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    return KVC_ERR_DEVICE;
 }

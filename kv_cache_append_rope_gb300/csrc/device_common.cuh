@@ -14,8 +14,28 @@ enum DeviceError : uint32_t {
     DEV_ERR_TMEM = 4u,        // tensor-memory allocation returned an unusable address
     DEV_ERR_FULL = 8u,        // a device-length decode step met a full sequence or a position
                               // beyond the RoPE table and was rejected as a whole
-    DEV_ERR_CUT = 16u         // a device-checked truncate met a cut beyond a length
+    DEV_ERR_CUT = 16u,        // a device-checked truncate met a cut beyond a length
+    DEV_ERR_BOUNDS = 32u      // debug builds: a length or slot index outside the cache; the
+                              // access was skipped
 };
+
+// Debug builds (compiled with -DKVC_DEBUG, libkvc_debug.so) check every length
+// and slot index a kernel derives against the capacity before it touches
+// storage; a failed check records DEV_ERR_BOUNDS in the error word and skips the
+// access -- never a trap or an assert, so the context stays usable and
+// kvc_check reports it.  Release builds compile the checks away.
+#ifdef KVC_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+
+// True when `ok` holds or the build has no debug checks; else records the bit.
+__device__ __forceinline__ bool debug_check(bool ok, uint32_t* err) {
+    if (!kDebug || ok) return true;
+    if (err) atomicOr(err, (uint32_t)DEV_ERR_BOUNDS);
+    return false;
+}
 
 // ---- storage dtype traits ------------------------------------------------
 

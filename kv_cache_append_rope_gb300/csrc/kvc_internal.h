@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <vector>
 
@@ -23,7 +24,17 @@ struct KvLayout {
     int P;                  // rows per block: a power of two >= 64
     int shift;              // log2(P)
     int C, Hkv;
+    int nblocks;            // paged: physical blocks in the pool (debug-build checks)
 };
+
+// Debug builds: the stored row of (b, slot) exists -- slot inside the capacity and,
+// for paged storage, a valid block behind it.
+__host__ __device__ inline bool kv_slot_ok(const KvLayout& L, int b, int slot) {
+    if (slot < 0 || slot >= L.C) return false;
+    if (!L.table) return true;
+    const int blk = L.table[(int64_t)b * L.nblk + (slot >> L.shift)];
+    return blk >= 0 && blk < L.nblocks;
+}
 
 __host__ __device__ inline int64_t kv_row(const KvLayout& L, int b, int h, int slot) {
     if (!L.table) return ((int64_t)b * L.Hkv + h) * L.C + slot;
@@ -158,9 +169,33 @@ struct Handle {
         while ((1 << L.shift) < L.P) ++L.shift;
         L.C = cfg.capacity;
         L.Hkv = cfg.heads_kv;
+        L.nblocks = nblocks;
         return L;
     }
     int32_t* next_layer(int l) const { return next_d + (size_t)l * cfg.batch; }
+};
+
+// One-time set-up of a kernel's attributes, done once per device: a function
+// attribute (such as the dynamic shared-memory opt-in) belongs to the context of
+// the device that was current when it was set, so a flag shared by the whole
+// process would skip the set-up on a second GPU.  Safe to call from several host
+// threads: the set-up is idempotent, so two threads may both run it.
+class PerDeviceOnce {
+public:
+    template <typename F>
+    cudaError_t run(F setup) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+        if (bit && (done_.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        e = setup();
+        if (e == cudaSuccess && bit) done_.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+
+private:
+    std::atomic<uint64_t> done_{0};
 };
 
 // ---- kernel launchers (each returns the launch status) ----------------------
@@ -191,6 +226,7 @@ struct GenericAttendLaunch {
     int B, Hq, Hkv, S, C, d;
     int window;              // 0, or each row attends its `window` most recent slots
     KvLayout kv;
+    uint32_t* err;           // device error word (debug-build bounds checks)
 };
 cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaStream_t s);
 
@@ -236,18 +272,27 @@ cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);
 int decode_bf16_ctas_per_sm(int group);
 
 cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,
-                          int uniform_rows, int B, cudaStream_t s);
+                          int uniform_rows, int B, int C, uint32_t* err, cudaStream_t s);
 cudaError_t launch_truncate(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                             cudaStream_t s);
 constexpr int kCommitMaxLayers = 64;      // layers one commit launch advances
 struct CommitLayers { int32_t layer[kCommitMaxLayers]; int n; };
-cudaError_t launch_commit_layers(int32_t* len, int32_t* next, const CommitLayers& layers, int B, cudaStream_t s);
+cudaError_t launch_commit_layers(int32_t* len, int32_t* next, const CommitLayers& layers, int B, int C,
+                                 uint32_t* err, cudaStream_t s);
 cudaError_t launch_truncate_checked(int32_t* len, int32_t* next, const int32_t* cut, int layers, int B,
                                     uint32_t* err, cudaStream_t s);
 // Copies whole blocks (src, dst) = pairs[i] of every layer's key and value pool.
 cudaError_t launch_copy_blocks(char* K, char* V, size_t layer_bytes, int layers, size_t block_bytes,
                                const int2* pairs, int npairs, cudaStream_t s);
 cudaError_t launch_set_lengths(int32_t* len, int32_t* next, int layers, int B, int b, int value, cudaStream_t s);
+// Logical rows of one layer into [B, H_kv, R, d] arrays (rows >= len zero, positions -1).
+cudaError_t launch_read_rows(const void* K, const void* V, const int32_t* pos, const int32_t* len, const KvLayout& kv,
+                             void* Ko, void* Vo, int32_t* Po, int B, int Hkv, int R, int row_bytes, cudaStream_t s);
+// Test-only: poison every storage row no sequence holds (keys 0, values vbits).
+cudaError_t launch_poison(void* K, void* V, size_t layer_bytes, const int32_t* live, int layers, int groups, int Hkv,
+                          int R, int d, int esz, unsigned long long vbits, cudaStream_t s);
+// Test-only: the next kvc_decode_attend_noalloc call's producer issues no loads.
+void noalloc_arm_test_stall();
 cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long long* first,
                              cudaStream_t s);
 

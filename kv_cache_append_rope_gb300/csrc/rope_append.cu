@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(AppendLaunch a) {
                 atomicOr(a.err, (uint32_t)DEV_ERR_SLOT);
                 continue;
             }
+            if (kind != 0 && !debug_check(kv_slot_ok(a.kv, b, slot), a.err)) continue;
             rope_one<T, QO, P, FAST>(a, kind, b, h, i0 + rr, slot, pos, c, in[rr]);
         }
     }
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(256) rope_append_bf16_kernel(AppendLaunch a) {
             atomicOr(a.err, (uint32_t)DEV_ERR_SLOT);
             continue;
         }
+        if (kind != 0 && !debug_check(kv_slot_ok(a.kv, b, slot), a.err)) continue;
         const bf* src = base + (int64_t)i * a.d + 8 * c;
         uint4 in[kHeads];
 #pragma unroll

@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     const int g = h / (a.Hq / a.Hkv);
     const int cut = a.slot0[b];
     const int rows_b = a.seqlen[b];
+    // debug builds: the item's query and key slots lie inside the sequence (checked by
+    // every thread alike, before any barrier or tensor-memory allocation)
+    if (!debug_check(cut >= 0 && rows_b >= 0 && cut + rows_b <= a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
     int jlo[QT], jhi[QT];
 #pragma unroll
     for (int X = 0; X < QT; ++X) tile_range(QT * qp + X, cut, rows_b, a.window, jlo[X], jhi[X]);
@@ -481,17 +484,16 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 int suffix_tc_grid(int sms) { return sms; }
 
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run([] {
         // the register split assumes the launch allocation it was computed for
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, suffix_tc_kernel);
-        if (e != cudaSuccess) return e;
+        cudaError_t r = cudaFuncGetAttributes(&fa, suffix_tc_kernel);
+        if (r != cudaSuccess) return r;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(suffix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+        return cudaFuncSetAttribute(suffix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (e != cudaSuccess) return e;
     if (grid <= 0) return cudaSuccess;
     suffix_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();

@@ -191,6 +191,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int g = h / (a.Hq / a.Hkv);
     const int cut = a.slot0[b];
     const int rows_b = a.seqlen[b];
+    // debug builds: both CTAs of the pair read the same item and leave together, before
+    // any cluster barrier
+    if (!debug_check(cut >= 0 && rows_b >= 0 && cut + rows_b <= a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
     // pair tile X covers query tiles 4 quad + 2 X (in CTA 0) and + 1 (in CTA 1); its key
     // range is the union of theirs
     int jlo[QT], jhi[QT];
@@ -519,16 +522,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_suffix_tc2(const SuffixLaunch2& a, int items, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run([] {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, suffix_tc2_kernel);
-        if (e != cudaSuccess) return e;
+        cudaError_t r = cudaFuncGetAttributes(&fa, suffix_tc2_kernel);
+        if (r != cudaSuccess) return r;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(suffix_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+        return cudaFuncSetAttribute(suffix_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (e != cudaSuccess) return e;
     if (items <= 0) return cudaSuccess;
     suffix_tc2_kernel<<<2 * items, THREADS, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();

@@ -197,6 +197,32 @@ class KVCache:
         self._check(L.lib.kvc_get_lengths(self._h, layer, ln, nx))
         return list(ln), list(nx)
 
+    def get_len(self, layer=0):
+        """kvc_get_len: the host mirror of one layer's logical lengths."""
+        ln = (ctypes.c_int32 * self.config.batch)()
+        self._check(L.lib.kvc_get_len(self._h, layer, ln))
+        return list(ln)
+
+    def read_rows(self, layer=0, rows=None, stream=None):
+        """kvc_read_rows: the logical snapshot of one layer -- keys and values [B, H_kv, R, d_h]
+        in the storage dtype and positions [B, R] int32 (R = ``rows``, default C); rows at or past a
+        sequence's length are zero (positions -1)."""
+        c = self.config
+        R = c.capacity if rows is None else int(rows)
+        shape = (c.batch, c.heads_kv, R, c.head_dim)
+        K = torch.empty(shape, dtype=self.storage_dtype, device=self.device)
+        V = torch.empty(shape, dtype=self.storage_dtype, device=self.device)
+        P = torch.empty((c.batch, R), dtype=torch.int32, device=self.device)
+        dk, dv = tensor_desc(K), tensor_desc(V)
+        self._check(L.lib.kvc_read_rows(self._h, layer, ctypes.byref(dk), ctypes.byref(dv),
+                                        ctypes.c_void_p(P.data_ptr()), _stream(stream)))
+        return K, V, P
+
+    def poison(self):
+        """Test only (KVC_OPT_TEST_POISON): every stored row no sequence holds gets keys 0 and
+        values 1e4, so that a kernel reading past a length shows in its output."""
+        self.set_option(L.OPT_TEST_POISON, 1)
+
     def share_prefix(self, dst, src, rows, stream=None):
         """kvc_share_prefix: sequence dst (empty) takes src's first rows by sharing its blocks."""
         self._check(L.lib.kvc_share_prefix(self._h, dst, src, rows, _stream(stream)))

@@ -3,7 +3,21 @@ import numpy as np
 import pytest
 import torch
 
+from gpu_helpers_cpu import REL_GUARD, rel_err  # noqa: F401  (re-export)
+
 TOL = {"f64": 1e-12, "f32": 1e-5, "bf16": 2e-2}
+
+
+def assert_close(got, ref, dtype, what=""):
+    """The contract (max-abs TOL[dtype]) and, for bf16, the relative-error regression
+    guard REL_GUARD on every output row (the last axis is the head dimension).
+    Returns the max-abs error."""
+    err = float(np.abs(np.asarray(got) - np.asarray(ref)).max())
+    assert err <= TOL[dtype], (what, err)
+    if dtype == "bf16":
+        rel = rel_err(got, ref)
+        assert rel <= REL_GUARD, (what, "relative error", rel)
+    return err
 TORCH = {"f64": torch.float64, "f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -18,23 +32,19 @@ def to_np(t):
 
 
 def storage_np(cache, layer=0):
-    """Stored keys and values as [B, H_kv, C, d_h] float64 and positions [B, C]; a paged
-    pool is gathered through the block table (slots without a block read as 0)."""
+    """Logical snapshot of one layer through kvc_read_rows: keys and values as
+    [B, H_kv, C, d_h] float64 and positions [B, C]; rows at or past a sequence's
+    length read as 0 (positions -1).  Paged storage is gathered by the library."""
+    K, V, P = cache.read_rows(layer)
+    return to_np(K), to_np(V), P.cpu().numpy()
+
+
+def raw_storage_np(cache, layer=0):
+    """Every byte of a contiguous layer's storage (rows past the lengths included):
+    keys and values [B, H_kv, C, d_h] float64, positions [B, C]."""
+    assert not cache.config.block_rows, "raw storage is read from contiguous caches only"
     K, V, P = cache.storage(layer)
-    K, V, P = to_np(K), to_np(V), P.cpu().numpy()
-    c = cache.config
-    if not c.block_rows:
-        return K, V, P
-    table, _ = cache.block_table()
-    out = []
-    for pool in (K, V):
-        x = np.zeros((c.batch, c.heads_kv, table.shape[1] * c.block_rows, c.head_dim))
-        for b in range(c.batch):
-            for j, blk in enumerate(table[b]):
-                if blk >= 0:
-                    x[b, :, j * c.block_rows:(j + 1) * c.block_rows] = pool[blk]
-        out.append(x[:, :, :c.capacity])
-    return out[0], out[1], P
+    return to_np(K), to_np(V), P.cpu().numpy()
 
 
 def device_tensor(a, dtype):

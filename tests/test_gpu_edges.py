@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, device_tensor, need_gpu, storage_np, to_np
+from gpu_helpers import TOL, device_tensor, need_gpu, raw_storage_np, storage_np, to_np
 from kv_cache_append_rope_gb300 import workloads as W
 from kv_cache_append_rope_gb300.kvc import KVCache, KVCError
 from oracle import attention as A
@@ -23,10 +23,10 @@ def test_empty_chunk_changes_nothing():
     cache = KVCache(B, H, C, D)
     k, v, q = _rows(B, H, 8, D, 1), _rows(B, H, 8, D, 2), _rows(B, H, 8, D, 3)
     cache.prefill_suffix(0, q, k, v, seqlen=[5, 3])
-    before = storage_np(cache)
+    before = raw_storage_np(cache)
     out = cache.prefill_suffix(0, q, k, v, seqlen=[0, 0])
     assert cache.get_lengths(0) == ([5, 3], [5, 3])
-    for a, b in zip(before, storage_np(cache)):
+    for a, b in zip(before, raw_storage_np(cache)):
         np.testing.assert_array_equal(a, b)
     assert torch.count_nonzero(out).item() == 0
     cache.check()
@@ -44,13 +44,13 @@ def test_capacity_boundary_and_position_limit():
     ref = A.decode_reference(to_np(q)[0, :, C - 1], C - 1, to_np(k)[0, :, :C], to_np(v)[0, :, :C], np.arange(C),
                              BASE, "bf16")
     assert np.abs(out[0, :, 0] - ref).max() <= TOL["bf16"]
-    before = storage_np(cache)
+    before = raw_storage_np(cache)
     for call in (lambda: cache.append_attend(0, one(q, C), one(k, C), one(v, C)),
                  lambda: cache.prefill_suffix(0, None, one(k, C), one(v, C), out=False)):
         with pytest.raises(KVCError) as e:
             call()
         assert e.value.name == "KVC_ERR_FULL"
-    for a, b in zip(before, storage_np(cache)):
+    for a, b in zip(before, raw_storage_np(cache)):
         np.testing.assert_array_equal(a, b)
     # RoPE table of 64 positions: position 63 is the last one, 64 is rejected
     small = KVCache(1, 2, 64, D, rope_max_positions=64)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from golden_data import ch37_trace
-from gpu_helpers import need_gpu, storage_np, to_np
+from gpu_helpers import need_gpu, raw_storage_np, storage_np, to_np
 from kv_cache_append_rope_gb300 import workloads as W
 from kv_cache_append_rope_gb300.kvc import KVCache, KVCError
 from oracle import attention as A
@@ -49,13 +49,16 @@ def test_fixture_trace_and_reset():
         assert np.abs(ref.reshape(1, 4) @ F.head_swap_projection() - got[p]).max() <= 1e-12
     # reset: length 0, same allocation, bytes unchanged, identical replay
     ptr_before = cache.storage(0)[0].data_ptr()
-    before = storage_np(cache)
+    before = raw_storage_np(cache)
     cache.reset()
-    assert cache.get_lengths(0) == ([0], [0])
-    after = storage_np(cache)
+    assert cache.get_lengths(0) == ([0], [0]) and cache.get_len(0) == [0]
+    after = raw_storage_np(cache)
     assert cache.storage(0)[0].data_ptr() == ptr_before
     for a, b in zip(before, after):
         np.testing.assert_array_equal(a, b)
+    # the logical snapshot holds no row after a reset
+    K0, V0, P0 = storage_np(cache)
+    assert not K0.any() and not V0.any() and (P0 == -1).all()
     replay = [_swap(cache.append_attend(0, _rows_dev(p), _rows_dev(p), _rows_dev(p))) for p in range(3)]
     for a, b in zip(replay, got):
         np.testing.assert_array_equal(a, b)
@@ -83,7 +86,7 @@ def test_random_variant_incremental_equals_full_prefix():
 
 
 def _state(cache):
-    K, V, P = storage_np(cache)
+    K, V, P = raw_storage_np(cache)
     return K.copy(), V.copy(), P.copy(), cache.get_lengths(0)
 
 

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, device_tensor, need_gpu, storage_np, to_np
+from gpu_helpers import TOL, device_tensor, need_gpu, raw_storage_np, storage_np, to_np
 from kv_cache_append_rope_gb300 import _lib as L
 from kv_cache_append_rope_gb300 import workloads as W
 from kv_cache_append_rope_gb300.kvc import KVCache, KVCError
@@ -128,14 +128,14 @@ def test_device_full_rejects_the_whole_step():
     cache.set_option(L.OPT_DEVICE_LENGTHS, 1)
     cache.append_attend(0, step_rows(q, L0, 0), step_rows(k, L0, 0), step_rows(v, L0, 0))   # fills sequence 1
     cache.check()
-    K0, V0, P0 = storage_np(cache)
+    K0, V0, P0 = raw_storage_np(cache)
     cache.append_attend(0, step_rows(q, L0, 1), step_rows(k, L0, 1), step_rows(v, L0, 1))   # rejected on the device
     with pytest.raises(KVCError) as e:
         cache.check()
     assert e.value.name == "KVC_ERR_DEVICE" and "cache full" in str(e.value)
     cache.sync_lengths()
     assert cache.get_lengths(0) == ([11, 128, 51], [11, 128, 51])
-    K1, V1, P1 = storage_np(cache)
+    K1, V1, P1 = raw_storage_np(cache)
     np.testing.assert_array_equal(K0, K1)
     np.testing.assert_array_equal(V0, V1)
     np.testing.assert_array_equal(P0, P1)

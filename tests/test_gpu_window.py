@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, device_tensor, need_gpu, storage_np, to_np
+from gpu_helpers import assert_close, TOL, device_tensor, need_gpu, storage_np, to_np
 from kv_cache_append_rope_gb300 import _lib as L
 from kv_cache_append_rope_gb300 import kvc
 from kv_cache_append_rope_gb300 import workloads as W
@@ -55,6 +55,7 @@ def test_windowed_decode_matches_oracle(dtype, D, Hq, Hkv, mode, window):
         cache.set_option(L.OPT_DECODE_SPLIT_ROWS, 64)
     S = max(L0)
     cache.prefill_suffix(0, None, kd[:, :, :S].contiguous(), vd[:, :, :S].contiguous(), seqlen=L0, out=False)
+    cache.poison()
     if mode == "device":
         cache.set_option(L.OPT_DEVICE_LENGTHS, 1)
     idx = lambda i: torch.tensor([l + i for l in L0], device="cuda")
@@ -67,7 +68,7 @@ def test_windowed_decode_matches_oracle(dtype, D, Hq, Hkv, mode, window):
         n = L0[b] + steps
         ref = A.decode_steps_reference(np.transpose(q[b, :, L0[b]:n], (1, 0, 2)), k[b, :, :n], v[b, :, :n],
                                        L0[b], BASE, dtype, window=window)
-        worst = max(worst, np.abs(np.stack([o[b, :, 0] for o in outs]) - ref).max())
+        worst = max(worst, assert_close(np.stack([o[b, :, 0] for o in outs]), ref, dtype, b))
         K, V = A.stored_rows(k[b, :, :n], v[b, :, :n], np.arange(n)[None], BASE, dtype)
         np.testing.assert_array_equal(Ks[b, :, :n], K)
         np.testing.assert_array_equal(Vs[b, :, :n], V)
@@ -84,6 +85,9 @@ def test_windowed_decode_matches_oracle(dtype, D, Hq, Hkv, mode, window):
     ("bf16", 128, 2, 2, 2, 5000),     # wider than every sequence: full attention
     ("bf16", 128, 4, 2, 1, 100),      # generic kernel
     ("f64", 16, 2, 2, 1, 33),
+    ("bf16", 128, 4, 2, 3, 100),      # pair-of-SMs tile kernel: rank 1's first tiles lie before its window
+    ("bf16", 128, 4, 4, 3, 1),
+    ("bf16", 128, 2, 1, 3, 700),
 ])
 def test_windowed_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, window):
     need_gpu()
@@ -95,14 +99,14 @@ def test_windowed_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel,
     cache.set_option(L.OPT_SUFFIX_KERNEL, kernel)
     cache.prefill_suffix(0, qd, kd, vd, out=False)
     cache.truncate(cuts)
+    cache.poison()
     S = max(T - c for c in cuts)
     sel = lambda x: torch.stack([torch.nn.functional.pad(x[b, :, cuts[b]:], (0, 0, 0, S - (T - cuts[b])))
                                  for b in range(B)]).contiguous()
     got = to_np(cache.prefill_suffix(0, sel(qd), sel(kd), sel(vd), seqlen=[T - c for c in cuts]))
     for b in range(B):
         ref = A.suffix_reference(q[b, :, cuts[b]:], k[b], v[b], np.arange(T), cuts[b], BASE, dtype, window=window)
-        err = np.abs(got[b, :, :T - cuts[b]] - ref).max()
-        assert err <= TOL[dtype], (b, err)
+        assert_close(got[b, :, :T - cuts[b]], ref, dtype, b)
     cache.check()
 
 

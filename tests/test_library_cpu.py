@@ -24,7 +24,26 @@ def test_every_declared_symbol_is_exported(kvc_lib):
     for n in names:
         assert hasattr(kvc_lib.lib, n), n
     assert set(names) == set(kvc_lib.EXPORTS)
-    assert kvc_lib.lib.kvc_abi_version() == 4
+    assert kvc_lib.lib.kvc_abi_version() == 5
+
+
+def test_debug_build_loads_and_exports_the_same_symbols(kvc_lib):
+    """libkvc_debug.so (every kernel's bounds checks compiled in) has the same ABI."""
+    from kv_cache_append_rope_gb300 import build
+    dbg = ctypes.CDLL(build.DEBUG_LIB)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    dbg.kvc_abi_version.restype = ctypes.c_int32
+    assert dbg.kvc_abi_version() == 5
+
+
+def test_length_query_and_no_handle_options_need_no_device(kvc_lib):
+    L = kvc_lib
+    ln = (ctypes.c_int32 * 1)()
+    assert L.STATUS[L.lib.kvc_get_len(None, 0, ln)] == "KVC_ERR_NULL"
+    assert L.STATUS[L.lib.kvc_read_rows(None, 0, None, None, None, None)] == "KVC_ERR_NULL"
+    # a NULL handle accepts only the no-alloc stall arm (a host flag), every other option is refused
+    assert L.STATUS[L.lib.kvc_set_option(None, L.OPT_TEST_POISON, 1)] == "KVC_ERR_NULL"
 
 
 def test_status_strings(kvc_lib):
