@@ -519,10 +519,11 @@ def start_workers(n=None):
 
 
 def cpu_baseline(bench, workers, unit):
-    """The oracle on the host cores: one task per core side by side (value = their work /
-    the slowest one's time), and one task alone (`one_core`)."""
+    """The oracle on the host cores, warm (a first untimed batch): one task per core side
+    by side (value = their work / the slowest one's time), and one task alone (`one_core`)."""
     scale = 1e9 if unit == "GB/s" else 1e12
     tasks, work, desc = bench.cpu_tasks(workers.n, **CPU_TASK[bench.name])
+    workers.run(tasks)                    # untimed: each process builds its cos/sin table once
     secs = workers.run(tasks)
     wall = max(secs)
     line = {"value": round(sum(work) / scale / wall, 6), "unit": unit, "cores": workers.n, "kind": "oracle",
