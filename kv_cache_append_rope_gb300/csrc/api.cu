@@ -1001,12 +1001,9 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
         if ((uint64_t)B * Hq * S > (uint64_t)INT32_MAX)
             return fail(h, KVC_ERR_ELEMENT_OVERFLOW, "B * H_q * S must fit in 31 bits for the tile kernel");
     }
-    // The one-SM tile kernel rotates its query rows itself (the append kernel then skips
-    // the queries); the pair kernel and the generic kernel read rotated queries from
-    // scratch: bf16 for the pair kernel, the accumulator dtype for the generic one.
-    const bool q_in_tile_kernel = use_tc && !use_tc2;
+    // qrot scratch for the chunk: bf16 for the tile kernel, the accumulator dtype for the generic one
     const size_t acc = use_tc ? 2 : (dt == KVC_F64 ? 8 : 4);
-    const size_t qbytes = q_in_tile_kernel ? 0 : (size_t)B * Hq * S * D * acc;
+    const size_t qbytes = (size_t)B * Hq * S * D * acc;
     if (out && qbytes > h->qrot_chunk_bytes) {
         cudaStreamSynchronize(s);
         cudaFree(h->qrot_chunk);
@@ -1035,13 +1032,11 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
     ap.q = out ? q->data : nullptr; ap.k = k->data; ap.v = v->data;
     ap.K = h->K_layer(layer); ap.V = h->V_layer(layer); ap.positions = h->pos_layer(layer);
     ap.slot0 = h->len_layer(layer); ap.pos0 = start_d; ap.seqlen = seqlen_d;
-    ap.qrot = out && !q_in_tile_kernel ? h->qrot_chunk : nullptr; ap.qrot_kind = use_tc ? 2 : (dt == KVC_F64 ? 1 : 0);
+    ap.qrot = out ? h->qrot_chunk : nullptr; ap.qrot_kind = use_tc ? 2 : (dt == KVC_F64 ? 1 : 0);
     ap.rope = h->rope; ap.rope_f = h->rope_f; ap.err = h->err_d;
-    ap.B = B; ap.Hq = out && !q_in_tile_kernel ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D;
-    ap.max_positions = h->max_positions;
+    ap.B = B; ap.Hq = out ? Hq : 0; ap.Hkv = Hkv; ap.S = S; ap.C = C; ap.d = D; ap.max_positions = h->max_positions;
     ap.kv = h->layout();
-    // Without an output (or with the tile kernel, which rotates its own queries) the
-    // query heads are skipped (Hq = 0 in the launch).
+    // Without an output the query heads are skipped (Hq = 0 in the launch).
     KVC_CUDA(h, timed(h, KVC_KERNEL_ROPE_APPEND, s, [&] { return launch_rope_append(dt, ap, s); }));
     if (out && use_tc2 && !work.empty()) {
         SuffixLaunch2 sl{};
@@ -1057,9 +1052,8 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
         KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc2(sl, (int)work.size(), s); }));
     } else if (out && use_tc && !work.empty()) {
         SuffixLaunch sl{};
-        sl.q = (const __nv_bfloat16*)q->data;
-        sl.pos0 = start_d;
-        sl.rope_f = h->rope_f;
+        if (!encode_rows_map(&sl.tmQ, h->qrot_chunk, (uint64_t)B * Hq * S, 128))
+            return fail(h, KVC_ERR_CUDA, "cannot encode the query tensor map");
         // contiguous: 128-row boxes; paged: 64-row boxes, two per key tile
         sl.tmK = h->paged() ? h->tmap_k[layer] : h->tmap_k128[layer];
         sl.tmV = h->paged() ? h->tmap_v[layer] : h->tmap_v128[layer];

@@ -298,10 +298,7 @@ cudaError_t launch_nonfinite(int dtype, const void* x, int64_t n, unsigned long 
 
 // Tensor-core suffix-chunk kernel (bf16, d_h = 128).
 struct SuffixLaunch {
-    CUtensorMap tmK, tmV;        // one layer's keys and values
-    const __nv_bfloat16* q;      // [B,H_q,S,128] unrotated queries (the caller's chunk)
-    const int32_t* pos0;         // [B] device: position of row 0 of each sequence
-    const float2* rope_f;        // float32 cos/sin table, or null (no rotation)
+    CUtensorMap tmQ, tmK, tmV;   // Q: [B*H_q*S, 128] bf16 rotated queries; K/V: one layer
     const int32_t* slot0;        // [B] device, slot of suffix row 0 (= cut)
     const int32_t* seqlen;       // [B] device
     const int4* work;            // tiles: (b, h, q_tile, n_kv_tiles), longest first

@@ -23,8 +23,9 @@
 // diagonal ones masked element-wise.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 K tiles
-//             into a 2-stage ring, lane 1 V tiles into a 2-stage ring.
+//   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 both Q
+//             tiles once and K tiles into a 2-stage ring, lane 1 V tiles into
+//             a 2-stage ring.
 //   warp 1    TMEM allocator (512 columns) and, on one elected thread, the MMA
 //             issuer.  Per key tile j: O_A += P_A V_j, then S_A = Q_A K_{j+1}^T,
 //             then O_B += P_B V_j, then S_B = Q_B K_{j+1}^T -- so that while one
@@ -38,19 +39,11 @@
 //   warps 2-3 idle (they complete warpgroup 0, whose registers go to the softmax).
 //   warps 4-7 softmax of tile A, warps 8-11 of tile B: one thread per query row
 //             (= TMEM lane of its sub-partition) owning the whole 128-column row
-//             -- no exchange between warps.  First each thread stages its query
-//             row: it reads the unrotated row ([Ch37] "Append along the position
-//             axis": the query is rotated for its position, used and never
-//             stored), rotates each interleaved pair at the row's position with
-//             the float32 cos/sin table and rounds it to bf16 into the Q tile in
-//             shared memory, in the 128-byte-swizzled layout the MMA descriptors
-//             read.  Then per key tile: tcgen05.ld of S, causal (and window)
-//             mask, running max in log2 units, O rescaled through TMEM only when
-//             the max grows by more than 2^8 (the final division by the running
-//             sum makes the stale max exact), P written with tcgen05.st in two
-//             halves of 64 keys, each signalled as soon as it is stored so that
-//             the MMA thread starts P V on the first half while the second is
-//             computed; finally the normalised O row is stored to global memory.
+//             -- no exchange between warps: tcgen05.ld of S, causal (and
+//             window) mask, running max in log2 units, O rescaled through TMEM
+//             only when the max grows by more than 2^8 (the final division by
+//             the running sum makes the stale max exact), P written with
+//             tcgen05.st, then the normalised O row stored to global memory.
 // Every mbarrier wait is bounded (DEV_ERR_WAIT_TIMEOUT); the MMA thread waits
 // for its own last commit and the TMA thread for its own copies before the
 // allocator warp frees the tensor memory.
@@ -91,7 +84,7 @@ constexpr int kTileCache = 256;            // paged: key tiles whose row coordin
 struct Bars {
     uint64_t q_full;
     uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
-    uint64_t s_full[QT], p_full[QT][2];   // P_X keys 0..63 and 64..127
+    uint64_t s_full[QT], p_full[QT];
     uint64_t o_done;
     uint32_t tmem_base;
     int err;
@@ -159,7 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     const int n = max(jhi[0], jhi[1]) - j_first;
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->q_full), NSW);   // one arrival per softmax warp (its rows staged)
+        mbar_init(smem_u32(&bars->q_full), 1);
         for (int s = 0; s < KST; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
             mbar_init(smem_u32(&bars->k_empty[s]), 1);
@@ -170,8 +163,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         }
         for (int X = 0; X < QT; ++X) {
             mbar_init(smem_u32(&bars->s_full[X]), 1);
-            mbar_init(smem_u32(&bars->p_full[X][0]), 4);
-            mbar_init(smem_u32(&bars->p_full[X][1]), 4);
+            mbar_init(smem_u32(&bars->p_full[X]), 4);
         }
         mbar_init(smem_u32(&bars->o_done), 1);
         bars->err = 0;
@@ -197,8 +189,8 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // lane 0 streams the K ring, lane 1 the V ring, so that the K look-ahead never
-        // waits behind a V stage that is still being read.
+        // lane 0 streams both Q tiles and the K ring, lane 1 the V ring, so that the
+        // K look-ahead never waits behind a V stage that is still being read.
         if (lane < 2) {
             const int kvrow = (b * a.Hkv + g) * a.C;   // contiguous storage
             const bool is_k = lane == 0;
@@ -208,6 +200,20 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             const CUtensorMap* map = is_k ? &a.tmK : &a.tmV;
             uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
             prefetch_tmap(map);
+            uint32_t qb = 0;
+            if (is_k) {
+                prefetch_tmap(&a.tmQ);
+                qb = smem_u32(&bars->q_full);
+                mbar_arrive_expect_tx(qb, QT * TILE);
+#pragma unroll
+                for (int X = 0; X < QT; ++X) {
+                    // rows past the chunk belong to the next head or lie outside the map
+                    // (filled with zeros); their results are never stored
+                    const int qrow = (b * a.Hq + h) * a.S + (QT * qp + X) * BM;
+                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE), &a.tmQ, 0, qrow, qb);
+                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE + HALF), &a.tmQ, 64, qrow, qb);
+                }
+            }
             int issued = 0;
             for (int j = 0; j < n && !*(volatile int*)&bars->err; ++j) {
                 const int s = j % NS, use = j / NS;
@@ -235,6 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             }
             // Our own copies must have landed before the CTA's shared memory is released
             // (bounded in time only: an error raised elsewhere must not cut this short).
+            if (is_k) mbar_wait_bounded(qb, 0);
             for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
                 mbar_wait_bounded(smem_u32(&full[t % NS]), (t / NS) & 1);
         }
@@ -285,25 +292,19 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 const uint64_t vd = dv + (uint64_t)((vs * TILE) >> 4);
                 for (int X = 0; ok && X < QT; ++X) {
                     if (active(X, jj)) {
-                        // P_X arrives in two halves of 64 keys: the first half's P V is
-                        // issued while the softmax warps still compute the second
-                        for (int half = 0; ok && half < 2; ++half) {
-                            if (!mbar_wait_bounded(smem_u32(&bars->p_full[X][half]), pv_count[X] & 1, a.err)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-#pragma unroll
-                            for (int k4 = 0; k4 < BN / 32; ++k4) {
-                                // A = P_X from tensor memory (16 keys = 8 columns per step),
-                                // B = V (rows = keys, contiguous head dims: MN-major)
-                                const int kk = half * (BN / 32) + k4;
-                                tc_mma_ts(tmem + COL_O + X * 128, tmem + COL_S + X * 128 + kk * 8,
-                                          vd + (uint64_t)(kk * 16 * 128 >> 4), idesc_pv,
-                                          (pv_count[X] > 0 || kk > 0));
-                            }
+                        if (!mbar_wait_bounded(smem_u32(&bars->p_full[X]), pv_count[X] & 1, a.err)) {
+                            ok = false;
+                            break;
                         }
-                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // A = P_X from tensor memory (16 keys = 8 columns per step),
+                            // B = V (rows = keys, contiguous head dims: MN-major)
+                            tc_mma_ts(tmem + COL_O + X * 128, tmem + COL_S + X * 128 + kk * 8,
+                                      vd + (uint64_t)(kk * 16 * 128 >> 4), idesc_pv,
+                                      (pv_count[X] > 0 || kk > 0));
+                        }
                         pv_count[X] += 1;
                     }
                     // the next S_X overwrites P_X: issued after the PV that reads it
@@ -335,41 +336,6 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         const uint32_t o_addr = lane_addr + COL_O + X * 128;
         const float sl2 = a.scale_log2;
         const int tile_slot0 = cut + qt * BM;        // slot of the tile's first row
-        {
-            // Stage the query row: rotate each interleaved pair (x, y) at the row's
-            // position p -- (x c - y s, x s + y c), c, s the float32 cos/sin of p theta_j,
-            // one fused multiply-add each -- round to bf16 and store the row's sixteen
-            // 16-byte chunks (4 pairs each) in the swizzled Q tile.  Rows past the chunk
-            // are zero (their results are never stored).
-            uint8_t* qtile = smem + OFF_Q + X * TILE;
-            const bool live = i < rows_b;
-            const uint4* src = reinterpret_cast<const uint4*>(a.q + (((int64_t)b * a.Hq + h) * a.S + i) * D);
-            const float4* cs = a.rope_f ? reinterpret_cast<const float4*>(a.rope_f + (int64_t)(a.pos0[b] + i) * (D / 2))
-                                        : nullptr;
-            uint4 raw[D / 8];
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) raw[c] = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                uint4 v = raw[c];
-                if (live && cs) {
-                    const float4 c01 = __ldg(cs + 2 * c), c23 = __ldg(cs + 2 * c + 1);
-                    const float cf[4] = {c01.x, c01.z, c23.x, c23.z}, sf[4] = {c01.y, c01.w, c23.y, c23.w};
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float x = __uint_as_float(w[p] << 16), y = __uint_as_float(w[p] & 0xffff0000u);
-                        w[p] = pack_bf16(fmaf(x, cf[p], -(y * sf[p])), fmaf(y, cf[p], x * sf[p]));
-                    }
-                    v = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                *reinterpret_cast<uint4*>(qtile + (c >> 3) * HALF + swz128(row, c & 7)) = v;
-            }
-            // generic-proxy stores, read next by the tensor core (async proxy)
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
-        }
         auto kbase_of = [](int jj) { return jj * BN; };
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -456,16 +422,13 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                         pk[e] = pack_bf16(p0, p1);
                     }
                     tmem_st16u(s_addr + q * 16, pk);
-                    if (q % 2 == 1) {
-                        // keys 0..63 (then 64..127) of P_X are stored: let the MMA thread go
-                        tmem_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X][q / 2]));
-                    }
                 }
                 l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
                 l_run += l4[0].x + l4[0].y;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X]));
             };
             if (masked)
                 tile(std::true_type{});
