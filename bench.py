@@ -83,6 +83,9 @@ def parse():
     p.add_argument("--graph", action="store_true",
                    help="decode workloads: lengths kept on the device, each bench step's decode calls "
                         "captured once in a CUDA graph and replayed")
+    p.add_argument("--suffix-kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                   help="suffix: 0 = the library's choice, 1 = generic, 2 = one-SM tile kernel, 3 = pair-of-SMs "
+                        "tile kernel")
     p.add_argument("--host-chunk", type=int, default=0,
                    help="suffix e2e: sequences per stage of the host-buffer call; 0 = the library's choice")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -546,6 +549,8 @@ def run_ours(args, name, world, rank, local, workers=None):
     cache = bench.cache
     if args.split_rows:
         cache.set_option(L.OPT_DECODE_SPLIT_ROWS, args.split_rows)
+    if args.suffix_kernel:
+        cache.set_option(L.OPT_SUFFIX_KERNEL, args.suffix_kernel)
     for _ in range(args.warmup):
         bench.step()
     torch.cuda.synchronize(device)

@@ -307,18 +307,22 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+            // (k-outer: the NT accumulators are independent chains, so consecutive MMAs
+            // do not wait on one another)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int row = kofs + nt * 8 + (lane & 7);
+            for (int kk = 0; kk < 4; ++kk) {
+                const int dim0 = kk * 32 + (lane >> 3) * 8;
+                uint32_t bk[NT][4];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int dim0 = kk * 32 + (lane >> 3) * 8;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int row = kofs + nt * 8 + (lane & 7);
                     const uint32_t addr = kt + (dim0 >> 6) * HALF_BYTES + swz128(row, (dim0 & 63) >> 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(sc[nt], qf[2 * kk], b0, b1);
-                    mma_bf16_16816(sc[nt], qf[2 * kk + 1], b2, b3);
+                    ldsm_x4(addr, bk[nt][0], bk[nt][1], bk[nt][2], bk[nt][3]);
                 }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk], bk[nt][0], bk[nt][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk + 1], bk[nt][2], bk[nt][3]);
             }
             // ---- mask keys beyond this split
 #pragma unroll
@@ -339,10 +343,24 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * rr], sc[nt][2 * rr + 1]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m[rr], mx);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float corr = fast_exp2(m[rr] - m_use);
-                m[rr] = m_new;
+                // The reference maximum moves only when a score passes it by more than 2^8
+                // (log2 units): exponentials up to 2^8 are exact enough in float32 and bf16,
+                // and the final division by the running sum cancels the reference, so a
+                // stale one changes nothing but rounding.  O is rescaled only then (a
+                // warp-wide decision: rows that did not move are multiplied by 1).
+                const bool grow = mx > m[rr] + 8.f;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float m_new = grow ? fmaxf(m[rr], mx) : m[rr];
+                    const float corr = grow && m[rr] > -INFINITY ? fast_exp2(m[rr] - m_new) : 1.f;
+                    m[rr] = m_new;
+                    l[rr] *= corr;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        o[n][2 * rr] *= corr;
+                        o[n][2 * rr + 1] *= corr;
+                    }
+                }
+                const float m_use = m[rr] == -INFINITY ? 0.f : m[rr];
                 float ps = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -352,12 +370,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                         sc[nt][2 * rr + e] = p;
                         ps += p;
                     }
-                l[rr] = l[rr] * corr + ps;
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][2 * rr] *= corr;
-                    o[n][2 * rr + 1] *= corr;
-                }
+                l[rr] += ps;
             }
             // ---- O += P V (V^T fragments through transposing ldmatrix)
 #pragma unroll

@@ -13,9 +13,9 @@
 // B = V with the 128 head dims split between the CTAs (64 each).  Per SM and key tile
 // the shared-memory port then carries 160 KB instead of 256 KB, and each CTA loads
 // half of every K and V tile.  MMA completions are multicast to both CTAs; P-ready
-// arrivals go to the leader's barriers.  Each CTA's TMA loads complete on its own
-// barriers, and an otherwise idle warp per CTA (warp 2: Q and K, warp 3: V) forwards
-// every completion to the leader's pair barrier with a cluster-scope arrive.
+// arrivals go to the leader's barriers.  Both CTAs' TMA loads complete directly on
+// the leader's barriers (the .cta_group::2 form of the bulk tensor copy signals the
+// pair's leader); the leader's producer arms each stage for the bytes of both CTAs.
 //
 // Tensor memory: both CTAs execute tcgen05.alloc.cta_group::2 and receive the same
 // base (the pair allocates together; 512 columns in each SM), and both free it after
@@ -60,7 +60,6 @@ constexpr float RESCALE_LOG2 = 8.0f;
 struct Bars {
     uint64_t q_full;                       // leader: both CTAs' query tiles landed
     uint64_t k_full[KST], v_full[VST];     // leader: both halves of a stage landed
-    uint64_t q_loc, k_loc[KST], v_loc[VST];  // each CTA: its own loads landed (TMA completion)
     uint64_t k_empty[KST], v_empty[VST];   // each CTA: the pair's MMAs released the stage
     uint64_t s_full[QT];                   // each CTA: S_X written
     uint64_t p_full[QT];                   // leader: P_X written in both CTAs
@@ -115,6 +114,16 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, cons
 }
 __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, const uint32_t* abort) {
     return __all_sync(0xffffffffu, wait_cluster(bar, parity, abort));
+}
+// Bulk tensor copy into this CTA's shared memory whose completion is counted on
+// `bar`, a barrier of the pair's leader (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -211,16 +220,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int my_tile[QT] = {4 * quad + (int)rank, 4 * quad + 2 + (int)rank};
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->q_full), 2);
-        mbar_init(smem_u32(&bars->q_loc), 1);
-        for (int s = 0; s < KST; ++s) mbar_init(smem_u32(&bars->k_loc[s]), 1);
-        for (int s = 0; s < VST; ++s) mbar_init(smem_u32(&bars->v_loc[s]), 1);
+        // full barriers: one arrival (the leader's producer, arming both CTAs' bytes)
+        mbar_init(smem_u32(&bars->q_full), 1);
         for (int s = 0; s < KST; ++s) {
-            mbar_init(smem_u32(&bars->k_full[s]), 2);
+            mbar_init(smem_u32(&bars->k_full[s]), 1);
             mbar_init(smem_u32(&bars->k_empty[s]), 1);
         }
         for (int s = 0; s < VST; ++s) {
-            mbar_init(smem_u32(&bars->v_full[s]), 2);
+            mbar_init(smem_u32(&bars->v_full[s]), 1);
             mbar_init(smem_u32(&bars->v_empty[s]), 1);
         }
         for (int X = 0; X < QT; ++X) {
@@ -246,73 +253,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         setmaxnreg_dec<kRegsLow>();
         if (warp == 0 && lane < 2) {
             // ------------------------------------------------------------ TMA producers
-            // (both CTAs; completions counted on the leader's barriers)
+            // (both CTAs; every copy completes on the leader's barrier of its stage, which
+            // the leader arms for both CTAs' bytes)
             const int kvrow = (b * a.Hkv + g) * a.C;
             const bool is_k = lane == 0;
             const int NS = is_k ? KST : VST;
             const uint32_t stage_bytes = is_k ? KSTAGE : VSTAGE;
-            uint64_t* full = is_k ? bars->k_loc : bars->v_loc;   // this CTA's own loads
+            uint64_t* full = is_k ? bars->k_full : bars->v_full;
             uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
             uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
             const CUtensorMap* map = is_k ? &a.tmK64 : &a.tmV128;
             prefetch_tmap(map);
             if (is_k) {
                 prefetch_tmap(&a.tmQ);
-                const uint32_t qb = smem_u32(&bars->q_loc);
-                mbar_arrive_expect_tx(qb, QT * TILE);
+                if (leader) mbar_arrive_expect_tx(smem_u32(&bars->q_full), 2 * QT * TILE);
+                const uint32_t qb = mapa(smem_u32(&bars->q_full), 0);
 #pragma unroll
                 for (int X = 0; X < QT; ++X) {
                     const int qrow = (b * a.Hq + h) * a.S + my_tile[X] * BM;
-                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE), &a.tmQ, 0, qrow, qb);
-                    tma_load_2d(smem_u32(smem + OFF_Q + X * TILE + HALF), &a.tmQ, 64, qrow, qb);
+                    tma_load_2d_pair(smem_u32(smem + OFF_Q + X * TILE), &a.tmQ, 0, qrow, qb);
+                    tma_load_2d_pair(smem_u32(smem + OFF_Q + X * TILE + HALF), &a.tmQ, 64, qrow, qb);
                 }
             }
-            int issued = 0;
+            bool failed = false;
             for (int j = 0; j < n && !*(volatile int*)&bars->err && !*(volatile uint32_t*)a.err; ++j) {
                 const int s = j % NS, use = j / NS;
                 if (j >= NS && !wait_cluster(smem_u32(&empty[s]), (use - 1) & 1, a.err)) {
                     fail_wait(bars, a.err);
+                    failed = true;
                     break;
                 }
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, stage_bytes);
+                if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * stage_bytes);
+                const uint32_t fb = mapa(smem_u32(&full[s]), 0);
                 const int key0 = kvrow + (j_first + j) * BN;
                 if (is_k) {
                     // this CTA's 64 keys of the tile, both 64-dim halves
-                    tma_load_2d(smem_u32(ring + s * KSTAGE), map, 0, key0 + 64 * (int)rank, fb);
-                    tma_load_2d(smem_u32(ring + s * KSTAGE + KHALF), map, 64, key0 + 64 * (int)rank, fb);
+                    tma_load_2d_pair(smem_u32(ring + s * KSTAGE), map, 0, key0 + 64 * (int)rank, fb);
+                    tma_load_2d_pair(smem_u32(ring + s * KSTAGE + KHALF), map, 64, key0 + 64 * (int)rank, fb);
                 } else {
                     // all 128 keys of the tile, this CTA's 64 dims
-                    tma_load_2d(smem_u32(ring + s * VSTAGE), map, 64 * (int)rank, key0, fb);
+                    tma_load_2d_pair(smem_u32(ring + s * VSTAGE), map, 64 * (int)rank, key0, fb);
                 }
-                issued = j + 1;
             }
-            // our own copies land before the final cluster barrier releases shared memory
-            if (is_k) mbar_wait_bounded(smem_u32(&bars->q_loc), 0);
-            for (int t = issued - NS < 0 ? 0 : issued - NS; t < issued; ++t)
-                mbar_wait_bounded(smem_u32(&full[t % NS]), (t / NS) & 1);
-        } else if ((warp == 2 || warp == 3) && lane == 0) {
-            // ------------------------------------------------------------ forwarders
-            // (both CTAs) each local completion becomes one arrival on the leader's pair
-            // barrier: warp 2 for Q and K, warp 3 for V
-            const bool is_k = warp == 2;
-            const int NS = is_k ? KST : VST;
-            uint64_t* loc = is_k ? bars->k_loc : bars->v_loc;
-            uint64_t* pair = is_k ? bars->k_full : bars->v_full;
-            bool ok = true;
-            if (is_k) {
-                ok = wait_cluster(smem_u32(&bars->q_loc), 0, a.err);
-                if (ok) mbar_arrive_cluster(mapa(smem_u32(&bars->q_full), 0));
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                const int s = j % NS;
-                if (!wait_cluster(smem_u32(&loc[s]), (j / NS) & 1, a.err)) {
-                    ok = false;
-                    break;
+            // Every copy issued here is consumed by the leader's MMAs, which wait for its
+            // stage to complete, before the final cluster barrier: on the normal path the
+            // shared memory is never released under a copy.  On an error path (a wait gave
+            // up) some copies may be unconsumed: give them a bounded 200 us to land.
+            if (failed || *(volatile int*)&bars->err || *(volatile uint32_t*)a.err) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) {
                 }
-                mbar_arrive_cluster(mapa(smem_u32(&pair[s]), 0));
             }
-            if (!ok) fail_wait(bars, a.err);
         } else if (warp == 1 && lane == 0 && leader) {
             // ------------------------------------------------------------ MMA issuer (leader)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(2 * BM, BN, false, false);
