@@ -60,8 +60,9 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # (ratio to the algorithmic bytes), the tile kernel's with the number of
 # sequences (each sequence's K/V comes from DRAM about once, then from L2).
 TRAFFIC = {
-    "mha_decode": ("ratio", (503467264.0 + 4079104.0) / 499236864.0),
-    "mqa_decode": ("ratio", (217853184.0 + 3945984.0) / 217403392.0),
+    "mha_decode": ("ratio", 1.013),
+    "gqa_decode": ("ratio", 1.0067),
+    "mqa_decode": ("ratio", 1.0106),
     "suffix": ("per_sequence", 375401472.0 + 174217472.0),
 }
 
