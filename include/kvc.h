@@ -471,13 +471,18 @@ typedef enum kvc_option {
                                       bf16), so that a kernel reading a row it must not moves its output
                                       by about 1e4 / t.  Lengths and held rows are unchanged; a prepared,
                                       uncommitted step's staged row is overwritten.  0 does nothing. */
-    KVC_OPT_TEST_PLANT_LENGTH = 10 /* test only, debug builds (libkvc_debug.so, compiled with KVC_DEBUG)
+    KVC_OPT_TEST_PLANT_LENGTH = 10, /* test only, debug builds (libkvc_debug.so, compiled with KVC_DEBUG)
                                       only, else KVC_ERR_CONFIG: synchronises the device and writes `value`
                                       into the DEVICE length and next position of layer 0, sequence 0,
                                       leaving the host mirror alone -- a state the host checks never
                                       produce -- so that the debug build's device bounds checks can be
                                       seen to record KVC_ERR_DEVICE bit 32 and skip the access.  Reset
                                       the cache afterwards. */
+    KVC_OPT_DECODE_TC = 11         /* 1 (default) = decode steps with more than 16 (up to 32) query heads per
+                                      key/value head run on the tensor-core decode kernel (tcgen05, the
+                                      heads as rows of a 128-row query tile, S and O in tensor memory)
+                                      when the step is fused, its lengths are host-held and the storage is
+                                      contiguous; 0 = the m16n8k16 decode kernel for every group size */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

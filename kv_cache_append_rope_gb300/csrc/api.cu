@@ -769,9 +769,22 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     ap.kv = h->layout();
 
     int split_rows = 0, max_splits = 1;
+    // Many query heads per key/value head on the fused step: the tensor-core decode kernel
+    // (one CTA per SM) instead of the m16n8k16 one (two per SM)
+    const bool tc_decode = fast && h->opt_decode_tc && h->opt_decode_fused && B <= kFusedMaxB && !dev_len &&
+                           !h->paged() && Hq / Hkv > 16 && Hq / Hkv <= 32;
     if (fast) {
         if (h->opt_split_rows > 0) {
             split_rows = (int)h->opt_split_rows;
+        } else if (tc_decode) {
+            // about one CTA of key rows per SM for the whole step: few, long splits keep the
+            // tensor-memory pipeline full (each CTA fills it once)
+            const int64_t keys = total_keys * Hkv;
+            const int sms = sm_count(h->cfg.device);
+            int64_t r = std::max<int64_t>(1024, (keys + sms - 1) / sms);
+            r = (r + 63) / 64 * 64;
+            r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
+            split_rows = (int)r;
         } else {
             const int G = Hq / Hkv;
             const int64_t target = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(G) * 4;
@@ -808,6 +821,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     if (fast && h->opt_decode_fused && B <= kFusedMaxB) {
         DecodeLaunch dl{};
         dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
+        dl.tmK128 = &h->tmap_k128[layer]; dl.tmV128 = &h->tmap_v128[layer];
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;
@@ -832,7 +846,9 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             dl.old_len[b] = lenh[b];
             dl.pos[b] = nexth[b];
         }
-        KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] { return launch_decode_bf16(dl, s); }));
+        KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] {
+            return tc_decode ? launch_decode_tc(dl, s) : launch_decode_bf16(dl, s);
+        }));
         if (!dl.merge_in_kernel && max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
         h->layer_version[layer] += 1;
@@ -1701,6 +1717,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_DECODE_PDL:
             h->opt_decode_pdl = value != 0;
+            return KVC_OK;
+        case KVC_OPT_DECODE_TC:
+            h->opt_decode_tc = value != 0;
             return KVC_OK;
         case KVC_OPT_DEVICE_LENGTHS: {
             if (value && h->paged())

@@ -147,6 +147,7 @@ struct Handle {
     int64_t opt_test_stall = 0;
     int64_t opt_device_lengths = 0;
     int64_t opt_decode_pdl = 1;
+    int64_t opt_decode_tc = 1;
     std::vector<uint64_t> layer_version;  // [L] bumped by every change of a layer's state or staged slot
     bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 
@@ -233,7 +234,8 @@ cudaError_t launch_attend_generic(int dtype, const GenericAttendLaunch& a, cudaS
 constexpr int kFusedMaxB = 256;   // sequences whose lengths travel as kernel parameters
 
 struct DecodeLaunch {
-    const CUtensorMap* tmK; const CUtensorMap* tmV;
+    const CUtensorMap* tmK; const CUtensorMap* tmV;       // 64-row boxes
+    const CUtensorMap* tmK128; const CUtensorMap* tmV128; // 128-row boxes (tensor-core decode)
     const float* qrot;       // [B,H_q,128] rotated queries (separate-kernel step)
     const int32_t* len;      // [B] old length: t = len + 1 (separate-kernel step)
     float* part_o; float2* part_ml;
@@ -269,6 +271,8 @@ struct DecodeLaunch {
 };
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);
+// Tensor-core decode (fused step, contiguous storage, 16 < H_q / H_kv <= 32); one CTA per SM.
+cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 int decode_bf16_ctas_per_sm(int group);
 
 cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,

@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 BASE = 10000.0
 
 
-def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0, fused=True):
+def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0, fused=True, tc=True,
+               window=0, out_dtype=None):
     """Prefill ragged prefixes, run `steps` decode steps; return (cache, outs, inputs)."""
     need_gpu()
     B = len(L0)
@@ -29,7 +30,9 @@ def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, see
     v = W.normal_np((B, Hkv, T, D), seed + 2)
     qd, kd, vd = (device_tensor(x, dtype) for x in (q, k, v))
     q, k, v = to_np(qd), to_np(kd), to_np(vd)        # the exact values the GPU sees
-    cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE)
+    cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE, window=window)
+    if not tc:
+        cache.set_option(L.OPT_DECODE_TC, 0)
     if generic:
         cache.set_option(L.OPT_FORCE_GENERIC, 1)
     if split_rows:
@@ -44,12 +47,13 @@ def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, see
     for i in range(steps):
         idx = torch.tensor([l + i for l in L0], device="cuda")
         sel = lambda x: x[torch.arange(B, device="cuda"), :, idx][:, :, None, :].contiguous()
-        outs.append(to_np(cache.append_attend(0, sel(qd), sel(kd), sel(vd))))
+        out = None if out_dtype is None else torch.empty((B, Hq, 1, D), dtype=out_dtype, device="cuda")
+        outs.append(to_np(cache.append_attend(0, sel(qd), sel(kd), sel(vd), out=out)))
     torch.cuda.synchronize()
     return cache, outs, (q, k, v)
 
 
-def check_against_oracle(dtype, cache, outs, qkv, L0, steps):
+def check_against_oracle(dtype, cache, outs, qkv, L0, steps, window=0):
     q, k, v = qkv
     B = len(L0)
     worst = 0.0
@@ -57,7 +61,7 @@ def check_against_oracle(dtype, cache, outs, qkv, L0, steps):
     for b in range(B):
         n = L0[b] + steps
         ref = A.decode_steps_reference(np.transpose(q[b, :, L0[b]:n], (1, 0, 2)), k[b, :, :n], v[b, :, :n],
-                                       L0[b], BASE, dtype)
+                                       L0[b], BASE, dtype, window=window)
         got = np.stack([o[b, :, 0] for o in outs])
         worst = max(worst, assert_close(got, ref, dtype, b))
         K, V = A.stored_rows(k[b, :, :n], v[b, :, :n], np.arange(n)[None], BASE, dtype)
@@ -90,6 +94,22 @@ def test_gqa_mqa_fast_path(Hkv):
     L0, steps = [1, 100, 257, 63], 3
     cache, outs, qkv = run_decode("bf16", 128, 32, Hkv, L0, steps, C=400)
     check_against_oracle("bf16", cache, outs, qkv, L0, steps)
+
+
+@pytest.mark.parametrize("Hq,Hkv,split_rows,window", [
+    (32, 1, 0, 0), (32, 1, 128, 0), (32, 1, 1024, 0), (32, 2, 0, 300), (48, 2, 256, 0), (32, 1, 64, 100),
+])
+def test_tensor_core_decode_matches_oracle_and_the_mma_sync_path(Hq, Hkv, split_rows, window):
+    """16 < G <= 32 query heads per key/value head run on the tcgen05 decode kernel: the
+    oracle, the m16n8k16 kernel (KVC_OPT_DECODE_TC = 0) and bf16 outputs agree."""
+    L0, steps = [1, 100, 257, 700], 3
+    cache, outs, qkv = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=800, split_rows=split_rows, window=window)
+    check_against_oracle("bf16", cache, outs, qkv, L0, steps, window=window)
+    _, ref, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=800, split_rows=split_rows, window=window, tc=False)
+    assert np.abs(np.stack(outs) - np.stack(ref)).max() < 1e-2
+    _, o16, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=800, split_rows=split_rows, window=window,
+                           out_dtype=torch.bfloat16)
+    np.testing.assert_array_equal(np.stack(o16), to_np(torch.from_numpy(np.stack(outs)).to(torch.bfloat16)))
 
 
 def test_split_sizes_agree():

@@ -20,14 +20,15 @@ from oracle import attention as A
 pytestmark = pytest.mark.gpu
 
 
-def test_bounded_wait_gives_up_and_is_reported():
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (32, 1)])     # m16n8k16 and tensor-core decode kernels
+def test_bounded_wait_gives_up_and_is_reported(Hq, Hkv):
     need_gpu()
-    B, H, D, C, L0 = 1, 1, 128, 256, 100
-    k = device_tensor(W.normal_np((B, H, L0 + 1, D), 101), "bf16")
-    v = device_tensor(W.normal_np((B, H, L0 + 1, D), 102), "bf16")
-    q = device_tensor(W.normal_np((B, H, L0 + 1, D), 103), "bf16")
+    B, D, C, L0 = 1, 128, 256, 100
+    k = device_tensor(W.normal_np((B, Hkv, L0 + 1, D), 101), "bf16")
+    v = device_tensor(W.normal_np((B, Hkv, L0 + 1, D), 102), "bf16")
+    q = device_tensor(W.normal_np((B, Hq, L0 + 1, D), 103), "bf16")
     one = lambda x: x[:, :, L0:L0 + 1].contiguous()
-    stalled = KVCache(B, H, C, D)
+    stalled = KVCache(B, Hq, C, D, heads_kv=Hkv)
     stalled.prefill_suffix(0, None, k[:, :, :L0].contiguous(), v[:, :, :L0].contiguous(), out=False)
     stalled.check()
     stalled.set_option(L.OPT_TEST_STALL, 1)
@@ -40,7 +41,7 @@ def test_bounded_wait_gives_up_and_is_reported():
     assert "timed out" in str(e.value)
     assert 0.5 < elapsed < 60.0
     # the context is intact: a new cache computes the same step correctly
-    fresh = KVCache(B, H, C, D)
+    fresh = KVCache(B, Hq, C, D, heads_kv=Hkv)
     fresh.prefill_suffix(0, None, k[:, :, :L0].contiguous(), v[:, :, :L0].contiguous(), out=False)
     out = to_np(fresh.append_attend(0, one(q), one(k), one(v)))
     ref = A.decode_steps_reference(to_np(q)[0, :, L0][None], to_np(k)[0], to_np(v)[0], L0, 10000.0, "bf16")
