@@ -773,18 +773,47 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
     // (one CTA per SM) instead of the m16n8k16 one (two per SM)
     const bool tc_decode = fast && h->opt_decode_tc && h->opt_decode_fused && B <= kFusedMaxB && !dev_len &&
                            !h->paged() && Hq / Hkv > 16 && Hq / Hkv <= 32;
+    struct {
+        bool on = false;
+        int32_t start[kFusedMaxB + 1];
+        int32_t seq[kFusedMaxB];
+        int32_t rows[kFusedMaxB];
+    } pieces;
     if (fast) {
         if (h->opt_split_rows > 0) {
             split_rows = (int)h->opt_split_rows;
         } else if (tc_decode) {
-            // about one CTA of key rows per SM for the whole step: few, long splits keep the
-            // tensor-memory pipeline full (each CTA fills it once)
-            const int64_t keys = total_keys * Hkv;
-            const int sms = sm_count(h->cfg.device);
-            int64_t r = std::max<int64_t>(1024, (keys + sms - 1) / sms);
-            r = (r + 63) / 64 * 64;
-            r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
-            split_rows = (int)r;
+            // One CTA per SM: every sequence is cut into its own number of equal pieces,
+            // about two waves of them in all, and the pieces are launched largest first,
+            // so that the in-order dispatch of CTAs to free SMs ends with the small ones.
+            const int64_t slots = 2 * (int64_t)sm_count(h->cfg.device);
+            std::vector<int> keys(B);
+            for (int b = 0; b < B; ++b) keys[b] = keys_of(lenh[b] + 1);
+            auto count = [&](int64_t r) {
+                int64_t c = 0;
+                for (int b = 0; b < B; ++b) c += (int64_t)Hkv * ((keys[b] + r - 1) / r);
+                return c;
+            };
+            int64_t R = std::max<int64_t>(1024, ((total_keys * Hkv + slots - 1) / slots + 63) / 64 * 64);
+            while (count(R) > slots && R < ((int64_t)max_t + 63) / 64 * 64) R += 64;
+            pieces.on = true;
+            std::vector<int> order(B);
+            for (int b = 0; b < B; ++b) {
+                int ns = (keys[b] + (int)R - 1) / (int)R;
+                pieces.rows[b] = ((keys[b] + ns - 1) / ns + 63) / 64 * 64;
+                order[b] = b;
+            }
+            std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pieces.rows[x] > pieces.rows[y]; });
+            pieces.start[0] = 0;
+            max_splits = 1;
+            for (int i = 0; i < B; ++i) {
+                const int b = order[i];
+                const int ns = (keys[b] + pieces.rows[b] - 1) / pieces.rows[b];
+                pieces.seq[i] = b;
+                pieces.start[i + 1] = pieces.start[i] + Hkv * ns;
+                max_splits = std::max(max_splits, ns);
+            }
+            split_rows = (int)R;
         } else {
             const int G = Hq / Hkv;
             const int64_t target = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(G) * 4;
@@ -798,7 +827,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
             split_rows = (int)r;
         }
-        max_splits = (max_t + split_rows - 1) / split_rows;
+        if (!pieces.on) max_splits = (max_t + split_rows - 1) / split_rows;
         if (dev_len) {
             // A device-length step keeps its grid for every later length (a captured
             // graph replays it) and each sequence takes max_splits splits of its own
@@ -845,6 +874,12 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         for (int b = 0; b < B && !dev_len; ++b) {
             dl.old_len[b] = lenh[b];
             dl.pos[b] = nexth[b];
+        }
+        dl.pieces = pieces.on;
+        if (pieces.on) {
+            memcpy(dl.item_start, pieces.start, (B + 1) * sizeof(int32_t));
+            memcpy(dl.seq_of, pieces.seq, B * sizeof(int32_t));
+            memcpy(dl.seq_rows, pieces.rows, B * sizeof(int32_t));
         }
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] {
             return tc_decode ? launch_decode_tc(dl, s) : launch_decode_bf16(dl, s);

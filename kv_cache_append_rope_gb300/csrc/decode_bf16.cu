@@ -495,6 +495,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
         rows = ((key_span(t, a.window) + a.max_splits - 1) / a.max_splits + KT - 1) / KT * KT;
     } else {
         t = (a.fused ? a.old_len[b] : a.len[b]) + 1;
+        if (a.pieces) rows = a.seq_rows[b];
     }
     if (!debug_check(t >= 1 && t <= a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
     const int ns = (key_span(t, a.window) + rows - 1) / rows;

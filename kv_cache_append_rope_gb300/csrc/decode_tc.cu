@@ -106,10 +106,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     Bars* bars = (Bars*)(smem + OFF_BAR);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int split = blockIdx.x;
-    const int lane_kv = blockIdx.y;
-    const int b = lane_kv / a.Hkv;
-    const int hkv = lane_kv - b * a.Hkv;
+    int split = blockIdx.x, b, hkv, split_rows = a.split_rows;
+    if (a.pieces) {
+        // the sequence whose CTA range holds this CTA, then its kv head and split
+        int lo_i = 0, hi_i = a.B;
+        while (hi_i - lo_i > 1) {
+            const int mid = (lo_i + hi_i) >> 1;
+            if (a.item_start[mid] <= (int)blockIdx.x) lo_i = mid;
+            else hi_i = mid;
+        }
+        b = a.seq_of[lo_i];
+        const int r = blockIdx.x - a.item_start[lo_i];
+        const int ns = (a.item_start[lo_i + 1] - a.item_start[lo_i]) / a.Hkv;
+        hkv = r / ns;
+        split = r - hkv * ns;
+        split_rows = a.seq_rows[b];
+    } else {
+        b = (int)blockIdx.y / a.Hkv;
+        hkv = (int)blockIdx.y - b * a.Hkv;
+    }
     const int G = a.Hq / a.Hkv;
     // everything below may read what the previous kernel of the stream wrote
     grid_dependency_wait();
@@ -123,11 +138,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     const int t = old_len + 1;
     const int lo = a.window > 0 ? max(0, t - a.window) : 0;
-    const int r0 = (lo & ~63) + split * a.split_rows;
+    const int r0 = (lo & ~63) + split * split_rows;
     if (r0 >= t) return;
-    const int r1 = min(t, r0 + a.split_rows);
+    const int r1 = min(t, r0 + split_rows);
     const int n = (r1 - r0 + BN - 1) / BN;                       // 128-key tiles
-    const int nsplit_lane = (key_span(t, a.window) + a.split_rows - 1) / a.split_rows;
+    const int nsplit_lane = (key_span(t, a.window) + split_rows - 1) / split_rows;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 2);
@@ -464,7 +479,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
     if (!a.fused || a.dev_len || a.kv.table || G <= 16 || G > 32) return cudaErrorInvalidValue;
     cudaLaunchAttribute attrs[1];
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(a.max_splits, a.B * a.Hkv);
+    cfg.gridDim = a.pieces ? dim3(a.item_start[a.B], 1) : dim3(a.max_splits, a.B * a.Hkv);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;

@@ -268,6 +268,15 @@ struct DecodeLaunch {
     int max_positions;
     int32_t old_len[kFusedMaxB];         // host mirrors: old length and RoPE position
     int32_t pos[kFusedMaxB];
+    // Piece list (tensor-core decode): blockIdx.x enumerates only CTAs with work, sequence
+    // by sequence in the order seq_of[0], seq_of[1], ... (largest pieces first, so that
+    // the in-order dispatch of CTAs to free SMs balances the load); sequence seq_of[i] owns
+    // CTAs item_start[i] .. item_start[i+1]-1: H_kv lanes x its own split count, each
+    // split seq_rows[b] key rows.
+    int pieces;
+    int32_t item_start[kFusedMaxB + 1];
+    int32_t seq_of[kFusedMaxB];
+    int32_t seq_rows[kFusedMaxB];
 };
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);

@@ -187,11 +187,15 @@ def test_bf16_without_rope_stores_inputs_unchanged():
 @pytest.mark.parametrize("Hkv,split_rows", [(8, 0), (2, 64), (1, 128)])
 def test_fused_and_separate_decode_steps_agree(Hkv, split_rows):
     """One launch per step (append + attend + merge + commit) against the separate
-    kernels: both match the oracle; stored rows, positions and lengths are identical."""
+    kernels of the same m16n8k16 decode kernel: both match the oracle; stored rows,
+    positions and lengths are identical.  (With 32 query heads per key/value head the
+    fused step otherwise runs on the tensor-core kernel, whose bf16 rounding points
+    differ: it is compared with the oracle and this path in its own test.)"""
     L0, steps = [1, 64, 257, 100], 3
     caches, outs = [], []
     for fused in (True, False):
-        cache, o, qkv = run_decode("bf16", 128, 32, Hkv, L0, steps, C=400, split_rows=split_rows, fused=fused)
+        cache, o, qkv = run_decode("bf16", 128, 32, Hkv, L0, steps, C=400, split_rows=split_rows, fused=fused,
+                                   tc=False)
         check_against_oracle("bf16", cache, o, qkv, L0, steps)
         caches.append(cache)
         outs.append(np.stack(o))
