@@ -478,11 +478,15 @@ typedef enum kvc_option {
                                       produce -- so that the debug build's device bounds checks can be
                                       seen to record KVC_ERR_DEVICE bit 32 and skip the access.  Reset
                                       the cache afterwards. */
-    KVC_OPT_DECODE_TC = 11         /* 1 (default) = decode steps with more than 16 (up to 32) query heads per
+    KVC_OPT_DECODE_TC = 11,        /* 1 (default) = decode steps with more than 16 (up to 32) query heads per
                                       key/value head run on the tensor-core decode kernel (tcgen05, the
                                       heads as rows of a 128-row query tile, S and O in tensor memory)
                                       when the step is fused, its lengths are host-held and the storage is
                                       contiguous; 0 = the m16n8k16 decode kernel for every group size */
+    KVC_OPT_DECODE_LANES = 12      /* 1 (default) = fused decode steps over many short lanes (every key span
+                                      at most 512 rows, at least four waves of lanes, at most 4 query heads
+                                      per key/value head) run with CTAs that walk several lanes each,
+                                      longest sequences first; 0 = one CTA per lane and split */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

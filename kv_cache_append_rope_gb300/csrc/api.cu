@@ -779,6 +779,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         int32_t seq[kFusedMaxB];
         int32_t rows[kFusedMaxB];
     } pieces;
+    int lanes_per_cta = 0;
     if (fast) {
         if (h->opt_split_rows > 0) {
             split_rows = (int)h->opt_split_rows;
@@ -828,6 +829,18 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             split_rows = (int)r;
         }
         if (!pieces.on) max_splits = (max_t + split_rows - 1) / split_rows;
+        // Short contexts with many lanes (at least four waves of one-split lanes, G <= 4):
+        // CTAs that walk several lanes each, longest sequences first (decode_lanes_kernel).
+        if (h->opt_decode_lanes && !tc_decode && h->opt_decode_fused && !dev_len && B <= kFusedMaxB &&
+            Hq / Hkv <= 4 && !h->opt_split_rows && max_t <= 512) {
+            const int64_t slots = (int64_t)sm_count(h->cfg.device) * decode_bf16_ctas_per_sm(Hq / Hkv);
+            const int64_t lanes = (int64_t)B * Hkv;
+            if (lanes >= 4 * slots) {
+                lanes_per_cta = (int)std::min<int64_t>(16, std::max<int64_t>(1, lanes / (2 * slots)));
+                split_rows = (max_t + 63) / 64 * 64;
+                max_splits = 1;
+            }
+        }
         if (dev_len) {
             // A device-length step keeps its grid for every later length (a captured
             // graph replays it) and each sequence takes max_splits splits of its own
@@ -876,13 +889,22 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             dl.pos[b] = nexth[b];
         }
         dl.pieces = pieces.on;
+        dl.lanes_per_cta = lanes_per_cta;
+        if (lanes_per_cta) {
+            // sequences longest first: the last CTAs to start are the shortest
+            std::vector<int> order(B);
+            for (int b = 0; b < B; ++b) order[b] = b;
+            std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return lenh[x] > lenh[y]; });
+            for (int i = 0; i < B; ++i) dl.seq_of[i] = order[i];
+        }
         if (pieces.on) {
             memcpy(dl.item_start, pieces.start, (B + 1) * sizeof(int32_t));
             memcpy(dl.seq_of, pieces.seq, B * sizeof(int32_t));
             memcpy(dl.seq_rows, pieces.rows, B * sizeof(int32_t));
         }
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] {
-            return tc_decode ? launch_decode_tc(dl, s) : launch_decode_bf16(dl, s);
+            return tc_decode ? launch_decode_tc(dl, s) : lanes_per_cta ? launch_decode_lanes(dl, s)
+                                                                       : launch_decode_bf16(dl, s);
         }));
         if (!dl.merge_in_kernel && max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
@@ -1755,6 +1777,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_DECODE_TC:
             h->opt_decode_tc = value != 0;
+            return KVC_OK;
+        case KVC_OPT_DECODE_LANES:
+            h->opt_decode_lanes = value != 0;
             return KVC_OK;
         case KVC_OPT_DEVICE_LENGTHS: {
             if (value && h->paged())

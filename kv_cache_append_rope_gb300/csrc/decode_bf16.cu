@@ -79,6 +79,109 @@ __device__ __forceinline__ void store_out(const DecodeLaunch& a, int64_t i, floa
         ((float*)a.out)[i] = x;
 }
 
+// One 64-key stage of a consumer warp: S = Q K^T for the warp's KW = 16 MT keys (key
+// key_base + j), masked outside [lo, r1); the online softmax of rows qa and qa + 8 of
+// its m tile; O += P V.  kt, vt: the stage's K and V tiles in shared memory.
+template <int MT>
+__device__ __forceinline__ void consume_stage(uint32_t kt, uint32_t vt, int key_base, int r1, int lo,
+                                              const uint32_t (&qf)[8][4], float (&o)[16][4], float (&m)[2],
+                                              float (&l)[2], int lane, int kofs) {
+    constexpr int KW = 16 * MT;              // keys per warp per stage
+    constexpr int NT = KW / 8;               // n8 tiles of S
+    constexpr int KS = KW / 16;              // k16 steps of P V
+    const int qc = (lane & 3) * 2;           // fragment column pair
+    // ---- S = Q K^T for this warp's KW keys
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+    // (k-outer: the NT accumulators are independent chains, so consecutive MMAs
+    // do not wait on one another)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int dim0 = kk * 32 + (lane >> 3) * 8;
+        uint32_t bk[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = kofs + nt * 8 + (lane & 7);
+            const uint32_t addr = kt + (dim0 >> 6) * HALF_BYTES + swz128(row, (dim0 & 63) >> 3);
+            ldsm_x4(addr, bk[nt][0], bk[nt][1], bk[nt][2], bk[nt][3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk], bk[nt][0], bk[nt][1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk + 1], bk[nt][2], bk[nt][3]);
+    }
+    // ---- mask keys beyond this split
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int key = key_base + nt * 8 + qc + e;
+            if (key >= r1 || key < lo) {
+                sc[nt][e] = -INFINITY;
+                sc[nt][2 + e] = -INFINITY;
+            }
+        }
+    // ---- online softmax (rows qa and qa + 8 of this m tile)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * rr], sc[nt][2 * rr + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // The reference maximum moves only when a score passes it by more than 2^8
+        // (log2 units): exponentials up to 2^8 are exact enough in float32 and bf16,
+        // and the final division by the running sum cancels the reference, so a
+        // stale one changes nothing but rounding.  O is rescaled only then (a
+        // warp-wide decision: rows that did not move are multiplied by 1).
+        const bool grow = mx > m[rr] + 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? fmaxf(m[rr], mx) : m[rr];
+            const float corr = grow && m[rr] > -INFINITY ? fast_exp2(m[rr] - m_new) : 1.f;
+            m[rr] = m_new;
+            l[rr] *= corr;
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                o[n][2 * rr] *= corr;
+                o[n][2 * rr + 1] *= corr;
+            }
+        }
+        const float m_use = m[rr] == -INFINITY ? 0.f : m[rr];
+        float ps = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float p = fast_exp2(sc[nt][2 * rr + e] - m_use);
+                sc[nt][2 * rr + e] = p;
+                ps += p;
+            }
+        l[rr] += ps;
+    }
+    // ---- O += P V (V^T fragments through transposing ldmatrix)
+#pragma unroll
+    for (int k2 = 0; k2 < KS; ++k2) {
+        uint32_t pf[4];
+        pf[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
+        pf[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
+        pf[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
+        pf[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+        const int vrow = kofs + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            const int dim = np * 16 + (lane >> 4) * 8;
+            const uint32_t addr = vt + (dim >> 6) * HALF_BYTES + swz128(vrow, (dim & 63) >> 3);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(addr, b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * np], pf, b0, b1);
+            mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
+        }
+    }
+}
+
 // MODE 0: separate-kernel step; 1: fused step, lengths from the host mirrors;
 // 2: fused step, lengths from device memory.
 template <int MT, int MODE>
@@ -301,96 +404,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const uint32_t vt = kt + TILE_BYTES;
             const int key_base = r0 + i * KT + kofs;
 
-            // ---- S = Q K^T for this warp's KW keys
-            float sc[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-            // (k-outer: the NT accumulators are independent chains, so consecutive MMAs
-            // do not wait on one another)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const int dim0 = kk * 32 + (lane >> 3) * 8;
-                uint32_t bk[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int row = kofs + nt * 8 + (lane & 7);
-                    const uint32_t addr = kt + (dim0 >> 6) * HALF_BYTES + swz128(row, (dim0 & 63) >> 3);
-                    ldsm_x4(addr, bk[nt][0], bk[nt][1], bk[nt][2], bk[nt][3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk], bk[nt][0], bk[nt][1]);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], qf[2 * kk + 1], bk[nt][2], bk[nt][3]);
-            }
-            // ---- mask keys beyond this split
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = key_base + nt * 8 + qc + e;
-                    if (key >= r1 || key < lo) {
-                        sc[nt][e] = -INFINITY;
-                        sc[nt][2 + e] = -INFINITY;
-                    }
-                }
-            // ---- online softmax (rows qa and qa + 8 of this m tile)
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * rr], sc[nt][2 * rr + 1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                // The reference maximum moves only when a score passes it by more than 2^8
-                // (log2 units): exponentials up to 2^8 are exact enough in float32 and bf16,
-                // and the final division by the running sum cancels the reference, so a
-                // stale one changes nothing but rounding.  O is rescaled only then (a
-                // warp-wide decision: rows that did not move are multiplied by 1).
-                const bool grow = mx > m[rr] + 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float m_new = grow ? fmaxf(m[rr], mx) : m[rr];
-                    const float corr = grow && m[rr] > -INFINITY ? fast_exp2(m[rr] - m_new) : 1.f;
-                    m[rr] = m_new;
-                    l[rr] *= corr;
-#pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        o[n][2 * rr] *= corr;
-                        o[n][2 * rr + 1] *= corr;
-                    }
-                }
-                const float m_use = m[rr] == -INFINITY ? 0.f : m[rr];
-                float ps = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float p = fast_exp2(sc[nt][2 * rr + e] - m_use);
-                        sc[nt][2 * rr + e] = p;
-                        ps += p;
-                    }
-                l[rr] += ps;
-            }
-            // ---- O += P V (V^T fragments through transposing ldmatrix)
-#pragma unroll
-            for (int k2 = 0; k2 < KS; ++k2) {
-                uint32_t pf[4];
-                pf[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
-                pf[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
-                pf[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
-                pf[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
-                const int vrow = kofs + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-#pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    const int dim = np * 16 + (lane >> 4) * 8;
-                    const uint32_t addr = vt + (dim >> 6) * HALF_BYTES + swz128(vrow, (dim & 63) >> 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * np], pf, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
-                }
-            }
+            consume_stage<MT>(kt, vt, key_base, r1, lo, qf, o, m, l, lane, kofs);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
@@ -513,6 +527,214 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     store_out(a, (int64_t)qh * D + threadIdx.x, O / L);
 }
 
+// ---- many short lanes per CTA ---------------------------------------------------
+//
+// Fused decode step for short contexts (every lane one split) with G <= 4 query heads
+// per key/value head: a CTA walks lanes_per_cta lanes in turn -- sequences in the order
+// seq_of[] (longest first), their key/value heads in order -- through one continuous
+// ring of stages, so that the producer loads the next lane's tiles while the consumers
+// finish the current one and the per-CTA set-up (barriers, pipeline fill) is paid once
+// for all of them.  Per lane it does exactly what the fused step does for a lane with
+// one split: the new key (bit-exact rotation) and value rows and the position are stored
+// before the lane's loads, the consumer warps process its 64-key stages
+// (consume_stage), merge through a small shared-memory buffer behind a barrier of the
+// four consumer warps only, and write the normalised output; the CTA of a sequence's
+// key/value head 0 commits its length.
+constexpr int kLanesMaxG = 4;
+constexpr int kLanesMergeBytes = NCW * kLanesMaxG * D * 4 + NCW * kLanesMaxG * 8;
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(THREADS, Cfg<1>::MINB)
+decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ DecodeLaunch a) {
+    constexpr int STAGES = Cfg<1>::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    volatile int* s_err = (volatile int*)(empty + STAGES);
+    float* Om = (float*)(smem + STAGES * STAGE_BYTES + 256);                 // [NCW][4][D]
+    float2* ML = (float2*)(smem + STAGES * STAGE_BYTES + 256 + NCW * kLanesMaxG * D * 4);  // [NCW][4]
+    grid_dependency_wait();
+    launch_dependents();
+    const int G = a.Hq / a.Hkv;
+    const int nlanes = a.B * a.Hkv;
+    const int l_begin = blockIdx.x * a.lanes_per_cta;
+    const int l_end = min(nlanes, l_begin + a.lanes_per_cta);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), NCW);
+        }
+        *s_err = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // lane li: the (li / H_kv)-th sequence of seq_of, key/value head li % H_kv
+    auto lane_of = [&](int li, int& b, int& hkv) {
+        b = a.seq_of[li / a.Hkv];
+        hkv = li % a.Hkv;
+    };
+    int issued = 0;
+    if (warp == NCW) {
+        // ---------------- producer ----------------
+        int gi = 0;
+        for (int li = l_begin; li < l_end && !*s_err; ++li) {
+            int b, hkv;
+            lane_of(li, b, hkv);
+            const int old_len = a.old_len[b], pos = a.pos[b];
+            if (!debug_check(old_len >= 0 && old_len < a.C, lane == 0 ? a.err : nullptr)) continue;
+            const int t = old_len + 1;
+            const int lo = a.window > 0 ? max(0, t - a.window) : 0;
+            const int r0 = lo & ~(KT - 1);
+            const int ntiles = (t - r0 + KT - 1) / KT;
+            // the new row (slot old_len), then its TMA reads: generic-proxy writes first
+            {
+                const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
+                const bool slot_ok = debug_check(kv_slot_ok(a.kv, b, old_len), lane == 0 ? a.err : nullptr);
+                const int64_t dst = slot_ok ? kv_row(a.kv, b, hkv, old_len) * D + lane * 4 : 0;
+                const uint2 kraw = *(const uint2*)(a.k_in + src);
+                const uint2 vraw = *(const uint2*)(a.v_in + src);
+                const __nv_bfloat16* kin = (const __nv_bfloat16*)&kraw;
+                __nv_bfloat16 kout[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float xf = __bfloat162float(kin[2 * e]), yf = __bfloat162float(kin[2 * e + 1]);
+                    if (a.rope_f) {
+                        const int j = lane * 2 + e;
+                        const float2 cs = a.rope_f[(int64_t)pos * (D / 2) + j];
+                        kout[2 * e] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, false);
+                        kout[2 * e + 1] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, true);
+                    } else {
+                        kout[2 * e] = kin[2 * e];
+                        kout[2 * e + 1] = kin[2 * e + 1];
+                    }
+                }
+                if (slot_ok) {
+                    *(uint2*)(a.K + dst) = *(const uint2*)kout;
+                    *(uint2*)(a.V + dst) = vraw;
+                    if (hkv == 0 && lane == 0) a.positions[(int64_t)b * a.C + old_len] = pos;
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+            }
+            if (lane == 0 && !a.test_stall) {
+                for (int i = 0; i < ntiles; ++i, ++gi) {
+                    const int s = gi % STAGES;
+                    if (gi >= STAGES && !mbar_wait_bounded(smem_u32(&empty[s]), ((gi / STAGES) - 1) & 1)) {
+                        *s_err = 1;
+                        atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+                        break;
+                    }
+                    const int y = (int)kv_row(a.kv, b, hkv, r0 + i * KT);
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    uint8_t* st = smem + s * STAGE_BYTES;
+                    tma_load_2d(smem_u32(st), &tmK, 0, y, fb);
+                    tma_load_2d(smem_u32(st + HALF_BYTES), &tmK, 64, y, fb);
+                    tma_load_2d(smem_u32(st + TILE_BYTES), &tmV, 0, y, fb);
+                    tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES), &tmV, 64, y, fb);
+                    issued = gi + 1;
+                }
+            }
+            gi = __shfl_sync(0xffffffffu, gi, 0);
+        }
+    } else {
+        // ---------------- consumers (one 16-row m tile, 16 keys of each stage per warp) ----------------
+        const int kofs = warp * 16;
+        const int qa = lane >> 2, qc = (lane & 3) * 2;
+        const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+        int gi = 0;
+        for (int li = l_begin; li < l_end; ++li) {
+            int b, hkv;
+            lane_of(li, b, hkv);
+            const int old_len = a.old_len[b], pos = a.pos[b];
+            if (!(old_len >= 0 && old_len < a.C) && kDebug) continue;
+            const int t = old_len + 1;
+            const int lo = a.window > 0 ? max(0, t - a.window) : 0;
+            const int r0 = lo & ~(KT - 1);
+            const int ntiles = (t - r0 + KT - 1) / KT;
+            uint32_t qf[8][4];
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int c = ks * 16 + qc;
+                const float2 z = make_float2(0.f, 0.f);
+                const int qh = hkv * G;
+                const float2 x0 = qa < G ? fused_q_pair(a, b, qh + qa, c, pos) : z;
+                const float2 x2 = qa < G ? fused_q_pair(a, b, qh + qa, c + 8, pos) : z;
+                qf[ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
+                qf[ks][1] = 0u;                              // rows 8 .. 15: beyond G <= 4
+                qf[ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
+                qf[ks][3] = 0u;
+            }
+            float o[16][4];
+            float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i, ++gi) {
+                const int s = gi % STAGES;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (gi / STAGES) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kt = smem_u32(smem + s * STAGE_BYTES);
+                consume_stage<1>(kt, kt + TILE_BYTES, r0 + i * KT + kofs, t, lo, qf, o, m, l, lane, kofs);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            }
+            if (!ok) {
+                *s_err = 1;
+                atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+            }
+            // merge the four consumer warps (rows < G), behind the consumers' own barrier
+            consumer_bar();
+            if (*s_err) break;
+            float lr = l[0];
+            lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+            lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+            if (qa < G) {
+                float* dst = Om + ((size_t)warp * kLanesMaxG + qa) * D;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) *(float2*)(dst + n * 8 + qc) = make_float2(o[n][0], o[n][1]);
+                if ((lane & 3) == 0) ML[warp * kLanesMaxG + qa] = make_float2(m[0], lr);
+            }
+            consumer_bar();
+            for (int u = threadIdx.x; u < G * D; u += NCW * 32) {
+                const int g = u / D, dim = u - g * D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, ML[w * kLanesMaxG + g].x);
+                float O = 0.f, L = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) {
+                    const float2 ml = ML[w * kLanesMaxG + g];
+                    const float f = fast_exp2(ml.x - M);
+                    O += Om[((size_t)w * kLanesMaxG + g) * D + dim] * f;
+                    L += ml.y * f;
+                }
+                store_out(a, ((int64_t)b * a.Hq + hkv * G + g) * D + dim, O / L);
+            }
+            if (threadIdx.x == 0 && hkv == 0 && !a.no_commit) {
+                a.len_out[b] = old_len + 1;
+                a.next_out[b] = pos + 1;
+            }
+            consumer_bar();                          // the buffer is free for the next lane
+        }
+    }
+    __syncthreads();
+    if (*s_err && warp == NCW && lane == 0) {
+        // let copies already issued land before the CTA's shared memory is released
+        for (int i = issued - STAGES < 0 ? 0 : issued - STAGES; i < issued; ++i)
+            mbar_wait_bounded(smem_u32(&full[i % STAGES]), (i / STAGES) & 1);
+    }
+}
+
 // Launch attributes: programmatic stream serialization when a.pdl is set.
 struct PdlConfig {
     cudaLaunchAttribute attr[1];
@@ -550,6 +772,19 @@ cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s) {
 }
 
 int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg<2>::MINB; }
+
+cudaError_t launch_decode_lanes(const DecodeLaunch& a, cudaStream_t s) {
+    constexpr int SMEM = smem_bytes<Cfg<1>::STAGES>() + kLanesMergeBytes;
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run(
+        [] { return cudaFuncSetAttribute(decode_lanes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM); });
+    if (e != cudaSuccess) return e;
+    if (!a.fused || a.dev_len || a.Hq / a.Hkv > kLanesMaxG || a.lanes_per_cta < 1 || a.B > kFusedMaxB)
+        return cudaErrorInvalidValue;
+    const int ctas = (a.B * a.Hkv + a.lanes_per_cta - 1) / a.lanes_per_cta;
+    PdlConfig pc(dim3(ctas), dim3(THREADS), SMEM, s, a.pdl != 0);
+    return cudaLaunchKernelEx(&pc.cfg, decode_lanes_kernel, *a.tmK, *a.tmV, a);
+}
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;

@@ -148,6 +148,7 @@ struct Handle {
     int64_t opt_device_lengths = 0;
     int64_t opt_decode_pdl = 1;
     int64_t opt_decode_tc = 1;
+    int64_t opt_decode_lanes = 1;
     std::vector<uint64_t> layer_version;  // [L] bumped by every change of a layer's state or staged slot
     bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 
@@ -274,12 +275,16 @@ struct DecodeLaunch {
     // CTAs item_start[i] .. item_start[i+1]-1: H_kv lanes x its own split count, each
     // split seq_rows[b] key rows.
     int pieces;
+    int lanes_per_cta;                   // many-lane short-context step: lanes each CTA walks
     int32_t item_start[kFusedMaxB + 1];
     int32_t seq_of[kFusedMaxB];
     int32_t seq_rows[kFusedMaxB];
 };
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);
+// Fused step with many short lanes per CTA (every lane one split, H_q / H_kv <= 4); lanes
+// in the order of seq_of (sequences) x key/value heads.
+cudaError_t launch_decode_lanes(const DecodeLaunch& a, cudaStream_t s);
 // Tensor-core decode (fused step, contiguous storage, 16 < H_q / H_kv <= 32); one CTA per SM.
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 int decode_bf16_ctas_per_sm(int group);

@@ -20,7 +20,7 @@ BASE = 10000.0
 
 
 def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0, fused=True, tc=True,
-               window=0, out_dtype=None):
+               window=0, out_dtype=None, lanes=True, block_rows=0):
     """Prefill ragged prefixes, run `steps` decode steps; return (cache, outs, inputs)."""
     need_gpu()
     B = len(L0)
@@ -30,9 +30,11 @@ def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, see
     v = W.normal_np((B, Hkv, T, D), seed + 2)
     qd, kd, vd = (device_tensor(x, dtype) for x in (q, k, v))
     q, k, v = to_np(qd), to_np(kd), to_np(vd)        # the exact values the GPU sees
-    cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE, window=window)
+    cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype=dtype, rope_base=BASE, window=window, block_rows=block_rows)
     if not tc:
         cache.set_option(L.OPT_DECODE_TC, 0)
+    if not lanes:
+        cache.set_option(L.OPT_DECODE_LANES, 0)
     if generic:
         cache.set_option(L.OPT_FORCE_GENERIC, 1)
     if split_rows:
@@ -110,6 +112,43 @@ def test_tensor_core_decode_matches_oracle_and_the_mma_sync_path(Hq, Hkv, split_
     _, o16, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=800, split_rows=split_rows, window=window,
                            out_dtype=torch.bfloat16)
     np.testing.assert_array_equal(np.stack(o16), to_np(torch.from_numpy(np.stack(outs)).to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("Hq,Hkv,window,block_rows,out_bf16", [
+    (32, 32, 0, 0, False), (32, 8, 0, 0, False), (32, 32, 100, 0, False), (32, 32, 0, 64, False),
+    (32, 32, 0, 0, True),
+])
+def test_many_short_lanes_per_cta_match_oracle(Hq, Hkv, window, block_rows, out_bf16):
+    """Short ragged contexts with many lanes run on CTAs that walk several lanes each
+    (KVC_OPT_DECODE_LANES): every sampled sequence against the oracle, stored rows bit
+    for bit, and the outputs against the one-CTA-per-lane path."""
+    B = 48 if Hkv == 32 else 160                     # at least four waves of lanes
+    L0 = np.random.default_rng(B + Hkv).integers(0, 301, size=B).tolist()
+    L0[0], L0[1] = 0, 300
+    steps = 3
+    od = torch.bfloat16 if out_bf16 else None
+    cache, outs, qkv = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=320, window=window, block_rows=block_rows,
+                                  out_dtype=od, seed=7)
+    q, k, v = qkv
+    Ks, Vs, Ps = storage_np(cache)
+    got = np.stack(outs)
+    for b in sorted(set([0, 1] + list(range(2, B, max(1, B // 10))))):
+        n = L0[b] + steps
+        ref = A.decode_steps_reference(np.transpose(q[b, :, L0[b]:n], (1, 0, 2)), k[b, :, :n], v[b, :, :n],
+                                       L0[b], BASE, "bf16", window=window)
+        if out_bf16:
+            assert np.abs(got[:, b, :, 0] - ref).max() <= TOL["bf16"]
+        else:
+            assert_close(got[:, b, :, 0], ref, "bf16", b)
+        K, V = A.stored_rows(k[b, :, :n], v[b, :, :n], np.arange(n)[None], BASE, "bf16")
+        np.testing.assert_array_equal(Ks[b, :, :n], K)
+        np.testing.assert_array_equal(Vs[b, :, :n], V)
+        assert Ps[b, :n].tolist() == list(range(n))
+    assert cache.get_lengths(0)[0] == [l + steps for l in L0]
+    cache.check()
+    _, ref_outs, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=320, window=window, block_rows=block_rows,
+                                out_dtype=od, seed=7, lanes=False)
+    assert np.abs(got - np.stack(ref_outs)).max() < 1e-2
 
 
 def test_split_sizes_agree():
