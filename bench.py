@@ -62,7 +62,8 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 TRAFFIC = {
     "mha_decode": ("ratio", 1.013),
     "gqa_decode": ("ratio", 1.0067),
-    "mqa_decode": ("ratio", 1.0106),
+    "mqa_decode": ("ratio", 1.0204),
+    "mha_decode_short": ("ratio", 1.073),
     "suffix": ("per_sequence", 375401472.0 + 174217472.0),
 }
 
@@ -316,6 +317,16 @@ class DecodeBench:
 
     def dominant(self):
         return "decode"
+
+    def kernel_name(self):
+        """The decode kernel the library picks for this workload's fused steps."""
+        c = self.cfg
+        G = c["Hq"] // c["Hkv"]
+        if 16 < G <= 32 and not self.block_rows and self.graph is None:
+            return "decode_tc_kernel"
+        if G <= 4 and c["B"] * c["Hkv"] >= 4 * 2 * 152 and c["hi"] + c["steps"] <= 512 and self.graph is None:
+            return "decode_lanes_kernel"
+        return "decode_bf16_kernel"
 
     def dominant_algorithmic(self, launches):
         """Algorithmic bytes of `launches` decode-kernel launches (cycling through the 64 steps)."""
@@ -602,7 +613,7 @@ def run_ours(args, name, world, rank, local, workers=None):
         achieved = alg / 1e9 / (dom_ms / 1e3)
         achieved_step = alg_step / 1e9 / (per_step_ms / 1e3)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": "decode_bf16_kernel",
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": bench.kernel_name(),
                 "peak_source": f"{peak_kind} hbm_gbs (a device copy's read + write rate, not a datasheet peak)",
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
                 "kernel_ms_per_launch": round(dom_ms / dom_launches, 5),

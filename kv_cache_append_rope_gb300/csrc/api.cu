@@ -511,13 +511,17 @@ kvc_status kvc_create_ex(const kvc_config* config, kvc_handle** out) {
         h->tmap_v.resize(c.layers);
         h->tmap_k128.resize(c.layers);
         h->tmap_v128.resize(c.layers);
+        h->tmap_k16.resize(c.layers);
+        h->tmap_v16.resize(c.layers);
         bool all = true;
         const uint64_t rows = store_rows;
         for (int l = 0; l < c.layers && all; ++l)
             all = encode_rows_map(&h->tmap_k[l], h->K_layer(l), rows, 64) &&
                   encode_rows_map(&h->tmap_v[l], h->V_layer(l), rows, 64) &&
                   encode_rows_map(&h->tmap_k128[l], h->K_layer(l), rows, 128) &&
-                  encode_rows_map(&h->tmap_v128[l], h->V_layer(l), rows, 128);
+                  encode_rows_map(&h->tmap_v128[l], h->V_layer(l), rows, 128) &&
+                  encode_rows_map(&h->tmap_k16[l], h->K_layer(l), rows, 16) &&
+                  encode_rows_map(&h->tmap_v16[l], h->V_layer(l), rows, 16);
         h->have_tmaps = all;
     }
     h->len_h.assign(LB, 0);
@@ -801,7 +805,9 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             std::vector<int> order(B);
             for (int b = 0; b < B; ++b) {
                 int ns = (keys[b] + (int)R - 1) / (int)R;
-                pieces.rows[b] = ((keys[b] + ns - 1) / ns + 63) / 64 * 64;
+                // whole 128-key tiles (the kernel's tile), so only a lane's last piece ends
+                // inside a tile
+                pieces.rows[b] = ((keys[b] + ns - 1) / ns + 127) / 128 * 128;
                 order[b] = b;
             }
             std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pieces.rows[x] > pieces.rows[y]; });
@@ -864,6 +870,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         DecodeLaunch dl{};
         dl.tmK = &h->tmap_k[layer]; dl.tmV = &h->tmap_v[layer];
         dl.tmK128 = &h->tmap_k128[layer]; dl.tmV128 = &h->tmap_v128[layer];
+        dl.tmK16 = &h->tmap_k16[layer]; dl.tmV16 = &h->tmap_v16[layer];
         dl.part_o = h->part_o; dl.part_ml = h->part_ml; dl.out = out->data; dl.err = h->err_d;
         dl.B = B; dl.Hq = Hq; dl.Hkv = Hkv; dl.C = C; dl.split_rows = split_rows; dl.max_splits = max_splits;
         dl.out_bf16 = out_bf16;

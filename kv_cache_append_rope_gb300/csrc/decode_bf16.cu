@@ -536,8 +536,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
 // finish the current one and the per-CTA set-up (barriers, pipeline fill) is paid once
 // for all of them.  Per lane it does exactly what the fused step does for a lane with
 // one split: the new key (bit-exact rotation) and value rows and the position are stored
-// before the lane's loads, the consumer warps process its 64-key stages
-// (consume_stage), merge through a small shared-memory buffer behind a barrier of the
+// before the lane's loads (a lane's last, partial tile loads only its 16-row boxes that
+// hold keys), the consumer warps process its 64-key stages (consume_stage), merge through a small shared-memory buffer behind a barrier of the
 // four consumer warps only, and write the normalised output; the CTA of a sequence's
 // key/value head 0 commits its length.
 constexpr int kLanesMaxG = 4;
@@ -547,6 +547,7 @@ __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;"
 
 __global__ void __launch_bounds__(THREADS, Cfg<1>::MINB)
 decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
                     const __grid_constant__ DecodeLaunch a) {
     constexpr int STAGES = Cfg<1>::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -622,6 +623,8 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 __syncwarp();
             }
             if (lane == 0 && !a.test_stall) {
+                prefetch_tmap(&tmK16);
+                prefetch_tmap(&tmV16);
                 for (int i = 0; i < ntiles; ++i, ++gi) {
                     const int s = gi % STAGES;
                     if (gi >= STAGES && !mbar_wait_bounded(smem_u32(&empty[s]), ((gi / STAGES) - 1) & 1)) {
@@ -631,12 +634,36 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     }
                     const int y = (int)kv_row(a.kv, b, hkv, r0 + i * KT);
                     const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     uint8_t* st = smem + s * STAGE_BYTES;
-                    tma_load_2d(smem_u32(st), &tmK, 0, y, fb);
-                    tma_load_2d(smem_u32(st + HALF_BYTES), &tmK, 64, y, fb);
-                    tma_load_2d(smem_u32(st + TILE_BYTES), &tmV, 0, y, fb);
-                    tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES), &tmV, 64, y, fb);
+                    const int rows = min(KT, t - (r0 + i * KT));
+                    if (rows == KT) {
+                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        tma_load_2d(smem_u32(st), &tmK, 0, y, fb);
+                        tma_load_2d(smem_u32(st + HALF_BYTES), &tmK, 64, y, fb);
+                        tma_load_2d(smem_u32(st + TILE_BYTES), &tmV, 0, y, fb);
+                        tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES), &tmV, 64, y, fb);
+                    } else {
+                        // the lane's last, partial tile: only its 16-row boxes that hold keys
+                        // (a 16-row box at a 2 KB offset keeps the tile's 128-byte swizzle
+                        // phase).  The value rows beyond them are zero-filled by boxes that lie
+                        // wholly outside the tensor (row -16): masked keys get probability 0,
+                        // and 0 times whatever the shared memory held before could be NaN.
+                        // (Key rows there are masked after the product, so they stay as they are.)
+                        const int nb = (rows + 15) / 16;
+                        mbar_arrive_expect_tx(fb, (uint32_t)(nb * 4 + (4 - nb) * 2) * 16 * 128);
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t o = q * 16 * 128;
+                            if (q < nb) {
+                                tma_load_2d(smem_u32(st) + o, &tmK16, 0, y + 16 * q, fb);
+                                tma_load_2d(smem_u32(st + HALF_BYTES) + o, &tmK16, 64, y + 16 * q, fb);
+                                tma_load_2d(smem_u32(st + TILE_BYTES) + o, &tmV16, 0, y + 16 * q, fb);
+                                tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES) + o, &tmV16, 64, y + 16 * q, fb);
+                            } else {
+                                tma_load_2d(smem_u32(st + TILE_BYTES) + o, &tmV16, 0, -16, fb);
+                                tma_load_2d(smem_u32(st + TILE_BYTES + HALF_BYTES) + o, &tmV16, 64, -16, fb);
+                            }
+                        }
+                    }
                     issued = gi + 1;
                 }
             }
@@ -783,7 +810,7 @@ cudaError_t launch_decode_lanes(const DecodeLaunch& a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const int ctas = (a.B * a.Hkv + a.lanes_per_cta - 1) / a.lanes_per_cta;
     PdlConfig pc(dim3(ctas), dim3(THREADS), SMEM, s, a.pdl != 0);
-    return cudaLaunchKernelEx(&pc.cfg, decode_lanes_kernel, *a.tmK, *a.tmV, a);
+    return cudaLaunchKernelEx(&pc.cfg, decode_lanes_kernel, *a.tmK, *a.tmV, *a.tmK16, *a.tmV16, a);
 }
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, cudaStream_t s) {

@@ -125,6 +125,7 @@ struct Handle {
     // TMA descriptors over each layer's keys and values (bf16, d_h = 128):
     // 64-row boxes for decode, 128-row boxes for the suffix-chunk kernel
     std::vector<CUtensorMap> tmap_k, tmap_v, tmap_k128, tmap_v128;
+    std::vector<CUtensorMap> tmap_k16, tmap_v16;   // 16-row boxes: the partial last tile of a short lane
     bool have_tmaps = false;
 
     ArgRing ring;
@@ -237,6 +238,7 @@ constexpr int kFusedMaxB = 256;   // sequences whose lengths travel as kernel pa
 struct DecodeLaunch {
     const CUtensorMap* tmK; const CUtensorMap* tmV;       // 64-row boxes
     const CUtensorMap* tmK128; const CUtensorMap* tmV128; // 128-row boxes (tensor-core decode)
+    const CUtensorMap* tmK16; const CUtensorMap* tmV16;   // 16-row boxes (short lanes' last tiles)
     const float* qrot;       // [B,H_q,128] rotated queries (separate-kernel step)
     const int32_t* len;      // [B] old length: t = len + 1 (separate-kernel step)
     float* part_o; float2* part_ml;
