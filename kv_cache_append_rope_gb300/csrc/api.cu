@@ -1279,12 +1279,13 @@ int64_t first_nonfinite_host(const void* p, int64_t n, int dtype) {
     return -1;
 }
 
-// Rows 0 .. n-1 of every head of sequences [b0, b1) of a [B, H, S, d] tensor: one strided
-// copy per sequence (H runs of n rows, S rows apart).
-cudaError_t copy_rows(char* dst, const char* src, int b0, int b1, const int32_t* n, int H, int S, size_t row_bytes,
-                      cudaMemcpyKind kind, cudaStream_t st) {
+// Rows 0 .. n-1 of every head of the sequences seqs[0 .. count) of a [B, H, S, d] tensor:
+// one strided copy per sequence (H runs of n rows, S rows apart).
+cudaError_t copy_rows(char* dst, const char* src, const int* seqs, int count, const int32_t* n, int H, int S,
+                      size_t row_bytes, cudaMemcpyKind kind, cudaStream_t st) {
     const size_t pitch = (size_t)S * row_bytes;
-    for (int b = b0; b < b1; ++b) {
+    for (int i = 0; i < count; ++i) {
+        const int b = seqs[i];
         if (n[b] == 0) continue;
         const size_t off = (size_t)b * H * pitch;
         cudaError_t e = cudaMemcpy2DAsync(dst + off, pitch, src + off, pitch, (size_t)n[b] * row_bytes, (size_t)H,
@@ -1386,6 +1387,20 @@ kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tenso
     }
     const int cs = chunk_sequences > 0 ? std::min(chunk_sequences, B) : std::max(1, (B + 7) / 8);
     const int nchunks = (B + cs - 1) / cs;
+    // Stage order: the pipeline waits for the first stage's upload before any work and for
+    // the last stage's download after all of it, so the smallest sequence goes first, the
+    // second smallest last, and the others largest first in between (the results do not
+    // depend on the order: sequences are independent).
+    std::vector<int> order(B);
+    for (int b = 0; b < B; ++b) order[b] = b;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return sl[x] < sl[y]; });
+    if (B > 2) {
+        std::vector<int> o2;
+        o2.push_back(order[0]);
+        for (int i = B - 1; i >= 2; --i) o2.push_back(order[i]);
+        o2.push_back(order[1]);
+        order.swap(o2);
+    }
     while ((int)h->io_ev.size() < 2 * nchunks) {
         cudaEvent_t e;
         KVC_CUDA(h, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
@@ -1402,14 +1417,14 @@ kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tenso
     KVC_CUDA(h, cudaStreamWaitEvent(h->io_h2d, h->io_last, 0));
     // 1. every chunk's inputs, in chunk order, on the upload stream
     for (int c = 0; c < nchunks; ++c) {
-        const int b0 = c * cs, b1 = std::min(B, b0 + cs);
+        const int i0 = c * cs, i1 = std::min(B, i0 + cs);
         if (need_q)
-            KVC_CUDA(h, copy_rows(dq, (const char*)q->data, b0, b1, sl.data(), Hq, S, row_bytes,
+            KVC_CUDA(h, copy_rows(dq, (const char*)q->data, order.data() + i0, i1 - i0, sl.data(), Hq, S, row_bytes,
                                   cudaMemcpyHostToDevice, h->io_h2d));
-        KVC_CUDA(h, copy_rows(dk, (const char*)k->data, b0, b1, sl.data(), Hkv, S, row_bytes, cudaMemcpyHostToDevice,
-                              h->io_h2d));
-        KVC_CUDA(h, copy_rows(dv, (const char*)v->data, b0, b1, sl.data(), Hkv, S, row_bytes, cudaMemcpyHostToDevice,
-                              h->io_h2d));
+        KVC_CUDA(h, copy_rows(dk, (const char*)k->data, order.data() + i0, i1 - i0, sl.data(), Hkv, S, row_bytes,
+                              cudaMemcpyHostToDevice, h->io_h2d));
+        KVC_CUDA(h, copy_rows(dv, (const char*)v->data, order.data() + i0, i1 - i0, sl.data(), Hkv, S, row_bytes,
+                              cudaMemcpyHostToDevice, h->io_h2d));
         KVC_CUDA(h, cudaEventRecord(h->io_ev[2 * c], h->io_h2d));
     }
     // 2. each chunk's append and attention on the caller's stream once its inputs have
@@ -1420,11 +1435,14 @@ kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tenso
     tv = *v; tv.data = dv;
     if (out) { to = *out; to.data = dout; }
     std::vector<int32_t> sl_c(B), sp_c(B);
+    std::vector<char> in_stage(B);
     for (int c = 0; c < nchunks; ++c) {
-        const int b0 = c * cs, b1 = std::min(B, b0 + cs);
+        const int i0 = c * cs, i1 = std::min(B, i0 + cs);
+        std::fill(in_stage.begin(), in_stage.end(), 0);
+        for (int i = i0; i < i1; ++i) in_stage[order[i]] = 1;
         int rows = 0;
         for (int b = 0; b < B; ++b) {
-            const bool in = b >= b0 && b < b1;
+            const bool in = in_stage[b] != 0;
             sl_c[b] = in ? sl[b] : 0;
             sp_c[b] = in ? sp[b] : h->next_h[(size_t)layer * B + b];
             rows += sl_c[b];
@@ -1441,8 +1459,8 @@ kvc_status kvc_prefill_suffix_host(kvc_handle* h, int32_t layer, const kvc_tenso
         if (out) {
             KVC_CUDA(h, cudaEventRecord(h->io_ev[2 * c + 1], s));
             KVC_CUDA(h, cudaStreamWaitEvent(h->io_d2h, h->io_ev[2 * c + 1], 0));
-            KVC_CUDA(h, copy_rows((char*)out->data, dout, b0, b1, sl.data(), Hq, S, (size_t)D * osz,
-                                  cudaMemcpyDeviceToHost, h->io_d2h));
+            KVC_CUDA(h, copy_rows((char*)out->data, dout, order.data() + i0, i1 - i0, sl.data(), Hq, S,
+                                  (size_t)D * osz, cudaMemcpyDeviceToHost, h->io_d2h));
         }
     }
     // io_last follows every launch and output copy of this call (the next call's uploads
