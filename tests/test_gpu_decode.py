@@ -114,15 +114,16 @@ def test_tensor_core_decode_matches_oracle_and_the_mma_sync_path(Hq, Hkv, split_
     np.testing.assert_array_equal(np.stack(o16), to_np(torch.from_numpy(np.stack(outs)).to(torch.bfloat16)))
 
 
-@pytest.mark.parametrize("Hq,Hkv,window,block_rows,out_bf16", [
-    (32, 32, 0, 0, False), (32, 8, 0, 0, False), (32, 32, 100, 0, False), (32, 32, 0, 64, False),
-    (32, 32, 0, 0, True),
+@pytest.mark.parametrize("Hq,Hkv,window,block_rows,out_bf16,B", [
+    (32, 32, 0, 0, False, 48), (32, 8, 0, 0, False, 160), (32, 32, 100, 0, False, 48), (32, 32, 0, 64, False, 48),
+    (32, 32, 0, 0, True, 48), (32, 32, 0, 0, False, 58),
 ])
-def test_many_short_lanes_per_cta_match_oracle(Hq, Hkv, window, block_rows, out_bf16):
+def test_many_short_lanes_per_cta_match_oracle(Hq, Hkv, window, block_rows, out_bf16, B):
     """Short ragged contexts with many lanes run on CTAs that walk several lanes each
     (KVC_OPT_DECODE_LANES): every sampled sequence against the oracle, stored rows bit
-    for bit, and the outputs against the one-CTA-per-lane path."""
-    B = 48 if Hkv == 32 else 160                     # at least four waves of lanes
+    for bit, and the outputs against the one-CTA-per-lane path.  At least four waves of
+    lanes; on 152 SMs B = 48 gives 6 lanes per CTA in whole CTAs, B = 58 gives 7 lanes
+    per CTA with one lane in the last CTA."""
     L0 = np.random.default_rng(B + Hkv).integers(0, 301, size=B).tolist()
     L0[0], L0[1] = 0, 300
     steps = 3
