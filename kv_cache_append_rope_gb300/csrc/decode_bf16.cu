@@ -62,13 +62,17 @@ __device__ __forceinline__ int key_span(int t, int window) {
     return window > 0 ? t - (max(0, t - window) & ~(KT - 1)) : t;
 }
 
+// A query pair (x, y) rotated by (cos, sin) = cs in float32.
+__device__ __forceinline__ float2 q_rotate(float x, float y, float2 cs) {
+    return make_float2(fmaf(x, cs.x, -(y * cs.y)), fmaf(y, cs.x, x * cs.y));
+}
+
 // Rotated query pair (c, c+1) of row `row` (< G) of this lane, as float32 (fused step).
 __device__ __forceinline__ float2 fused_q_pair(const DecodeLaunch& a, int b, int qh, int c, int pos) {
     const __nv_bfloat162 v = *(const __nv_bfloat162*)(a.q_in + ((int64_t)b * a.Hq + qh) * D + c);
     const float x = __low2float(v), y = __high2float(v);
     if (!a.rope_f) return make_float2(x, y);
-    const float2 cs = a.rope_f[(int64_t)pos * (D / 2) + c / 2];
-    return make_float2(fmaf(x, cs.x, -(y * cs.y)), fmaf(y, cs.x, x * cs.y));
+    return q_rotate(x, y, a.rope_f[(int64_t)pos * (D / 2) + c / 2]);
 }
 
 // Final output element: float32, or rounded to bf16 when the caller asked for bf16 output.
@@ -541,6 +545,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
 // four consumer warps only, and write the normalised output; the CTA of a sequence's
 // key/value head 0 commits its length.
 constexpr int kLanesMaxG = 4;
+constexpr int kLanesQBytes = kLanesMaxG * D * 2;  // a lane's rotated, scaled bf16 queries
 constexpr int kLanesMergeBytes = NCW * kLanesMaxG * D * 4 + NCW * kLanesMaxG * 8;
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -557,6 +562,9 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     volatile int* s_err = (volatile int*)(empty + STAGES);
     float* Om = (float*)(smem + STAGES * STAGE_BYTES + 256);                 // [NCW][4][D]
     float2* ML = (float2*)(smem + STAGES * STAGE_BYTES + 256 + NCW * kLanesMaxG * D * 4);  // [NCW][4]
+    // [STAGES][kLanesMaxG][D] bf16: the queries of the lane whose first tile is in stage s
+    uint8_t* Qs = smem + STAGES * STAGE_BYTES + 256 + kLanesMergeBytes;
+    const float qscale = 1.4426950408889634f * rsqrtf((float)D);
     grid_dependency_wait();
     launch_dependents();
     const int G = a.Hq / a.Hkv;
@@ -592,13 +600,27 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             const int lo = a.window > 0 ? max(0, t - a.window) : 0;
             const int r0 = lo & ~(KT - 1);
             const int ntiles = (t - r0 + KT - 1) / KT;
-            // the new row (slot old_len), then its TMA reads: generic-proxy writes first
+            // The new row (slot old_len), then its TMA reads: generic-proxy writes first.  The
+            // lane's queries are loaded with it (one memory latency for both), rotated,
+            // scaled and stored as bf16 in the query slot of the stage that takes the lane's
+            // first tile: the consumers read them from shared memory once that stage is full,
+            // instead of waiting for the loads at the start of every lane.
+            uint2 qpk[kLanesMaxG];
             {
                 const int64_t src = ((int64_t)b * a.Hkv + hkv) * D + lane * 4;
                 const bool slot_ok = debug_check(kv_slot_ok(a.kv, b, old_len), lane == 0 ? a.err : nullptr);
                 const int64_t dst = slot_ok ? kv_row(a.kv, b, hkv, old_len) * D + lane * 4 : 0;
                 const uint2 kraw = *(const uint2*)(a.k_in + src);
                 const uint2 vraw = *(const uint2*)(a.v_in + src);
+                uint2 qraw[kLanesMaxG];
+#pragma unroll
+                for (int g = 0; g < kLanesMaxG; ++g)
+                    if (g < G) qraw[g] = *(const uint2*)(a.q_in + ((int64_t)b * a.Hq + hkv * G + g) * D + lane * 4);
+                float2 cs[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+                if (a.rope_f) {
+                    cs[0] = a.rope_f[(int64_t)pos * (D / 2) + lane * 2];
+                    cs[1] = a.rope_f[(int64_t)pos * (D / 2) + lane * 2 + 1];
+                }
                 const __nv_bfloat16* kin = (const __nv_bfloat16*)&kraw;
                 __nv_bfloat16 kout[4];
 #pragma unroll
@@ -606,12 +628,25 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const float xf = __bfloat162float(kin[2 * e]), yf = __bfloat162float(kin[2 * e + 1]);
                     if (a.rope_f) {
                         const int j = lane * 2 + e;
-                        const float2 cs = a.rope_f[(int64_t)pos * (D / 2) + j];
-                        kout[2 * e] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, false);
-                        kout[2 * e + 1] = rope_bf16_exact(xf, yf, cs.x, cs.y, a.rope, pos, D / 2, j, true);
+                        kout[2 * e] = rope_bf16_exact(xf, yf, cs[e].x, cs[e].y, a.rope, pos, D / 2, j, false);
+                        kout[2 * e + 1] = rope_bf16_exact(xf, yf, cs[e].x, cs[e].y, a.rope, pos, D / 2, j, true);
                     } else {
                         kout[2 * e] = kin[2 * e];
                         kout[2 * e + 1] = kin[2 * e + 1];
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < kLanesMaxG; ++g) {
+                    if (g < G) {
+                        const __nv_bfloat16* qin = (const __nv_bfloat16*)&qraw[g];
+                        uint32_t w[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float2 x = make_float2(__bfloat162float(qin[2 * e]), __bfloat162float(qin[2 * e + 1]));
+                            if (a.rope_f) x = q_rotate(x.x, x.y, cs[e]);
+                            w[e] = pack_bf16(x.x * qscale, x.y * qscale);
+                        }
+                        qpk[g] = make_uint2(w[0], w[1]);
                     }
                 }
                 if (slot_ok) {
@@ -622,7 +657,25 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __syncwarp();
             }
-            if (lane == 0 && !a.test_stall) {
+            if (a.test_stall) continue;
+            // the query slot belongs to the first tile's stage: free once that stage is
+            {
+                const int s0 = gi % STAGES;
+                const bool free_ok =
+                    gi < STAGES || __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty[s0]), ((gi / STAGES) - 1) & 1));
+                if (!free_ok) {
+                    if (lane == 0) {
+                        *s_err = 1;
+                        atomicOr(a.err, (uint32_t)DEV_ERR_WAIT_TIMEOUT);
+                    }
+                    break;
+                }
+#pragma unroll
+                for (int g = 0; g < kLanesMaxG; ++g)
+                    if (g < G) *(uint2*)(Qs + s0 * kLanesQBytes + (g * D + lane * 4) * 2) = qpk[g];
+                __syncwarp();
+            }
+            if (lane == 0) {
                 prefetch_tmap(&tmK16);
                 prefetch_tmap(&tmV16);
                 for (int i = 0; i < ntiles; ++i, ++gi) {
@@ -673,30 +726,17 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         // ---------------- consumers (one 16-row m tile, 16 keys of each stage per warp) ----------------
         const int kofs = warp * 16;
         const int qa = lane >> 2, qc = (lane & 3) * 2;
-        const float qscale = 1.4426950408889634f * rsqrtf((float)D);
         int gi = 0;
         for (int li = l_begin; li < l_end; ++li) {
             int b, hkv;
             lane_of(li, b, hkv);
-            const int old_len = a.old_len[b], pos = a.pos[b];
+            const int old_len = a.old_len[b];
             if (!(old_len >= 0 && old_len < a.C) && kDebug) continue;
             const int t = old_len + 1;
             const int lo = a.window > 0 ? max(0, t - a.window) : 0;
             const int r0 = lo & ~(KT - 1);
             const int ntiles = (t - r0 + KT - 1) / KT;
             uint32_t qf[8][4];
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const int c = ks * 16 + qc;
-                const float2 z = make_float2(0.f, 0.f);
-                const int qh = hkv * G;
-                const float2 x0 = qa < G ? fused_q_pair(a, b, qh + qa, c, pos) : z;
-                const float2 x2 = qa < G ? fused_q_pair(a, b, qh + qa, c + 8, pos) : z;
-                qf[ks][0] = pack_bf16(x0.x * qscale, x0.y * qscale);
-                qf[ks][1] = 0u;                              // rows 8 .. 15: beyond G <= 4
-                qf[ks][2] = pack_bf16(x2.x * qscale, x2.y * qscale);
-                qf[ks][3] = 0u;
-            }
             float o[16][4];
             float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 #pragma unroll
@@ -709,6 +749,17 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), (gi / STAGES) & 1))) {
                     ok = false;
                     break;
+                }
+                if (i == 0) {
+                    // the lane's queries, written by the producer before it armed this stage
+                    const uint32_t* qs = (const uint32_t*)(Qs + s * kLanesQBytes) + qa * (D / 2);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        qf[ks][0] = qa < G ? qs[(ks * 16 + qc) / 2] : 0u;
+                        qf[ks][1] = 0u;                      // rows 8 .. 15: beyond G <= 4
+                        qf[ks][2] = qa < G ? qs[(ks * 16 + qc + 8) / 2] : 0u;
+                        qf[ks][3] = 0u;
+                    }
                 }
                 const uint32_t kt = smem_u32(smem + s * STAGE_BYTES);
                 consume_stage<1>(kt, kt + TILE_BYTES, r0 + i * KT + kofs, t, lo, qf, o, m, l, lane, kofs);
@@ -749,7 +800,7 @@ decode_lanes_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             }
             if (threadIdx.x == 0 && hkv == 0 && !a.no_commit) {
                 a.len_out[b] = old_len + 1;
-                a.next_out[b] = pos + 1;
+                a.next_out[b] = a.pos[b] + 1;
             }
             consumer_bar();                          // the buffer is free for the next lane
         }
@@ -801,7 +852,7 @@ cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s) {
 int decode_bf16_ctas_per_sm(int group) { return group <= 16 ? Cfg<1>::MINB : Cfg<2>::MINB; }
 
 cudaError_t launch_decode_lanes(const DecodeLaunch& a, cudaStream_t s) {
-    constexpr int SMEM = smem_bytes<Cfg<1>::STAGES>() + kLanesMergeBytes;
+    constexpr int SMEM = smem_bytes<Cfg<1>::STAGES>() + kLanesMergeBytes + Cfg<1>::STAGES * kLanesQBytes;
     static PerDeviceOnce attr;
     cudaError_t e = attr.run(
         [] { return cudaFuncSetAttribute(decode_lanes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM); });
