@@ -295,28 +295,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ query rows 0 .. 31
-        // row g < G: query head hkv * G + g rotated at `pos`; rows G .. 31 zero
+        // row g < G: query head hkv * G + g rotated at `pos`; rows G .. 31 zero.  Lane l
+        // takes columns 4 l .. 4 l + 3 (rotation pairs 2 l, 2 l + 1) of every row, so that
+        // all 32 row loads are in flight at once and the cos/sin pairs are loaded once.
         uint8_t* qt = smem + OFF_Q;
-        const int g = lane;
-        const __nv_bfloat16* qrow = a.q_in + ((int64_t)b * a.Hq + hkv * G + g) * D;
-        const float2* cs = a.rope_f ? a.rope_f + (int64_t)pos * (D / 2) : nullptr;
-#pragma unroll 4
-        for (int c = 0; c < D / 8; ++c) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (g < G) {
-                v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-                if (cs) {
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float2 cs[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+        if (a.rope_f) {
+            cs[0] = a.rope_f[(int64_t)pos * (D / 2) + 2 * lane];
+            cs[1] = a.rope_f[(int64_t)pos * (D / 2) + 2 * lane + 1];
+        }
+        const __nv_bfloat16* q0 = a.q_in + ((int64_t)b * a.Hq + hkv * G) * D + 4 * lane;
+        uint2 raw[32];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float x = __uint_as_float(w[p] << 16), y = __uint_as_float(w[p] & 0xffff0000u);
-                        const float2 f = cs[4 * c + p];
-                        w[p] = pack_bf16(fmaf(x, f.x, -(y * f.y)), fmaf(y, f.x, x * f.y));
-                    }
-                    v = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int g = 0; g < 32; ++g) raw[g] = g < G ? *reinterpret_cast<const uint2*>(q0 + (int64_t)g * D) : make_uint2(0u, 0u);
+        const int chunk = lane >> 1;                   // 16-byte chunk of the 256-byte row
+#pragma unroll
+        for (int g = 0; g < 32; ++g) {
+            uint32_t w[2] = {raw[g].x, raw[g].y};
+            if (a.rope_f && g < G) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float x = __uint_as_float(w[p] << 16), y = __uint_as_float(w[p] & 0xffff0000u);
+                    w[p] = pack_bf16(fmaf(x, cs[p].x, -(y * cs[p].y)), fmaf(y, cs[p].x, x * cs[p].y));
                 }
             }
-            *reinterpret_cast<uint4*>(qt + (c >> 3) * HALF + swz128(g, c & 7)) = v;
+            *reinterpret_cast<uint2*>(qt + (chunk >> 3) * HALF + swz128(g, chunk & 7) + (lane & 1) * 8) =
+                make_uint2(w[0], w[1]);
         }
         fence_proxy_async_smem();
         __syncwarp();
