@@ -134,6 +134,21 @@ class KVCache:
                                             ctypes.byref(dv), ctypes.byref(do), _stream(stream)))
         return out
 
+    def bind_append_attend(self, layer, q, k, v, out, stream=None):
+        """A kvc_append_attend call on fixed tensors, its descriptors and stream built once:
+        returns a function that enqueues one decode step (for loops that reuse the same
+        buffers every step, where building the arguments would cost more host time than
+        the call itself)."""
+        descs = tuple(tensor_desc(t) for t in (q, k, v, out))
+        refs = tuple(ctypes.byref(d) for d in descs)
+        st, fn, h, check = _stream(stream), L.lib.kvc_append_attend, self._h, self._check
+        keep = (descs, q, k, v, out)
+
+        def call():
+            check(fn(h, layer, refs[0], refs[1], refs[2], refs[3], st))
+            return keep[-1]
+        return call
+
     def prepare_attend(self, layer, q, k, v, out=None, stream=None):
         """kvc_prepare_attend: a decode step without its commit; returns (out, ticket)."""
         if out is None:

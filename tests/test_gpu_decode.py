@@ -320,3 +320,45 @@ def test_dependent_launch_option_changes_no_result(Hkv):
         np.testing.assert_array_equal(x, y)
     for c in caches:
         c.check()
+
+
+@pytest.mark.gpu
+def test_bound_append_attend_equals_the_plain_call():
+    """KVCache.bind_append_attend (descriptors marshalled once, the bench's loop) enqueues the
+    same kvc_append_attend call: outputs and stored rows equal the plain call's bit for bit,
+    and the bound call keeps working when the tensors' contents change between steps."""
+    need_gpu()
+    B, Hq, Hkv, D, steps, C = 6, 8, 2, 128, 3, 96
+    L0 = [0, 5, 17, 40, 64, 70]
+    q = W.normal_np((steps, B, Hq, 1, D), 11)
+    k = W.normal_np((steps, B, Hkv, 1, D), 12)
+    v = W.normal_np((steps, B, Hkv, 1, D), 13)
+    pre_k = W.normal_np((B, Hkv, max(L0), D), 14)
+    pre_v = W.normal_np((B, Hkv, max(L0), D), 15)
+    results = []
+    for bound in (False, True):
+        cache = KVCache(B, Hq, C, D, heads_kv=Hkv, dtype="bf16", rope_base=BASE)
+        cache.prefill_suffix(0, None, device_tensor(pre_k, "bf16"), device_tensor(pre_v, "bf16"), seqlen=L0,
+                             out=False)
+        qi, ki, vi = (torch.empty((B, H, 1, D), dtype=torch.bfloat16, device="cuda") for H in (Hq, Hkv, Hkv))
+        out = torch.empty((B, Hq, 1, D), dtype=torch.float32, device="cuda")
+        call = cache.bind_append_attend(0, qi, ki, vi, out) if bound else None
+        outs = []
+        for i in range(steps):
+            qi.copy_(device_tensor(q[i], "bf16"))
+            ki.copy_(device_tensor(k[i], "bf16"))
+            vi.copy_(device_tensor(v[i], "bf16"))
+            if bound:
+                call()
+            else:
+                cache.append_attend(0, qi, ki, vi, out=out)
+            outs.append(to_np(out).copy())
+        torch.cuda.synchronize()
+        Ks, Vs, _ = storage_np(cache)
+        results.append((np.stack(outs), Ks, Vs, cache.get_lengths(0)[0]))
+        cache.check()
+    (o0, k0, v0, l0), (o1, k1, v1, l1) = results
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(k0, k1)
+    np.testing.assert_array_equal(v0, v1)
+    assert l0 == l1 == [l + steps for l in L0]
