@@ -541,20 +541,32 @@ def start_workers(n=None):
     return Workers(n or os.cpu_count() or 1)
 
 
-def cpu_baseline(bench, workers, unit):
-    """The oracle on the host cores, warm (a first untimed batch): one task per core side
-    by side (value = their work / the slowest one's time), and one task alone (`one_core`)."""
+CPU_BASELINE_SECONDS = 10.0     # timed oracle wall time per workload (rounds of one task per core)
+
+
+def cpu_baseline(bench, workers, unit, seconds=CPU_BASELINE_SECONDS):
+    """The oracle on the host cores, warm (a first untimed round): rounds of one task per
+    core side by side until about `seconds` of wall time (value = the rounds' work / the sum
+    of each round's slowest task), and one task alone (`one_core`, at least a fifth as long)."""
     scale = 1e9 if unit == "GB/s" else 1e12
     tasks, work, desc = bench.cpu_tasks(workers.n, **CPU_TASK[bench.name])
     workers.run(tasks)                    # untimed: each process builds its cos/sin table once
-    secs = workers.run(tasks)
-    wall = max(secs)
-    line = {"value": round(sum(work) / scale / wall, 6), "unit": unit, "cores": workers.n, "kind": "oracle",
-            "sample": f"{workers.n} {desc}, one oracle process per core side by side",
-            "seconds": round(wall, 2), "cpu_seconds": round(sum(secs), 2)}
-    one = workers.run(tasks[:1])[0]
-    line["one_core"] = {"value": round(work[0] / scale / one, 6), "unit": unit, "cores": 1,
-                        "sample": f"1 {desc}, alone", "seconds": round(one, 2)}
+    wall = cpu = 0.0
+    rounds = 0
+    while rounds == 0 or (wall < seconds and rounds < 10000):
+        secs = workers.run(tasks)
+        wall += max(secs)
+        cpu += sum(secs)
+        rounds += 1
+    line = {"value": round(rounds * sum(work) / scale / wall, 6), "unit": unit, "cores": workers.n, "kind": "oracle",
+            "sample": f"{rounds} rounds of {workers.n} {desc}, one oracle process per core side by side",
+            "seconds": round(wall, 2), "cpu_seconds": round(cpu, 2)}
+    one, n1 = 0.0, 0
+    while n1 == 0 or (one < seconds / 5 and n1 < 10000):
+        one += workers.run(tasks[:1])[0]
+        n1 += 1
+    line["one_core"] = {"value": round(n1 * work[0] / scale / one, 6), "unit": unit, "cores": 1,
+                        "sample": f"{n1} rounds of 1 {desc}, alone", "seconds": round(one, 2)}
     return line
 
 

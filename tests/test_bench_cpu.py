@@ -51,3 +51,29 @@ def test_reference_inputs_do_not_load_the_library():
         "print('ok')\n")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_cpu_baseline_times_rounds_up_to_the_requested_seconds():
+    """bench.cpu_baseline repeats rounds of one task per worker until the requested wall
+    time and reports the rounds' work over the sum of each round's slowest task."""
+    code = (
+        "import sys, torch\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "sys.argv = ['bench.py']\n"
+        "import bench\n"
+        "from oracle.timing import Workers\n"
+        "b = bench.make_bench('gqa_decode', torch.device('cpu'), batch=2, with_cache=False)\n"
+        "bench.CPU_TASK['gqa_decode'] = dict(steps=1)\n"
+        "w = Workers(2)\n"
+        "try:\n"
+        "    line = bench.cpu_baseline(b, w, 'GB/s', seconds=0.5)\n"
+        "finally:\n"
+        "    w.close()\n"
+        "rounds = int(line['sample'].split()[0])\n"
+        "assert line['cores'] == 2 and line['kind'] == 'oracle' and line['value'] > 0\n"
+        "assert line['seconds'] >= 0.5 and rounds >= 1, line\n"
+        "assert line['cpu_seconds'] >= line['seconds'] * 0.9, line\n"
+        "assert line['one_core']['cores'] == 1 and line['one_core']['seconds'] >= 0.1, line\n"
+        "print('ok')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
