@@ -1031,6 +1031,7 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
         return fail(h, KVC_ERR_CONFIG, "the tensor-core suffix kernel needs bf16 storage and d_h = 128");
     const bool use_tc = out && tc_ok && !h->opt_force_generic && h->opt_suffix_kernel != 1;
     const bool use_tc2 = use_tc && h->opt_suffix_kernel == 3 && !h->paged();
+    const bool use_tcp = use_tc && h->opt_suffix_kernel == 4 && !h->paged();
     std::vector<int4> work;
     if (use_tc2) {
         // one item per (sequence, query head, four 128-row query tiles): a pair of CTAs
@@ -1155,7 +1156,12 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
         sl.out = (float*)out->data; sl.err = h->err_d;
         sl.B = B; sl.Hq = Hq; sl.Hkv = Hkv; sl.S = S; sl.C = C; sl.window = h->cfg.window;
         sl.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-        KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc(sl, (int)work.size(), s); }));
+        if (use_tcp) {
+            const int sms = sm_count(h->cfg.device);
+            KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tcp(sl, sms, s); }));
+        } else {
+            KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc(sl, (int)work.size(), s); }));
+        }
     } else if (out && !use_tc) {
         GenericAttendLaunch g{};
         g.qrot = h->qrot_chunk; g.K = h->K_layer(layer); g.V = h->V_layer(layer);
@@ -1797,7 +1803,7 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             h->opt_force_generic = value != 0;
             return KVC_OK;
         case KVC_OPT_SUFFIX_KERNEL:
-            if (value < 0 || value > 3) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1, 2 or 3");
+            if (value < 0 || value > 4) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1, 2, 3 or 4");
             h->opt_suffix_kernel = value;
             return KVC_OK;
         case KVC_OPT_TIMING:

@@ -333,6 +333,9 @@ struct SuffixLaunch {
     float scale_log2;            // log2(e) / sqrt(d_h)
 };
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);
+// Persistent form: one CTA per SM (at most n_work) walks the work list round robin;
+// contiguous storage only.
+cudaError_t launch_suffix_tcp(const SuffixLaunch& a, int sms, cudaStream_t s);
 
 // Pair-of-SMs tile kernel (cta_group::2): a cluster of two CTAs per work item.
 struct SuffixLaunch2 {

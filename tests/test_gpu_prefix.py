@@ -35,6 +35,9 @@ def make_inputs(B, Hq, Hkv, T, D, dtype, seed):
     ("bf16", 128, 4, 4, 3, 300, [150, 0, 257]),      # pair-of-SMs tile kernel
     ("bf16", 128, 8, 2, 3, 300, [150, 0, 257]),
     ("bf16", 128, 2, 1, 3, 1500, [1200, 37, 640]),
+    ("bf16", 128, 4, 4, 4, 300, [150, 0, 257]),      # persistent tile kernel, one item per CTA
+    ("bf16", 128, 2, 1, 4, 1500, [1200, 37, 640]),
+    ("bf16", 128, 32, 8, 4, 1500, [1200, 37, 640]),  # persistent: 384 items, several per CTA
 ])
 def test_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, T, cuts):
     need_gpu()
@@ -204,3 +207,29 @@ def test_toy_decoder_prefix_reuse_through_library(seed, condition):
         else:
             assert err > 1e-12
         gpu.cache.check()
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_persistent_tile_kernel_equals_the_one_item_kernel(window):
+    """The persistent tile kernel (one CTA per SM walking the work list, barriers counting
+    across items, the next item's loads and QK^T overlapping the epilogue) computes every
+    item as the one-item-per-CTA kernel does: outputs equal bit for bit, with several items
+    per CTA, ragged sequences and a sliding window."""
+    need_gpu()
+    B, Hq, Hkv, D, T = 4, 32, 8, 128, 1400
+    cuts = [1100, 0, 613, 1333]
+    qd, kd, vd = make_inputs(B, Hq, Hkv, T, D, "bf16", seed=45)
+    S = max(T - c for c in cuts)
+    sel = lambda x: torch.stack([torch.nn.functional.pad(x[b, :, cuts[b]:], (0, 0, 0, S - (T - cuts[b])))
+                                 for b in range(B)]).contiguous()
+    outs = []
+    for kernel in (2, 4):
+        cache = KVCache(B, Hq, T + 20, D, heads_kv=Hkv, dtype="bf16", rope_base=BASE, window=window)
+        cache.set_option(L.OPT_SUFFIX_KERNEL, kernel)
+        cache.prefill_suffix(0, qd, kd, vd, out=False)
+        cache.truncate(cuts)
+        cache.poison()
+        outs.append(to_np(cache.prefill_suffix(0, sel(qd), sel(kd), sel(vd), seqlen=[T - c for c in cuts])))
+        assert cache.kernel_stats("suffix")[1] == 1
+        cache.check()
+    np.testing.assert_array_equal(outs[0], outs[1])
