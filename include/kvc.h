@@ -484,10 +484,15 @@ typedef enum kvc_option {
                                       heads as rows of a 128-row query tile, S and O in tensor memory)
                                       when the step is fused, its lengths are host-held and the storage is
                                       contiguous; 0 = the m16n8k16 decode kernel for every group size */
-    KVC_OPT_DECODE_LANES = 12      /* 1 (default) = fused decode steps over many short lanes (every key span
+    KVC_OPT_DECODE_LANES = 12,     /* 1 (default) = fused decode steps over many short lanes (every key span
                                       at most 512 rows, at least four waves of lanes, at most 4 query heads
                                       per key/value head) run with CTAs that walk several lanes each,
                                       longest sequences first; 0 = one CTA per lane and split */
+    KVC_OPT_DECODE_STREAMK = 13    /* 1 (default) = tensor-core decode steps (see KVC_OPT_DECODE_TC) with at
+                                      most 256 lanes (B x H_kv) run as one wave of CTAs, one per SM, each
+                                      over an equal run of 128-key tiles of the lanes laid end to end (a
+                                      CTA's run may span lanes; a lane's partials are merged after);
+                                      0 = per-sequence pieces, about two waves, largest first */
 } kvc_option;
 
 kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value);

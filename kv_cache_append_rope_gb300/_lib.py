@@ -33,6 +33,7 @@ OPT_TEST_POISON = 9
 OPT_TEST_PLANT_LENGTH = 10
 OPT_DECODE_TC = 11
 OPT_DECODE_LANES = 12
+OPT_DECODE_STREAMK = 13
 KERNELS = {"rope_append": 0, "decode": 1, "decode_combine": 2, "suffix": 3, "generic_attend": 4,
            "bookkeeping": 5}
 

@@ -784,9 +784,41 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
         int32_t rows[kFusedMaxB];
     } pieces;
     int lanes_per_cta = 0;
+    struct {
+        bool on = false;
+        int P = 0, T = 0;
+        int32_t start[kFusedMaxB + 1];
+        int32_t first[kFusedMaxB];
+        int32_t ns[kFusedMaxB];
+    } sk;
     if (fast) {
         if (h->opt_split_rows > 0) {
             split_rows = (int)h->opt_split_rows;
+        } else if (tc_decode && h->opt_decode_streamk && (int64_t)B * Hkv <= kFusedMaxB) {
+            // Stream-K: the lanes' 128-key tiles laid end to end, one wave of CTAs (one per
+            // SM) over equal runs of them; a lane's partials: one per CTA its tiles touch.
+            // CTA c starts at tile floor(c T / P); the CTA holding tile x is
+            // floor(((x + 1) P - 1) / T).
+            const int lanes = B * Hkv;
+            int64_t T = 0;
+            for (int l = 0; l < lanes; ++l) {
+                sk.start[l] = (int32_t)T;
+                T += (keys_of(lenh[l / Hkv] + 1) + 127) / 128;
+            }
+            sk.start[lanes] = (int32_t)T;
+            const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sm_count(h->cfg.device), T));
+            max_splits = 1;
+            for (int l = 0; l < lanes; ++l) {
+                const int64_t x0 = sk.start[l], x1 = sk.start[l + 1] - 1;
+                const int64_t c0 = ((x0 + 1) * P - 1) / T, c1 = ((x1 + 1) * P - 1) / T;
+                sk.first[l] = (int32_t)c0;
+                sk.ns[l] = (int32_t)(c1 - c0 + 1);
+                max_splits = std::max(max_splits, sk.ns[l]);
+            }
+            sk.on = true;
+            sk.P = (int)P;
+            sk.T = (int)T;
+            split_rows = 128;
         } else if (tc_decode) {
             // One CTA per SM: every sequence is cut into its own number of equal pieces,
             // about two waves of them in all, and the pieces are launched largest first,
@@ -834,7 +866,7 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
             split_rows = (int)r;
         }
-        if (!pieces.on) max_splits = (max_t + split_rows - 1) / split_rows;
+        if (!pieces.on && !sk.on) max_splits = (max_t + split_rows - 1) / split_rows;
         // Short contexts with many lanes (at least four waves of one-split lanes, G <= 4):
         // CTAs that walk several lanes each, longest sequences first (decode_lanes_kernel).
         // Lanes per CTA: 2 .. 8, the count that minimises waves x (lanes + 0.5), the 0.5
@@ -916,14 +948,22 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return lenh[x] > lenh[y]; });
             for (int i = 0; i < B; ++i) dl.seq_of[i] = order[i];
         }
+        if (sk.on) {
+            dl.streamk = sk.P;
+            dl.streamk_tiles = sk.T;
+            memcpy(dl.item_start, sk.start, (B * Hkv + 1) * sizeof(int32_t));
+            memcpy(dl.seq_of, sk.first, B * Hkv * sizeof(int32_t));
+            memcpy(dl.seq_rows, sk.ns, B * Hkv * sizeof(int32_t));
+        }
         if (pieces.on) {
             memcpy(dl.item_start, pieces.start, (B + 1) * sizeof(int32_t));
             memcpy(dl.seq_of, pieces.seq, B * sizeof(int32_t));
             memcpy(dl.seq_rows, pieces.rows, B * sizeof(int32_t));
         }
         KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE, s, [&] {
-            return tc_decode ? launch_decode_tc(dl, s) : lanes_per_cta ? launch_decode_lanes(dl, s)
-                                                                       : launch_decode_bf16(dl, s);
+            return tc_decode ? (sk.on ? launch_decode_tck(dl, s) : launch_decode_tc(dl, s))
+                             : lanes_per_cta ? launch_decode_lanes(dl, s)
+                                             : launch_decode_bf16(dl, s);
         }));
         if (!dl.merge_in_kernel && max_splits > 1)
             KVC_CUDA(h, timed(h, KVC_KERNEL_DECODE_COMBINE, s, [&] { return launch_decode_combine(dl, s); }));
@@ -1823,6 +1863,9 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             return KVC_OK;
         case KVC_OPT_DECODE_LANES:
             h->opt_decode_lanes = value != 0;
+            return KVC_OK;
+        case KVC_OPT_DECODE_STREAMK:
+            h->opt_decode_streamk = value != 0;
             return KVC_OK;
         case KVC_OPT_DEVICE_LENGTHS: {
             if (value && h->paged())

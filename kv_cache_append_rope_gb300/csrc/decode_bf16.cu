@@ -516,7 +516,9 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
         if (a.pieces) rows = a.seq_rows[b];
     }
     if (!debug_check(t >= 1 && t <= a.C, threadIdx.x == 0 ? a.err : nullptr)) return;
-    const int ns = (key_span(t, a.window) + rows - 1) / rows;
+    // stream-K: the lane's partials, one per CTA its tiles touched
+    const int ns = a.streamk ? a.seq_rows[b * a.Hkv + (qh - b * a.Hq) / (a.Hq / a.Hkv)]
+                             : (key_span(t, a.window) + rows - 1) / rows;
     if (ns <= 1) return;
     const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
     float M = -INFINITY;

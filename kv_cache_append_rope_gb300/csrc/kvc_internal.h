@@ -150,6 +150,7 @@ struct Handle {
     int64_t opt_decode_pdl = 1;
     int64_t opt_decode_tc = 1;
     int64_t opt_decode_lanes = 1;
+    int64_t opt_decode_streamk = 1;
     std::vector<uint64_t> layer_version;  // [L] bumped by every change of a layer's state or staged slot
     bool mirrors_stale = false;    // device-length steps ran since the mirrors were last read back
 
@@ -278,6 +279,11 @@ struct DecodeLaunch {
     // split seq_rows[b] key rows.
     int pieces;
     int lanes_per_cta;                   // many-lane short-context step: lanes each CTA walks
+    // Stream-K tensor-core decode (streamk = P CTAs, 0 = off): lane l = b H_kv + hkv owns
+    // tiles item_start[l] .. item_start[l+1]-1 of streamk_tiles; CTA c takes tiles
+    // [c T / P, (c+1) T / P); seq_of[l] is the lane's first CTA, seq_rows[l] its partials.
+    int streamk;
+    int streamk_tiles;
     int32_t item_start[kFusedMaxB + 1];
     int32_t seq_of[kFusedMaxB];
     int32_t seq_rows[kFusedMaxB];
@@ -289,6 +295,8 @@ cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t s);
 cudaError_t launch_decode_lanes(const DecodeLaunch& a, cudaStream_t s);
 // Tensor-core decode (fused step, contiguous storage, 16 < H_q / H_kv <= 32); one CTA per SM.
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
+// Stream-K form of the tensor-core decode: one wave of a.streamk CTAs.
+cudaError_t launch_decode_tck(const DecodeLaunch& a, cudaStream_t s);
 int decode_bf16_ctas_per_sm(int group);
 
 cudaError_t launch_commit(int32_t* len, int32_t* next, const int32_t* pos0, const int32_t* seqlen,

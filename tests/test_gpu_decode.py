@@ -20,7 +20,7 @@ BASE = 10000.0
 
 
 def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, seed=0, fused=True, tc=True,
-               window=0, out_dtype=None, lanes=True, block_rows=0):
+               window=0, out_dtype=None, lanes=True, block_rows=0, streamk=True):
     """Prefill ragged prefixes, run `steps` decode steps; return (cache, outs, inputs)."""
     need_gpu()
     B = len(L0)
@@ -35,6 +35,8 @@ def run_decode(dtype, D, Hq, Hkv, L0, steps, C, generic=False, split_rows=0, see
         cache.set_option(L.OPT_DECODE_TC, 0)
     if not lanes:
         cache.set_option(L.OPT_DECODE_LANES, 0)
+    if not streamk:
+        cache.set_option(L.OPT_DECODE_STREAMK, 0)
     if generic:
         cache.set_option(L.OPT_FORCE_GENERIC, 1)
     if split_rows:
@@ -112,6 +114,23 @@ def test_tensor_core_decode_matches_oracle_and_the_mma_sync_path(Hq, Hkv, split_
     _, o16, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=800, split_rows=split_rows, window=window,
                            out_dtype=torch.bfloat16)
     np.testing.assert_array_equal(np.stack(o16), to_np(torch.from_numpy(np.stack(outs)).to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("Hq,Hkv,window,B", [(32, 1, 0, 64), (32, 2, 0, 40), (24, 1, 0, 64), (32, 1, 200, 64)])
+def test_streamk_tensor_core_decode_matches_oracle(Hq, Hkv, window, B):
+    """Stream-K tensor-core decode (KVC_OPT_DECODE_STREAMK, the default): the lanes' 128-key
+    tiles laid end to end and cut into one equal run per SM, so that with these short ragged
+    lanes most CTAs span two or three lanes and most lanes several CTAs.  Every sequence
+    against the oracle (stored rows bit for bit, lengths), and the outputs against the
+    per-sequence piece plan."""
+    rng = np.random.default_rng(B + Hq + window)
+    L0 = rng.integers(0, 700, size=B).tolist()
+    L0[:6] = [0, 1, 127, 128, 255, 699]
+    steps = 2
+    cache, outs, qkv = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=704, window=window, seed=5)
+    check_against_oracle("bf16", cache, outs, qkv, L0, steps, window=window)
+    _, ref, _ = run_decode("bf16", 128, Hq, Hkv, L0, steps, C=704, window=window, seed=5, streamk=False)
+    assert np.abs(np.stack(outs) - np.stack(ref)).max() < 1e-2
 
 
 @pytest.mark.parametrize("Hq,Hkv,window,block_rows,out_bf16,B", [
