@@ -62,7 +62,7 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 TRAFFIC = {
     "mha_decode": ("ratio", 1.013),
     "gqa_decode": ("ratio", 1.0067),
-    "mqa_decode": ("ratio", 1.0204),
+    "mqa_decode": ("ratio", 1.0071),
     "mha_decode_short": ("ratio", 1.073),
     "suffix": ("per_sequence", 375401472.0 + 174217472.0),
 }
@@ -331,7 +331,7 @@ class DecodeBench:
         c = self.cfg
         G = c["Hq"] // c["Hkv"]
         if 16 < G <= 32 and not self.block_rows and self.graph is None:
-            return "decode_tc_kernel"
+            return "decode_tck_kernel" if c["B"] * c["Hkv"] <= 256 else "decode_tc_kernel"
         if G <= 4 and c["B"] * c["Hkv"] >= 4 * 2 * 152 and c["hi"] + c["steps"] <= 512 and self.graph is None:
             return "decode_lanes_kernel"
         return "decode_bf16_kernel"
