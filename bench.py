@@ -114,6 +114,16 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def sustained_bf16():
+    """The measured cuBLAS bf16 rate of a seconds-long back-to-back loop under the power
+    cap (None when not measured)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -646,6 +656,7 @@ def run_ours(args, name, world, rank, local, workers=None):
                 "frac": round(achieved / tflops, 4), "traffic": traffic, "kernel": dom,
                 "peak_source": f"{peak_kind} bf16_tflops (burst)",
                 "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4), "nominal_peak": NOMINAL_BF16_TFLOPS,
+                "frac_of_sustained": (round(achieved / sustained_bf16(), 4) if sustained_bf16() else None),
                 "kernel_ms_per_launch": round(dom_ms / dom_launches, 3),
                 "algorithmic_flops_per_launch": round(alg / dom_launches),
                 "step_achieved": round(achieved_step, 1), "step_frac": round(achieved_step / tflops, 4)}
