@@ -666,14 +666,14 @@ def run_ours(args, name, world, rank, local, workers=None):
 
     e2e = None
     if not args.no_e2e:
-        # three runs of the timed steps (the host link's rate varies from run to run on a
-        # shared machine); the median is reported, every run listed
+        # five runs of the timed steps (on a shared machine a host-buffer step now and then
+        # takes several times as long as the others); the median is reported, every run listed
         bench.e2e_setup()
         for _ in range(max(1, args.warmup)):
             bench.e2e_step()
         torch.cuda.synchronize(device)
         runs = []
-        for _ in range(3):
+        for _ in range(5):
             barrier(world)
             t0 = time.perf_counter()
             for _ in range(args.steps):
@@ -682,9 +682,9 @@ def run_ours(args, name, world, rank, local, workers=None):
             barrier(world)
             e2e_s = max_over_ranks(time.perf_counter() - t0, world)
             runs.append(units * world / e2e_s)
-        e2e = {"value": round(sorted(runs)[1], 2), "unit": unit, "h2d_bytes_per_step": int(bench.h2d),
+        e2e = {"value": round(sorted(runs)[2], 2), "unit": unit, "h2d_bytes_per_step": int(bench.h2d),
                "d2h_bytes_per_step": int(bench.d2h), "runs": [round(r, 2) for r in runs],
-               "statistic": "median of 3 runs of the timed steps"}
+               "statistic": "median of 5 runs of the timed steps"}
 
     cpu = None
     if rank == 0 and world == 1 and workers is not None:
