@@ -116,7 +116,8 @@ def test_tensor_core_decode_matches_oracle_and_the_mma_sync_path(Hq, Hkv, split_
     np.testing.assert_array_equal(np.stack(o16), to_np(torch.from_numpy(np.stack(outs)).to(torch.bfloat16)))
 
 
-@pytest.mark.parametrize("Hq,Hkv,window,B", [(32, 1, 0, 64), (32, 2, 0, 40), (24, 1, 0, 64), (32, 1, 200, 64)])
+@pytest.mark.parametrize("Hq,Hkv,window,B", [(32, 1, 0, 64), (32, 2, 0, 40), (24, 1, 0, 64), (32, 1, 200, 64),
+                                              (32, 1, 0, 256)])   # 256 lanes: the plan's limit
 def test_streamk_tensor_core_decode_matches_oracle(Hq, Hkv, window, B):
     """Stream-K tensor-core decode (KVC_OPT_DECODE_STREAMK, the default): the lanes' 128-key
     tiles laid end to end and cut into one equal run per SM, so that with these short ragged
