@@ -246,7 +246,10 @@ kvc_status kvc_prefill_suffix(kvc_handle* h, int32_t layer, const kvc_tensor* q,
  * kvc_prefill_suffix with q, k, v and out in HOST memory (page-locked memory
  * lets the copies overlap the work; pageable memory works, without overlap).
  * Same arguments, layouts, results and errors as kvc_prefill_suffix, plus:
- *   chunk_sequences: sequences per pipeline stage (0 -> ceil(B / 8)).
+ *   chunk_sequences: sequences per pipeline stage (0 -> ceil(B / 8)); the stages take
+ *                    the sequences smallest first, the second smallest last and the
+ *                    others largest first (by seqlen), so that the first upload and the
+ *                    last download are short.
  * Every check of the whole call (shapes, dtypes, capacity, positions, storage
  * blocks; in checked mode the finiteness of k and v, scanned on the host) runs
  * before any copy or launch; an error leaves the state unchanged.  The call
