@@ -356,8 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 // The whole 128-column row is read with one wait, then reduced to its
                 // maximum, then turned into exponentials in place.
                 float x[BN];
-#pragma unroll
-                for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+                tmem_ld128(s_addr, x);
                 tmem_wait_ld();
                 if constexpr (decltype(mask_c)::value) {
                     const int kb = jj * BN;
