@@ -416,8 +416,7 @@ decode_tck_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 const bool masked = kb < sg.lo || kb + BN > sg.r1;
                 auto tile = [&](auto mask_c) -> bool {
                     float x[BN];
-#pragma unroll
-                    for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+                    tmem_ld128(s_addr, x);
                     tmem_wait_ld();
                     if constexpr (decltype(mask_c)::value) {
 #pragma unroll
@@ -470,20 +469,17 @@ decode_tck_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 #pragma unroll
                     for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
                     const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
+                    uint32_t pk[BN / 2];
 #pragma unroll
-                    for (int q = 0; q < BN / 32; ++q) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int c2 = q * 32 + 2 * e;
-                            const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
-                            const float p0 = fast_exp2(arg.x);
-                            const float p1 = fast_exp2(arg.y);
-                            l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
-                            pk[e] = pack_bf16(p0, p1);
-                        }
-                        tmem_st16u(s_addr + q * 16, pk);
+                    for (int e = 0; e < BN / 2; ++e) {
+                        const int c2 = 2 * e;
+                        const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
+                        const float p0 = fast_exp2(arg.x);
+                        const float p1 = fast_exp2(arg.y);
+                        l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
+                        pk[e] = pack_bf16(p0, p1);
                     }
+                    tmem_st64u(s_addr, pk);
                     l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
                     l_run += l4[0].x + l4[0].y;
                     tmem_wait_st();
