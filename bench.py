@@ -64,7 +64,7 @@ TRAFFIC = {
     "gqa_decode": ("ratio", 1.0067),
     "mqa_decode": ("ratio", 1.0071),
     "mha_decode_short": ("ratio", 1.073),
-    "suffix": ("per_sequence", 375401472.0 + 174217472.0),
+    "suffix": ("per_sequence", 375812608.0 + 175133952.0),
 }
 
 
