@@ -83,6 +83,44 @@ __device__ __forceinline__ void store_out(const DecodeLaunch& a, int64_t i, floa
         ((float*)a.out)[i] = x;
 }
 
+// Log-sum-exp merge of one query head's ns split partials ((max, sum) in ml, O rows in po,
+// already offset to one head dim): the loads of the first kMergeBatch splits are all issued
+// before any is used (one memory round trip instead of two per split), and the sums run
+// over the splits in order.
+constexpr int kMergeBatch = 8;
+__device__ __forceinline__ float merge_splits(const float2* ml, const float* po, int ns) {
+    float2 mv[kMergeBatch];
+    float ov[kMergeBatch];
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s) {
+        if (s < ns) {
+            mv[s] = __ldcg(&ml[s]);
+            ov[s] = __ldcg(po + (int64_t)s * D);
+        }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s)
+        if (s < ns) M = fmaxf(M, mv[s].x);
+    for (int s = kMergeBatch; s < ns; ++s) M = fmaxf(M, __ldcg(&ml[s].x));
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s) {
+        if (s < ns) {
+            const float f = fast_exp2(mv[s].x - M);
+            L += mv[s].y * f;
+            O += ov[s] * f;
+        }
+    }
+    for (int s = kMergeBatch; s < ns; ++s) {
+        const float2 v = __ldcg(&ml[s]);
+        const float f = fast_exp2(v.x - M);
+        L += v.y * f;
+        O += __ldcg(po + (int64_t)s * D) * f;
+    }
+    return O / L;
+}
+
 // One 64-key stage of a consumer warp: S = Q K^T for the warp's KW = 16 MT keys (key
 // key_base + j), masked outside [lo, r1); the online softmax of rows qa and qa + 8 of
 // its m tile; O += P V.  kt, vt: the stage's K and V tiles in shared memory.
@@ -484,18 +522,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     for (int u = threadIdx.x; u < G * D; u += THREADS) {
         const int g = u / D, dim = u - g * D;
         const int64_t qh = (int64_t)b * a.Hq + hkv * G + g;
-        const float2* ml = a.part_ml + qh * a.max_splits;
-        const float* po = a.part_o + qh * a.max_splits * D + dim;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit_lane; ++sp) M = fmaxf(M, __ldcg(&ml[sp].x));
-        float L = 0.f, O = 0.f;
-        for (int sp = 0; sp < nsplit_lane; ++sp) {
-            const float2 v = __ldcg(&ml[sp]);
-            const float f = fast_exp2(v.x - M);
-            L += v.y * f;
-            O += __ldcg(po + (int64_t)sp * D) * f;
-        }
-        store_out(a, qh * D + dim, O / L);
+        store_out(a, qh * D + dim,
+                  merge_splits(a.part_ml + qh * a.max_splits, a.part_o + qh * a.max_splits * D + dim, nsplit_lane));
     }
     if (threadIdx.x == 0) a.lane_ticket[lane_kv] = 0;
 }
@@ -520,17 +548,9 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeLaunch a) {
     const int ns = a.streamk ? a.seq_rows[b * a.Hkv + (qh - b * a.Hq) / (a.Hq / a.Hkv)]
                              : (key_span(t, a.window) + rows - 1) / rows;
     if (ns <= 1) return;
-    const float2* ml = a.part_ml + (int64_t)qh * a.max_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
-    float L = 0.f, O = 0.f;
-    const float* po = a.part_o + (int64_t)qh * a.max_splits * D + threadIdx.x;
-    for (int s = 0; s < ns; ++s) {
-        const float f = fast_exp2(ml[s].x - M);
-        L += ml[s].y * f;
-        O += po[(int64_t)s * D] * f;
-    }
-    store_out(a, (int64_t)qh * D + threadIdx.x, O / L);
+    store_out(a, (int64_t)qh * D + threadIdx.x,
+              merge_splits(a.part_ml + (int64_t)qh * a.max_splits,
+                           a.part_o + (int64_t)qh * a.max_splits * D + threadIdx.x, ns));
 }
 
 // ---- many short lanes per CTA ---------------------------------------------------
