@@ -85,9 +85,9 @@ def parse():
     p.add_argument("--graph", action="store_true",
                    help="decode workloads: lengths kept on the device, each bench step's decode calls "
                         "captured once in a CUDA graph and replayed")
-    p.add_argument("--suffix-kernel", type=int, default=0, choices=[0, 1, 2, 3, 4],
+    p.add_argument("--suffix-kernel", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
                    help="suffix: 0 = the library's choice, 1 = generic, 2 = one-SM tile kernel, 3 = pair-of-SMs "
-                        "tile kernel, 4 = persistent tile kernel")
+                        "tile kernel, 4 = persistent tile kernel, 5 = tile kernel with two softmax threads per query row")
     p.add_argument("--host-chunk", type=int, default=0,
                    help="suffix e2e: sequences per stage of the host-buffer call; 0 = the library's choice")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -434,7 +434,8 @@ typedef enum kvc_option {
     KVC_OPT_FORCE_GENERIC = 2,     /* 1 = use the dtype-generic CUDA-core kernels even for bf16, d_h = 128 */
     KVC_OPT_SUFFIX_KERNEL = 3,     /* 0 = automatic, 1 = generic, 2 = tensor-core tile kernel, 3 = the tile
                                       kernel on pairs of SMs, 4 = the persistent tile kernel (one CTA per
-                                      SM walking the work items; 3 and 4 need contiguous storage, else 2) */
+                                      SM walking the work items; 3 and 4 need contiguous storage, else 2),
+                                      5 = the tile kernel with two softmax threads per query row */
     KVC_OPT_TIMING = 4,            /* 1 = record a CUDA event pair around every kernel launch */
     KVC_OPT_DECODE_FUSED = 5,      /* 1 (default) = bf16 decode steps with B <= 256 append, attend and
                                       commit in one launch (plus a merge launch when H_q / H_kv > 16);

@@ -1200,7 +1200,9 @@ kvc_status prefill_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q, const
             const int sms = sm_count(h->cfg.device);
             KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tcp(sl, sms, s); }));
         } else {
-            KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s, [&] { return launch_suffix_tc(sl, (int)work.size(), s); }));
+            const int split = h->opt_suffix_kernel == 5 ? 2 : 1;
+            KVC_CUDA(h, timed(h, KVC_KERNEL_SUFFIX, s,
+                              [&] { return launch_suffix_tc(sl, (int)work.size(), s, split); }));
         }
     } else if (out && !use_tc) {
         GenericAttendLaunch g{};
@@ -1843,7 +1845,7 @@ kvc_status kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
             h->opt_force_generic = value != 0;
             return KVC_OK;
         case KVC_OPT_SUFFIX_KERNEL:
-            if (value < 0 || value > 4) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0, 1, 2, 3 or 4");
+            if (value < 0 || value > 5) return fail(h, KVC_ERR_CONFIG, "suffix kernel must be 0 .. 5");
             h->opt_suffix_kernel = value;
             return KVC_OK;
         case KVC_OPT_TIMING:

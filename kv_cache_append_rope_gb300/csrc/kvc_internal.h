@@ -340,7 +340,8 @@ struct SuffixLaunch {
     KvLayout kv;                 // paged: K/V tiles load as two 64-row boxes (tmK/tmV 64-row maps)
     float scale_log2;            // log2(e) / sqrt(d_h)
 };
-cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s);
+// split: softmax threads per query row (1 or 2)
+cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s, int split);
 // Persistent form: one CTA per SM (at most n_work) walks the work list round robin;
 // contiguous storage only.
 cudaError_t launch_suffix_tcp(const SuffixLaunch& a, int sms, cudaStream_t s);

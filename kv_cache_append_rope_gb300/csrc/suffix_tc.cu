@@ -67,15 +67,35 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + QT * TILE;
 constexpr int OFF_V = OFF_K + KST * TILE;
 constexpr int OFF_BAR = OFF_V + VST * TILE;
-constexpr int SMEM_BYTES = OFF_BAR + 4096 + 1024;
-constexpr int NSW = 4 * QT;                // softmax warps: one per TMEM sub-partition per query tile
-constexpr int THREADS = (4 + NSW) * 32;    // warpgroup 0: producer, MMA issuer, 2 idle; 1-2: softmax
-// Registers: three warps per SM sub-partition cap a thread at 168 at launch; warpgroup 0
-// then gives registers back so that the softmax warpgroups can hold a whole 128-column
-// row of S.  The split must add up to the launch allocation exactly (checked on the host
-// against the built kernel's register count before the first launch).
-constexpr int kLaunchRegs = 168, kRegsLow = 120, kRegsHigh = 192;
-static_assert(128 * kRegsLow + 2 * 128 * kRegsHigh == THREADS * kLaunchRegs, "register split");
+// split rows: the partners' row maxima (two buffers), wait verdicts (two buffers), row sums
+constexpr int OFF_XCH = OFF_BAR + 4096;
+constexpr int XCH_MAX = 0, XCH_FLAG = QT * 2 * 2 * 128 * 4, XCH_SUM = XCH_FLAG + QT * 2 * 4 * 2 * 4;
+constexpr int XCH_BYTES = XCH_SUM + QT * 2 * 128 * 4;
+// SPLIT softmax threads share one query row, each owning BN / SPLIT of its key columns
+// (and D / SPLIT of its output columns).  SPLIT = 1: one thread per row, the whole
+// 128-column row of S in its registers.  SPLIT = 2: two warpgroups per query tile halve
+// the work on the softmax's critical path per key tile; the partners exchange their
+// halves' row maxima through shared memory once per tile.
+// Registers: the warps per SM sub-partition cap a thread at kLaunchRegs at launch;
+// warpgroup 0 then gives registers back to the softmax warpgroups.  The split must add up
+// to the launch allocation exactly (checked on the host against the built kernel's
+// register count before the first launch).
+template <int SPLIT> struct TileCfg;
+template <> struct TileCfg<1> {
+    static constexpr int kLaunchRegs = 168, kRegsLow = 120, kRegsHigh = 192;
+};
+template <> struct TileCfg<2> {
+    static constexpr int kLaunchRegs = 96, kRegsLow = 64, kRegsHigh = 104;
+};
+template <int SPLIT> constexpr int kSoftmaxWarps = 4 * QT * SPLIT;   // one per TMEM sub-partition, tile, part
+template <int SPLIT> constexpr int kThreads = (4 + kSoftmaxWarps<SPLIT>) * 32;  // + producer, MMA, 2 idle
+template <int SPLIT> constexpr int kSmemBytes = OFF_XCH + (SPLIT > 1 ? XCH_BYTES : 0) + 1024;
+static_assert(128 * TileCfg<1>::kRegsLow + 2 * 128 * TileCfg<1>::kRegsHigh == kThreads<1> * TileCfg<1>::kLaunchRegs,
+              "register split");
+static_assert(128 * TileCfg<2>::kRegsLow + 4 * 128 * TileCfg<2>::kRegsHigh == kThreads<2> * TileCfg<2>::kLaunchRegs,
+              "register split");
+// the epilogue stages 4 KB per softmax warp in the query tiles' shared memory
+static_assert(kSoftmaxWarps<2> * 4096 <= QT * TILE, "epilogue staging");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256; // S_X at 128 X, O_X at 256 + 128 X
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -129,7 +149,9 @@ __device__ __forceinline__ void tile_range(int qt, int cut, int rows, int window
     hi = (cut + q_end - 1) / BN + 1;
 }
 
-__global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_constant__ SuffixLaunch a) {
+template <int SPLIT>
+__global__ void __launch_bounds__(kThreads<SPLIT>, 1) suffix_tc_kernel(const __grid_constant__ SuffixLaunch a) {
+    using Cfg = TileCfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Bars* bars = (Bars*)(smem + OFF_BAR);
@@ -163,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         }
         for (int X = 0; X < QT; ++X) {
             mbar_init(smem_u32(&bars->s_full[X]), 1);
-            mbar_init(smem_u32(&bars->p_full[X]), 4);
+            mbar_init(smem_u32(&bars->p_full[X]), 4 * SPLIT);
         }
         mbar_init(smem_u32(&bars->o_done), 1);
         bars->err = 0;
@@ -186,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     if (warp < 4) {
-    setmaxnreg_dec<kRegsLow>();
+    setmaxnreg_dec<Cfg::kRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // lane 0 streams both Q tiles and the K ring, lane 1 the V ring, so that the
@@ -321,11 +343,15 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         }
     }
     } else {
-        setmaxnreg_inc<kRegsHigh>();
+        setmaxnreg_inc<Cfg::kRegsHigh>();
         // ------------------------------------------------------------ softmax warps
-        // Warps 4-7 take query tile A, 8-11 tile B; warp w reads TMEM lanes
-        // 32 * (w % 4) .. + 31, one query row per thread.
-        const int X = (warp - 4) >> 2;
+        // Query tile X has 4 * SPLIT warps; warp w reads TMEM lanes 32 * (w % 4) .. + 31, one
+        // query row per thread, and part `half` of the row's key (and output) columns.
+        constexpr int CW = BN / SPLIT;               // key columns per thread
+        constexpr int OW = D / SPLIT;                // output columns per thread
+        const int wi = warp - 4;
+        const int X = wi / (4 * SPLIT);
+        const int half = (wi >> 2) % SPLIT;
         const int sub = warp & 3;
         const int row = sub * 32 + lane;             // query row inside the tile = TMEM lane
         const int qt = QT * qp + X;
@@ -333,15 +359,25 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
         const int qslot = cut + i;
         const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
         const uint32_t s_addr = lane_addr + COL_S + X * 128;
-        const uint32_t o_addr = lane_addr + COL_O + X * 128;
+        const uint32_t sx_addr = s_addr + half * CW;         // this thread's columns of S
+        const uint32_t p_addr = s_addr + half * (CW / 2);    // its packed bf16 columns of P
+        const uint32_t o_addr = lane_addr + COL_O + X * 128 + half * OW;
         const float sl2 = a.scale_log2;
         const int tile_slot0 = cut + qt * BM;        // slot of the tile's first row
         auto kbase_of = [](int jj) { return jj * BN; };
+        // SPLIT = 2: per (query tile, part) double-buffered row maxima, per warp wait verdicts
+        float* xm = reinterpret_cast<float*>(smem + OFF_XCH + XCH_MAX);
+        int* xf = reinterpret_cast<int*>(smem + OFF_XCH + XCH_FLAG);
+        float* xs = reinterpret_cast<float*>(smem + OFF_XCH + XCH_SUM);
+        const int pair_bar = 1 + X * 4 + sub;        // named barrier of the two partner warps
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int c = 0;
         for (int jj = jlo[X]; jj < jhi[X]; ++jj, ++c) {
-            if (!warp_wait(smem_u32(&bars->s_full[X]), c & 1, a.err)) {
+            const bool okw = warp_wait(smem_u32(&bars->s_full[X]), c & 1, a.err);
+            // SPLIT = 1 leaves at once; partners first agree on the verdict (below), so that
+            // both leave at the same tile and neither waits at the named barrier alone
+            if (SPLIT == 1 && !okw) {
                 ok = false;
                 break;
             }
@@ -352,31 +388,51 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
             // unmasked tiles (nearly all) carry no masking instructions.
             const bool masked =
                 kbase_of(jj) + BN - 1 > tile_slot0 || (a.window > 0 && kbase_of(jj) < tile_slot0 + BM - a.window);
-            auto tile = [&](auto mask_c) {
-                // The whole 128-column row is read with one wait, then reduced to its
-                // maximum, then turned into exponentials in place.
-                float x[BN];
-                tmem_ld128(s_addr, x);
-                tmem_wait_ld();
+            auto tile = [&](auto mask_c) -> bool {
+                // The thread's columns of the row are read with one wait, then reduced to
+                // their maximum, then turned into exponentials in place.
+                float x[CW];
+                if (SPLIT == 1 || okw) {
+                    if constexpr (CW == 128)
+                        tmem_ld128(sx_addr, x);
+                    else
+                        tmem_ld64(sx_addr, x);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < CW; ++e) x[e] = 0.f;   // not used: the partners leave below
+                }
                 if constexpr (decltype(mask_c)::value) {
-                    const int kb = jj * BN;
+                    const int kb = jj * BN + half * CW;
                     const int klo = a.window > 0 ? qslot - a.window + 1 : 0;
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
+                    for (int e = 0; e < CW; ++e) x[e] = (kb + e > qslot || kb + e < klo) ? -INFINITY : x[e];
                 }
-                // row maximum (8 independent chains of 3-input maxima)
+                // maximum (8 independent chains of 3-input maxima)
                 float m8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) m8[q] = fmax3(x[q], x[8 + q], x[16 + q]);
 #pragma unroll
-                for (int e = 24; e + 16 <= BN; e += 16)
+                for (int e = 24; e + 16 <= CW; e += 16)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], x[e + q], x[e + 8 + q]);
-                m8[0] = fmax3(m8[0], x[120], x[121]);
-                m8[1] = fmax3(m8[1], x[122], x[123]);
-                m8[2] = fmax3(m8[2], x[124], x[125]);
-                m8[3] = fmax3(m8[3], x[126], x[127]);
-                const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) m8[q] = fmax3(m8[q], x[CW - 8 + 2 * q], x[CW - 7 + 2 * q]);
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                if constexpr (SPLIT == 2) {
+                    // the partner's maximum of the other half of the row (both partners have
+                    // read their columns of S before either overwrites any with P)
+                    const int buf = c & 1;
+                    xm[((X * 2 + half) * 2 + buf) * 128 + row] = mx;
+                    if (lane == 0) xf[((X * 2 + half) * 4 + sub) * 2 + buf] = okw;
+                    tc_fence_before();
+                    named_bar_sync(pair_bar, 64);
+                    tc_fence_after();
+                    const float mp = xm[((X * 2 + (half ^ 1)) * 2 + buf) * 128 + row];
+                    const int okp = xf[((X * 2 + (half ^ 1)) * 4 + sub) * 2 + buf];
+                    if (!okw || !okp) return false;
+                    mx = fmaxf(mx, mp);
+                }
                 const float m_tile = mx * sl2;
                 const bool grow = m_tile > m_run + RESCALE_LOG2 || c == 0;
                 const float m_new = grow ? fmaxf(m_run, m_tile) : m_run;
@@ -385,32 +441,39 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 // (.sync.aligned), so the whole warp rescales when any of its rows must, the
                 // other rows by 1.
                 const bool rescale = grow && c > 0 && m_run > -INFINITY;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float corr = rescale ? fast_exp2(m_run - m_new) : 1.0f;
-                    l_run *= corr;
+                const float m_old = m_run;
+                auto rescale_o = [&] {
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        const float corr = rescale ? fast_exp2(m_old - m_new) : 1.0f;
+                        l_run *= corr;
 #pragma unroll 1
-                    for (int q = 0; q < D / 32; ++q) {
-                        float o[32];
-                        tmem_ld32(o_addr + q * 32, o);
-                        tmem_wait_ld();
+                        for (int q = 0; q < OW / 32; ++q) {
+                            float o[32];
+                            tmem_ld32(o_addr + q * 32, o);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= corr;
-                        tmem_st32(o_addr + q * 32, o);
+                            for (int e = 0; e < 32; ++e) o[e] *= corr;
+                            tmem_st32(o_addr + q * 32, o);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
-                }
+                };
+                // SPLIT = 2 rescales after the exponentials, when the row's S values no longer
+                // occupy registers (only the arrive on p_full must follow it)
+                if constexpr (SPLIT == 1) rescale_o();
                 m_run = m_new;
                 const float mu = m_run == -INFINITY ? 0.f : m_run;
-                // P = exp2(x * scale - max), packed to bf16 pairs into columns 0 .. 63 of S_X
-                // (all of S is in registers already); packed float32x2 arithmetic, since the
-                // softmax warps issue most of the kernel's instructions.
+                // P = exp2(x * scale - max), packed to bf16 pairs into the thread's P columns
+                // (its S columns are in registers already; SPLIT = 2: part 1's P columns are
+                // part 0's S columns, read before the named barrier); packed float32x2
+                // arithmetic, since the softmax warps issue most of the kernel's instructions.
                 float2 l4[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
                 const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
-                uint32_t pk[BN / 2];
+                uint32_t pk[CW / 2];
 #pragma unroll
-                for (int e = 0; e < BN / 2; ++e) {
+                for (int e = 0; e < CW / 2; ++e) {
                     const int c2 = 2 * e;
                     const float2 arg = __ffma2_rn(make_float2(x[c2], x[c2 + 1]), sl2v, negmu);
                     const float p0 = fast_exp2(arg.x);
@@ -418,18 +481,33 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                     l4[e & 3] = __fadd2_rn(l4[e & 3], make_float2(p0, p1));
                     pk[e] = pack_bf16(p0, p1);
                 }
-                tmem_st64u(s_addr, pk);
+                if constexpr (CW == 128)
+                    tmem_st64u(p_addr, pk);
+                else
+                    tmem_st32u(p_addr, pk);
                 l4[0] = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+                if constexpr (SPLIT == 2) rescale_o();
                 l_run += l4[0].x + l4[0].y;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[X]));
+                return true;
             };
-            if (masked)
-                tile(std::true_type{});
-            else
-                tile(std::false_type{});
+            const bool good = masked ? tile(std::true_type{}) : tile(std::false_type{});
+            if (!good) {
+                ok = false;
+                break;
+            }
+        }
+        if constexpr (SPLIT == 2) {
+            // the row sum is the partners' two partial sums (taken before any further wait, so
+            // that both partners reach this barrier: they left the loop at the same tile)
+            if (ok && c > 0) {
+                xs[(X * 2 + half) * 128 + row] = l_run;
+                named_bar_sync(pair_bar, 64);
+                l_run += xs[(X * 2 + (half ^ 1)) * 128 + row];
+            }
         }
         if (ok && c > 0) {
             if (!warp_wait(smem_u32(&bars->o_done), 0, a.err)) {
@@ -442,11 +520,11 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
                 // 4 rows x 128 bytes per instruction -- whole lines instead of 32 scattered
                 // 16-byte pieces.  16-byte slots are XOR-swizzled by row (mod 8), so both
                 // sides take the minimum of 4 shared-memory wavefronts per instruction.
-                float4* stage = reinterpret_cast<float4*>(smem + OFF_Q) + (warp - 4) * 256;
+                float4* stage = reinterpret_cast<float4*>(smem + OFF_Q) + wi * 256;
                 const int row0 = qt * BM + sub * 32;             // query row of lane 0
-                float* obase = a.out + (((int64_t)b * a.Hq + h) * a.S) * D;
+                float* obase = a.out + (((int64_t)b * a.Hq + h) * a.S) * D + half * OW;
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = 0; q < OW / 32; ++q) {
                     float o[32];
                     tmem_ld32(o_addr + q * 32, o);
                     tmem_wait_ld();
@@ -479,20 +557,29 @@ __global__ void __launch_bounds__(THREADS, 1) suffix_tc_kernel(const __grid_cons
 
 int suffix_tc_grid(int sms) { return sms; }
 
-cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s) {
+namespace {
+
+template <int SPLIT> cudaError_t launch_tile(const SuffixLaunch& a, int grid, cudaStream_t s) {
     static PerDeviceOnce attr;
     cudaError_t e = attr.run([] {
         // the register split assumes the launch allocation it was computed for
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, suffix_tc_kernel);
+        cudaError_t r = cudaFuncGetAttributes(&fa, suffix_tc_kernel<SPLIT>);
         if (r != cudaSuccess) return r;
-        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(suffix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (fa.numRegs != TileCfg<SPLIT>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+        return cudaFuncSetAttribute(suffix_tc_kernel<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBytes<SPLIT>);
     });
     if (e != cudaSuccess) return e;
     if (grid <= 0) return cudaSuccess;
-    suffix_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a);
+    suffix_tc_kernel<SPLIT><<<grid, kThreads<SPLIT>, kSmemBytes<SPLIT>, s>>>(a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s, int split) {
+    return split == 2 ? launch_tile<2>(a, grid, s) : launch_tile<1>(a, grid, s);
 }
 
 }  // namespace kvc

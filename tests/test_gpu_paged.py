@@ -89,7 +89,7 @@ def test_paged_decode_matches_oracle(dtype, D, Hq, Hkv, P, mode, window):
 
 @pytest.mark.parametrize("dtype,D,kernel,P,window", [
     ("bf16", 128, 2, 64, 0), ("bf16", 128, 2, 128, 0), ("bf16", 128, 2, 64, 300), ("bf16", 128, 1, 64, 0),
-    ("f32", 64, 1, 64, 0),
+    ("f32", 64, 1, 64, 0), ("bf16", 128, 5, 64, 0), ("bf16", 128, 5, 64, 300),
 ])
 def test_paged_suffix_chunk_matches_full_recompute(dtype, D, kernel, P, window):
     need_gpu()

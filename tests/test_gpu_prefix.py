@@ -38,6 +38,9 @@ def make_inputs(B, Hq, Hkv, T, D, dtype, seed):
     ("bf16", 128, 4, 4, 4, 300, [150, 0, 257]),      # persistent tile kernel, one item per CTA
     ("bf16", 128, 2, 1, 4, 1500, [1200, 37, 640]),
     ("bf16", 128, 32, 8, 4, 1500, [1200, 37, 640]),  # persistent: 384 items, several per CTA
+    ("bf16", 128, 4, 4, 5, 300, [150, 0, 257]),      # tile kernel, two softmax threads per query row
+    ("bf16", 128, 8, 2, 5, 300, [150, 0, 257]),
+    ("bf16", 128, 2, 1, 5, 1500, [1200, 37, 640]),
 ])
 def test_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, T, cuts):
     need_gpu()

@@ -90,6 +90,9 @@ def test_windowed_decode_matches_oracle(dtype, D, Hq, Hkv, mode, window):
     ("bf16", 128, 2, 1, 3, 700),
     ("bf16", 128, 4, 2, 4, 100),      # persistent tile kernel
     ("bf16", 128, 32, 8, 4, 700),     # persistent, several items per CTA
+    ("bf16", 128, 4, 2, 5, 100),      # two softmax threads per query row
+    ("bf16", 128, 4, 4, 5, 1),
+    ("bf16", 128, 2, 1, 5, 700),
 ])
 def test_windowed_suffix_chunk_matches_full_recompute(dtype, D, Hq, Hkv, kernel, window):
     need_gpu()
