@@ -60,11 +60,11 @@ METRIC = "decode-attention KV GB/s & %HBM peak; suffix-chunk TFLOP/s; steps/s"
 # (ratio to the algorithmic bytes), the tile kernel's with the number of
 # sequences (each sequence's K/V comes from DRAM about once, then from L2).
 TRAFFIC = {
-    "mha_decode": ("ratio", 1.013),
-    "gqa_decode": ("ratio", 1.0067),
-    "mqa_decode": ("ratio", 1.0071),
-    "mha_decode_short": ("ratio", 1.073),
-    "suffix": ("per_sequence", 375812608.0 + 175133952.0),
+    "mha_decode": ("ratio", 1.0126),
+    "gqa_decode": ("ratio", 1.0062),
+    "mqa_decode": ("ratio", 1.012),
+    "mha_decode_short": ("ratio", 1.0579),
+    "suffix": ("per_sequence", 375510016.0 + 175409664.0),
 }
 
 
