@@ -863,6 +863,12 @@ kvc_status append_attend_impl(kvc_handle* h, int32_t layer, const kvc_tensor* q,
             int64_t r = (keys + target - 1) / target;
             r = std::max<int64_t>(r, std::min<int64_t>(256 * G, keys / sm_count(h->cfg.device)));
             r = (r + 63) / 64 * 64;
+            // at most 4096 rows, in multiples of 512 from 1024 up: B = 64, H_kv = 8, 16-32K
+            // contexts ran 1.5% faster with 4096-row splits than with the 10816 the wave
+            // count alone gives (more, shorter CTAs drain more evenly), B = 32, H = 32, up to
+            // 8K 0.4% faster with 3072 rows than with 3200
+            r = std::min<int64_t>(r, 4096);
+            if (r >= 1024) r = r / 512 * 512;
             r = std::min<int64_t>(r, ((int64_t)max_t + 63) / 64 * 64);
             split_rows = (int)r;
         }
