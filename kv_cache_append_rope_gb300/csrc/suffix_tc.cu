@@ -22,7 +22,7 @@
 // cut + i) attends key slots 0 .. cut + i; key tiles are 128 slots, the
 // diagonal ones masked element-wise.
 //
-// Warp roles (384 threads, three warpgroups):
+// Warp roles (SPLIT = 1: 384 threads, three warpgroups):
 //   warp 0    TMA producers (128-byte swizzle, no multicast): lane 0 both Q
 //             tiles once and K tiles into a 2-stage ring, lane 1 V tiles into
 //             a 2-stage ring.
@@ -44,6 +44,12 @@
 //             only when the max grows by more than 2^8 (the final division by
 //             the running sum makes the stale max exact), P written with
 //             tcgen05.st, then the normalised O row stored to global memory.
+// The SPLIT = 2 form (640 threads) gives each query tile two softmax warpgroups:
+// warps 4-7 and 8-11 take the two 64-key halves of tile A's rows, warps 12-15 and
+// 16-19 those of tile B.  The two warps of one TMEM lane quarter exchange their
+// halves' row maxima (and their wait verdicts) through shared memory at a 64-thread
+// named barrier per key tile and add their partial row sums at the end; part 1 writes
+// its P columns (part 0's S columns) only after that barrier.
 // Every mbarrier wait is bounded (DEV_ERR_WAIT_TIMEOUT); the MMA thread waits
 // for its own last commit and the TMA thread for its own copies before the
 // allocator warp frees the tensor memory.
