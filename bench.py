@@ -500,7 +500,7 @@ class SuffixBench:
         return tasks, work, desc
 
 
-# ----------------------------------------------------------------- driver
+# ----------------------------------------------------------------- main
 
 def make_bench(name, device, batch=0, graph=False, block_rows=0, with_cache=True):
     if name == "suffix":

@@ -342,8 +342,8 @@ struct SuffixLaunch {
 };
 // split: softmax threads per query row (1 or 2)
 cudaError_t launch_suffix_tc(const SuffixLaunch& a, int grid, cudaStream_t s, int split);
-// Persistent form: one CTA per SM (at most n_work) walks the work list round robin;
-// contiguous storage only.
+// Persistent form: one CTA per SM (at most n_work) takes work items in list order through
+// a global counter (zeroed before the launch); contiguous storage only.
 cudaError_t launch_suffix_tcp(const SuffixLaunch& a, int sms, cudaStream_t s);
 
 // Pair-of-SMs tile kernel (cta_group::2): a cluster of two CTAs per work item.
